@@ -1,0 +1,263 @@
+"""Pins for the CPU oracle: values the pages print, hand-worked examples,
+closed forms, invariants and library routines (CPU only, no GPU).
+
+Each test would fail under a plausible slip in the oracle: a wrong shift
+table or word index, a dropped zero-point or scale, a wrong sign or group
+index, a transposed operand.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4synth
+from conftest import golden_kv, golden_lines
+
+LAYOUTS = [oracle.KN_SEQ, oracle.NK_SEQ, oracle.NK_EXLLAMA]
+
+
+def _word_array(words_hex, layout):
+    w = np.array([np.uint32(int(h, 16)).view(np.int32) for h in words_hex], dtype=np.int32)
+    # K=8, N=len(words): KN_SEQ is [1, N], NK layouts are [N, 1]
+    return w.reshape(1, -1) if layout == oracle.KN_SEQ else w.reshape(-1, 1)
+
+
+# ---------------------------------------------------------------- packing ---
+
+def test_exllama_words_match_page_formula():
+    rows = golden_lines("exllama_pack.txt")
+    q = np.array([[int(x) for x in r[:8]] for r in rows], dtype=np.uint8).T  # [8, N]
+    w = oracle.pack(q, oracle.NK_EXLLAMA)
+    expect = _word_array([r[8] for r in rows], oracle.NK_EXLLAMA)
+    assert np.array_equal(w, expect)
+    assert np.array_equal(oracle.unpack(expect, oracle.NK_EXLLAMA, 8, q.shape[1]), q)
+
+
+def test_exllama_shift_table():
+    shifts = [int(x) for x in golden_lines("exllama_shifts.txt")[0]]
+    for j, sh in enumerate(shifts):
+        for v in range(16):
+            word = np.array([[np.uint32(v << sh).view(np.int32)]], dtype=np.int32)
+            q = oracle.unpack(word, oracle.NK_EXLLAMA, 8, 1)[:, 0]
+            expect = np.zeros(8, np.uint8)
+            expect[j] = v
+            assert np.array_equal(q, expect), (j, v)
+
+
+def test_sequential_words():
+    rows = golden_lines("sequential_pack.txt")
+    q = np.array([[int(x) for x in r[:8]] for r in rows], dtype=np.uint8).T
+    for layout in (oracle.KN_SEQ, oracle.NK_SEQ):
+        expect = _word_array([r[8] for r in rows], layout)
+        assert np.array_equal(oracle.pack(q, layout), expect)
+        assert np.array_equal(oracle.unpack(expect, layout, 8, q.shape[1]), q)
+
+
+def test_kn_and_nk_are_transposes():
+    rng = np.random.default_rng(1)
+    q = rng.integers(0, 16, size=(64, 24), dtype=np.uint8)
+    assert np.array_equal(oracle.pack(q, oracle.KN_SEQ), oracle.pack(q, oracle.NK_SEQ).T)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_pack_unpack_round_trip(layout):
+    rng = np.random.default_rng(layout)
+    K, N = 96, 40
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    w = oracle.pack(q, layout)
+    assert np.array_equal(oracle.unpack(w, layout, K, N), q)
+    words = w4synth.random_words(w4synth.packed_shape(layout, K, N), torch.Generator().manual_seed(3))
+    assert np.array_equal(oracle.pack(oracle.unpack(words, layout, K, N), layout), words.numpy())
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_every_nibble_in_every_position(layout):
+    # brute force over one word: each of the 8 positions x 16 values
+    for j in range(8):
+        for v in range(16):
+            q = np.zeros((8, 1), np.uint8)
+            q[j, 0] = v
+            w = oracle.pack(q, layout)
+            assert oracle.nibble(w, layout, 8, 1, j, 0) == v
+            assert sum(oracle.nibble(w, layout, 8, 1, k, 0) for k in range(8)) == v
+
+
+def test_value_table():
+    for r in golden_lines("values.txt"):
+        q, b8, u4, i4 = (int(x) for x in r)
+        assert oracle.value(q, oracle.UINT4B8) == b8
+        assert oracle.value(q, oracle.UINT4) == u4
+        assert oracle.value(q, oracle.INT4) == i4
+
+
+# ----------------------------------------------------------------- W4A16 ---
+
+def _one_col(q_list, layout=oracle.NK_EXLLAMA):
+    q = np.array(q_list, dtype=np.uint8).reshape(8, 1)
+    return oracle.pack(q, layout)
+
+
+def test_w4a16_worked_example():
+    g = golden_kv("worked_examples.txt")
+    a = np.array([[float(x) for x in g["w4a16_a"]]])
+    for layout in LAYOUTS:
+        w = _one_col([int(x) for x in g["w4a16_q"]], layout)
+        s = np.array([[float(g["w4a16_s"][0])]])
+        ref, absref = oracle.w4a16(a, w, layout, oracle.UINT4B8, s, None, -1, 8, 1)
+        assert ref[0, 0] == float(g["w4a16_ref"][0])
+        assert absref[0, 0] == float(g["w4a16_absref"][0])
+        z = np.array([[float(g["w4a16_z_uint4"][0])]])
+        ref2, _ = oracle.w4a16(a, w, layout, oracle.UINT4, s, z, -1, 8, 1)
+        assert ref2[0, 0] == float(g["w4a16_ref"][0])
+
+
+def _pow2_problem(M, N, K, gs, seed, zeros):
+    """Inputs whose every product and sum is exact in fp64: fp16 activations,
+    power-of-two scales, power-of-two-multiple zero-points."""
+    rng = np.random.default_rng(seed)
+    G = K // gs
+    a = torch.randn(M, K, generator=torch.Generator().manual_seed(seed)).to(torch.float16)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    s = (2.0 ** rng.integers(-8, -3, size=(G, N))).astype(np.float64)
+    z = (rng.integers(0, 16, size=(G, N)) * s).astype(np.float64) if zeros else None
+    return a, q, s, z
+
+
+@pytest.mark.parametrize("wtype", [oracle.UINT4B8, oracle.UINT4])
+@pytest.mark.parametrize("zeros", [False, True])
+def test_w4a16_equals_blockwise_library_matmul(wtype, zeros):
+    M, N, K, gs = 5, 24, 256, 64
+    a, q, s, z = _pow2_problem(M, N, K, gs, 7 + wtype, zeros)
+    w = oracle.pack(q, oracle.KN_SEQ)
+    ref, _ = oracle.w4a16(a, w, oracle.KN_SEQ, wtype, s, z, gs, K, N)
+    v = q.astype(np.float64) - (8.0 if wtype == oracle.UINT4B8 else 0.0)
+    a64 = a.to(torch.float64).numpy()
+    expect = np.zeros((M, N))
+    for gi in range(K // gs):
+        blk = slice(gi * gs, (gi + 1) * gs)
+        what = v[blk] * s[gi][None, :] - (z[gi][None, :] if zeros else 0.0)
+        expect += a64[:, blk] @ what
+    assert np.array_equal(ref, expect)
+
+
+def test_w4a16_unit_scale_is_plain_matmul():
+    M, N, K = 3, 17, 64
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    a = torch.randn(M, K, generator=torch.Generator().manual_seed(5)).to(torch.float16)
+    w = oracle.pack(q, oracle.NK_SEQ)
+    ref, _ = oracle.w4a16(a, w, oracle.NK_SEQ, oracle.UINT4, np.ones((1, N)), None, -1, K, N)
+    assert np.array_equal(ref, a.to(torch.float64).numpy() @ q.astype(np.float64))
+
+
+def test_w4a16_one_hot_rows_give_dequantized_weights():
+    M, N, K, gs = 8, 16, 128, 32
+    a, q, s, z = _pow2_problem(M, N, K, gs, 11, True)
+    a = torch.zeros(K, K, dtype=torch.float16)
+    a[torch.arange(K), torch.arange(K)] = 1.0
+    w = oracle.pack(q, oracle.NK_EXLLAMA)
+    ref, _ = oracle.w4a16(a, w, oracle.NK_EXLLAMA, oracle.UINT4, s, z, gs, K, N)
+    # row k of the product is w_hat[k, :]; check against the scale/zero of k's group
+    for k in (0, 31, 32, 100, 127):
+        gi = k // gs
+        assert np.array_equal(ref[k], q[k].astype(np.float64) * s[gi] - z[gi])
+
+
+def test_w4a16_invariants():
+    M, N, K = 4, 32, 256
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=oracle.UINT4,
+                          layout=oracle.NK_EXLLAMA, group_size=128, zeros=True, seed=2)
+    args = (d["w"], d["layout"])
+    # zero-points that are all zero equal no zero-points
+    r0, _ = oracle.w4a16(d["a"], *args, oracle.UINT4, d["s"], torch.zeros_like(d["z"]), 128, K, N)
+    r1, _ = oracle.w4a16(d["a"], *args, oracle.UINT4, d["s"], None, 128, K, N)
+    assert np.array_equal(r0, r1)
+    # uint4 with w_z = 8*s equals uint4b8 (exact: 8*s is a power-of-two multiple)
+    r2, _ = oracle.w4a16(d["a"], *args, oracle.UINT4, d["s"], d["s"].double() * 8, 128, K, N)
+    r3, _ = oracle.w4a16(d["a"], *args, oracle.UINT4B8, d["s"], None, 128, K, N)
+    assert np.allclose(r2, r3, rtol=0, atol=1e-12)
+    # group_size = K equals per-channel with the one scale row broadcast
+    s1 = d["s"][:1]
+    r4, _ = oracle.w4a16(d["a"], *args, oracle.UINT4B8, s1.repeat(2, 1), None, 128, K, N)
+    r5, _ = oracle.w4a16(d["a"], *args, oracle.UINT4B8, s1, None, -1, K, N)
+    assert np.array_equal(r4, r5)
+    # rows are independent: M=1 (a GEMV) equals the matching row of the batch
+    full, absfull = oracle.w4a16(d["a"], *args, oracle.UINT4, d["s"], d["z"], 128, K, N)
+    for m in range(M):
+        row, _ = oracle.w4a16(d["a"][m:m + 1], *args, oracle.UINT4, d["s"], d["z"], 128, K, N)
+        assert np.array_equal(row[0], full[m])
+    # |ref| <= sum|terms|, and linear in a
+    assert np.all(np.abs(full) <= absfull + 1e-12)
+    a2 = (d["a"].double() * 2).to(torch.bfloat16)  # exact doubling
+    r6, _ = oracle.w4a16(a2, *args, oracle.UINT4, d["s"], d["z"], 128, K, N)
+    assert np.array_equal(r6, 2 * full)
+    # sampled elements equal the full product at those positions
+    rows = np.array([0, 3, 1, 2]); cols = np.array([0, 31, 7, 16])
+    e, ea = oracle.w4a16_elems(d["a"], *args, oracle.UINT4, d["s"], d["z"], 128, K, N, rows, cols)
+    assert np.array_equal(e, full[rows, cols]) and np.array_equal(ea, absfull[rows, cols])
+
+
+def test_w4a16_layouts_agree():
+    M, N, K = 3, 24, 128
+    rng = np.random.default_rng(9)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    a = torch.randn(M, K, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    s = torch.rand(1, N, generator=torch.Generator().manual_seed(10)).to(torch.bfloat16)
+    outs = [oracle.w4a16(a, oracle.pack(q, L), L, oracle.UINT4B8, s, None, -1, K, N)[0]
+            for L in LAYOUTS]
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+# ------------------------------------------------------------------ W4A8 ---
+
+def test_w4a8_worked_example():
+    g = golden_kv("worked_examples.txt")
+    a = np.array([[int(x) for x in g["w4a8_a"]]], dtype=np.int8)
+    for layout in LAYOUTS:
+        w = _one_col([int(x) for x in g["w4a8_q"]], layout)
+        acc = oracle.w4a8(a, w, layout, oracle.INT4, None, -1, 8, 1)
+        assert acc[0, 0] == int(g["w4a8_acc_channel"][0])
+        sg = np.array([[int(x)] for x in g["w4a8_sg"]], dtype=np.int8)  # [G=2, N=1]
+        acc2 = oracle.w4a8(a, w, layout, oracle.INT4, sg, 4, 8, 1)
+        assert acc2[0, 0] == int(g["w4a8_acc_g4"][0])
+
+
+def test_w4a8_equals_integer_matmul():
+    M, N, K = 6, 40, 512
+    d = w4synth.gen_w4a8(M, N, K, group_size=128, seed=4)
+    q = oracle.unpack(d["w"], d["layout"], K, N).astype(np.int64)
+    v = np.where(q >= 8, q - 16, q)
+    a = d["a"].numpy().astype(np.int64)
+    acc = oracle.w4a8(d["a"], d["w"], d["layout"], oracle.INT4, None, -1, K, N)
+    assert np.array_equal(acc, a @ v)
+    sg = d["sg"].numpy().astype(np.int64)
+    accg = oracle.w4a8(d["a"], d["w"], d["layout"], oracle.INT4, d["sg"], 128, K, N)
+    assert np.array_equal(accg, a @ (v * np.repeat(sg, 128, axis=0)))
+    # unit group scales equal per-channel; constant group scale c multiplies by c
+    ones = torch.ones_like(d["sg"])
+    assert np.array_equal(oracle.w4a8(d["a"], d["w"], d["layout"], oracle.INT4, ones, 128, K, N), acc)
+    assert np.array_equal(oracle.w4a8(d["a"], d["w"], d["layout"], oracle.INT4, ones * 5, 128, K, N), 5 * acc)
+    # uint4b8 and int4 hold the same values once the top bit of each nibble is flipped
+    flipped = (d["w"].numpy().view(np.uint32) ^ np.uint32(0x88888888)).view(np.int32)
+    assert np.array_equal(oracle.w4a8(d["a"], flipped, d["layout"], oracle.UINT4B8, None, -1, K, N), acc)
+    rows = np.array([0, 5, 2]); cols = np.array([39, 0, 17])
+    assert np.array_equal(oracle.w4a8_elems(d["a"], d["w"], d["layout"], oracle.INT4, d["sg"], 128,
+                                            K, N, rows, cols), accg[rows, cols])
+
+
+def test_w4a8_extreme_accumulator_fits_int32():
+    # the largest |acc| the QQQ shape allows: K=21760, a=-127, v=-8, sg=16
+    K, N = 21760, 1
+    q = np.full((K, N), 8, dtype=np.uint8)  # int4 nibble 8 -> -8
+    w = oracle.pack(q, oracle.NK_EXLLAMA)
+    a = np.full((1, K), -127, dtype=np.int8)
+    sg = np.full((K // 128, N), 16, dtype=np.int8)
+    acc = oracle.w4a8(a, w, oracle.NK_EXLLAMA, oracle.INT4, sg, 128, K, N)
+    assert acc[0, 0] == 21760 * 127 * 8 * 16 and acc[0, 0] < 2**31
+
+
+def test_w4a8_scale_closed_form():
+    acc = np.array([3, -7, 1 << 20]); rows = np.array([0, 1, 1]); cols = np.array([1, 0, 1])
+    s_tok = np.array([0.5, 0.25]); s_ch = np.array([2.0, 0.125])
+    ref = oracle.w4a8_scale(acc, rows, cols, s_tok, s_ch)
+    assert list(ref) == [3 * 0.5 * 0.125, -7 * 0.25 * 2.0, (1 << 20) * 0.25 * 0.125]
