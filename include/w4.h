@@ -1,0 +1,174 @@
+/*
+ * w4.h — C ABI of libw4, a GB300 (sm_103a) 4-bit-weight mixed-precision GEMM.
+ *
+ *   out[M,N] = a[M,K] x dequant(W)[K,N]
+ *
+ * W holds 4-bit weights.  Three modes:
+ *   W4A16 symmetric : uint4b8 nibbles (value q-8), fp16/bf16 group scales.
+ *   W4A16 asymmetric: uint4 nibbles (value q) with pre-scaled zero-points.
+ *   W4A8 (QQQ style): int4 weights, int8 activations with per-token fp32
+ *                     scales, per-channel fp32 weight scales, optional int8
+ *                     per-group (g128) weight scales.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [MR]  Machete Readme, "Machete (Mixed Precision Cutlass-Based GEMM)":
+ *         "Overview" (the dequant formula, w_z pre-scaled so the step is one
+ *         FMA), "API" (prepack the weights to a tensor-core-friendly layout,
+ *         then call the GEMM with b_type, b_scales, b_group_size),
+ *         "Code Generation" (schedules chosen by a default heuristic, with an
+ *         optional `schedule` override).
+ *   [PR9855] vLLM PR #9855 "[Kernel] Initial Machete W4A8 support +
+ *         Refactors": QQQ-style W4A8; uint4b8 and uint4 share one prepack
+ *         because prepacking only moves data.
+ *   [RDNA] vLLM API page "rdna_hybrid_w4a16": ExLlama shuffle packing
+ *         (pack_int4_exllama_shuffle), ZP_BIAS 8, the argument checks of
+ *         triton_w4a16_skinny_fmt_gemm (contiguity, shapes, group_size -1
+ *         meaning K).
+ *   [QQQ] pytorch/ao PR #1113 "support W4A8 Marlin kernel": W4A8 per-channel
+ *         and per-group (g128), symmetric weights only, fp16 output only.
+ *   [PT]  vLLM PR #6547 "Enable Dynamic Per Token fp8": per-token activation
+ *         scales applied in the GEMM epilogue.
+ *
+ * Conventions for every entry point:
+ *   - All matrices are dense, contiguous, row-major, in DEVICE memory owned
+ *     by the caller.  The library allocates no memory and keeps no pointer
+ *     after a call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it; calls return after enqueue.
+ *   - Argument errors are reported synchronously, before anything is
+ *     enqueued; w4_last_error() then holds a one-line message.  The library
+ *     never aborts the process and its kernels never trap.
+ */
+#ifndef W4_H_
+#define W4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum w4_status {
+  W4_OK = 0,
+  W4_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad enum, bad shape or group size */
+  W4_ERR_UNSUPPORTED = 2,      /* well-formed, but outside what the kernels tile */
+  W4_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
+  W4_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+  W4_ERR_TIMEOUT = 5           /* a device-side wait gave up (w4_check_status) */
+} w4_status;
+
+/* Weight types ([PR9855] summary; [RDNA] ZP_BIAS; [QQQ] symmetric int4). */
+typedef enum w4_wtype {
+  W4_UINT4B8 = 0, /* stored q in 0..15, value q - 8 */
+  W4_UINT4 = 1,   /* stored q in 0..15, value q (use with zero-points) */
+  W4_INT4 = 2     /* two's complement nibble, value in -8..7 */
+} w4_wtype;
+
+/* Input layouts of the packed int32 weights (8 nibbles per word, K packed). */
+typedef enum w4_layout {
+  W4_LAYOUT_KN_SEQ = 0,    /* [K/8][N] words, K-value j of a word at bits 4j */
+  W4_LAYOUT_NK_SEQ = 1,    /* [N][K/8] words, K-value j at bits 4j */
+  W4_LAYOUT_NK_EXLLAMA = 2 /* [N][K/8] words, ExLlama order [0,2,4,6,1,3,5,7]:
+                              K-value j at bits (j/2)*4 + (j%2)*16 ([RDNA]) */
+} w4_layout;
+
+typedef enum w4_dtype { W4_F16 = 0, W4_BF16 = 1, W4_S8 = 2, W4_S32 = 3 } w4_dtype;
+
+/* Version of the prepacked weight layout produced by w4_prepack_B.  A
+ * buffer prepacked under one version must not be used with another. */
+int w4_layout_version(void);
+
+/* Bytes of the prepacked buffer for a K x N weight: ceil(N/128)*128 * K/2.
+ * Returns 0 for K <= 0, N <= 0 or K % 64 != 0. */
+size_t w4_prepacked_size(int64_t K, int64_t N);
+
+/* Rearrange packed 4-bit weights into the tensor-core tile order ([MR] API:
+ * "prepacking the weight matrix to more closely match the tensor core
+ * layouts").  w_q: int32 words in `in_layout` (device).  b_packed: device
+ * buffer of w4_prepacked_size(K, N) bytes, written in full (padding rows
+ * zeroed).  uint4 and uint4b8 prepack identically ([PR9855]); int4 nibbles
+ * are stored with their top bit flipped (offset binary, value q' - 8).
+ * Errors: INVALID_ARGUMENT for null pointers, bad enums, K % 8 != 0,
+ * K <= 0 or N <= 0; UNSUPPORTED for K % 64 != 0. */
+w4_status w4_prepack_B(const int32_t* w_q, int wtype, int in_layout, int64_t K, int64_t N,
+                       void* b_packed, void* stream);
+
+/* Inverse of w4_prepack_B (for tests and tooling): writes w_q in
+ * `out_layout` from a prepacked buffer with the same wtype, K and N. */
+w4_status w4_unprepack_B(const void* b_packed, int wtype, int out_layout, int64_t K, int64_t N,
+                         int32_t* w_q, void* stream);
+
+/* Workspace bytes w4_gemm needs for this problem under any schedule
+ * (always >= 256).  The workspace holds a status word, split-K tile
+ * counters and partial sums, and (W4A8) a bf16 copy of the activations.
+ * It must be zero-filled before its first use; every call leaves its
+ * counters at zero again.  Calls that share a workspace must not overlap
+ * on the GPU. */
+size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size);
+
+/* out = a x dequant(W)  ([MR] Overview and API; [QQQ]; [PT]).
+ *
+ *   a         [M,K] activations: W4_F16 / W4_BF16 (W4A16) or W4_S8 (W4A8).
+ *   b_packed  output of w4_prepack_B for this K, N and wtype.
+ *   group_size  128-multiple dividing K, or -1 / K for one group per
+ *             column ([RDNA]: -1 resolves to K).  G = K / group_size.
+ *   W4A16: b_scales [G,N] with scale_type == a_type; b_zeros [G,N] of the
+ *          same type holding PRE-SCALED zero-points w_z, or NULL.
+ *          w_hat[k][n] = v(q) * s[g][n] - w_z[g][n], rounded once to the
+ *          activation type (one fused multiply-add, [MR] Overview NOTE);
+ *          out = sum_k a*w_hat accumulated in fp32, rounded to out_type,
+ *          which must equal a_type.  a_token_scales and ch_scales NULL.
+ *   W4A8:  wtype W4_INT4 or W4_UINT4B8 (symmetric only, [QQQ]); b_zeros
+ *          NULL; b_scales = int8 group scales sg [G,N] (scale_type W4_S8)
+ *          for per-group, or NULL for per-channel (group_size -1 or K).
+ *          The integer weight v*sg must lie in [-128,127] (sg in 1..16).
+ *          acc = sum_k a*v*sg exactly in int32 (|acc| < 2^31 required).
+ *          out_type W4_F16: out = fp16_rn((float)acc * s_tok[m] * s_ch[n]),
+ *          multiplied left to right in fp32, with a_token_scales = s_tok [M]
+ *          and ch_scales = s_ch [N] (fp32, device).
+ *          out_type W4_S32: out = acc, both scale pointers NULL.
+ *   workspace  device buffer of at least w4_gemm_workspace_size(...) bytes.
+ *
+ * M == 0 is a no-op; K == 0 writes zeros.  Errors: INVALID_ARGUMENT
+ * (null required pointer, dtype mismatch, K % 8 != 0, group_size not
+ * dividing K, negative sizes), UNSUPPORTED (K % 64 != 0, group_size not a
+ * multiple of 64, W4A8 with zero-points, uint4 or a non-fp16/int32 output),
+ * WORKSPACE, CUDA. */
+w4_status w4_gemm(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                  int wtype, int64_t N, const void* b_scales, int scale_type,
+                  const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                  const float* ch_scales, void* out, int out_type, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* w4_gemm with an explicit schedule ([MR] Code Generation: the optional
+ * `schedule` argument).  schedule < 0 means the default heuristic;
+ * otherwise an index in [0, w4_num_schedules()).  A schedule that cannot
+ * run this problem returns UNSUPPORTED. */
+w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                     int wtype, int64_t N, const void* b_scales, int scale_type,
+                     const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                     const float* ch_scales, void* out, int out_type, void* workspace,
+                     size_t workspace_bytes, void* stream, int schedule);
+
+/* Schedules: their count, names, and the one the default heuristic picks
+ * for a problem (-1 when none can run it). */
+int w4_num_schedules(void);
+const char* w4_schedule_name(int schedule);
+int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size);
+
+/* Synchronize `stream`, then report (and clear) a device-side timeout that
+ * a kernel recorded in `workspace`: W4_ERR_TIMEOUT, else W4_OK.  On a
+ * timeout the split-K counters are zeroed again. */
+w4_status w4_check_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static text for a status code; message of the last failed call on this
+ * host thread ("" when none). */
+const char* w4_status_string(int status);
+const char* w4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H_ */

@@ -1,0 +1,418 @@
+// w4_api.cu — the C ABI of libw4 (declared in include/w4.h): argument
+// validation, the schedule table and default heuristic, workspace planning,
+// tensor-map creation and kernel launch.  No allocation happens here: the
+// caller owns every buffer.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/w4.h"
+#include "w4_internal.h"
+
+namespace w4 {
+namespace {
+
+thread_local std::string g_last_error;
+
+w4_status fail(w4_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+w4_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(W4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Schedules ("Machete Readme", "Code Generation": a set of schedule configs
+// with a default heuristic and an optional explicit choice).
+const Schedule kSchedules[] = {
+    {"simt", kEngineSimt, 0, kDataParallel},       {"tc16_sk", kEngineTc, 16, kStreamK},
+    {"tc32_sk", kEngineTc, 32, kStreamK},          {"tc64_sk", kEngineTc, 64, kStreamK},
+    {"tc128_sk", kEngineTc, 128, kStreamK},        {"tc128_dp", kEngineTc, 128, kDataParallel},
+    {"tc256_sk", kEngineTc, 256, kStreamK},        {"tc256_dp", kEngineTc, 256, kDataParallel},
+};
+constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
+constexpr size_t kCounterBytes = 64 * 1024;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;  // GB300
+  }
+  return n;
+}
+
+int mode_of(int a_type) {
+  return a_type == W4_F16 ? kW4A16_F16 : a_type == W4_BF16 ? kW4A16_BF16 : kW4A8;
+}
+
+// Whether schedule `si` can run this (already validated) problem shape.
+bool schedule_fits(int si, int mode, int64_t N, bool has_sg) {
+  const Schedule& sc = kSchedules[si];
+  if (sc.engine == kEngineSimt) return true;
+  if (N % 8 != 0) return false;                      // 16-byte scale rows
+  if (mode == kW4A8 && has_sg && N % 16 != 0) return false;
+  if (mode == kW4A8 && sc.bm > 128) return false;    // D + int32 copy in tensor memory
+  return true;
+}
+
+// Build the launch plan of a tc schedule.
+TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) {
+  const Schedule& sc = kSchedules[si];
+  TcPlan p{};
+  p.mode = mode;
+  p.bm = sc.bm;
+  p.stages = tc_max_stages(p.bm, mode);
+  p.smem_bytes = tc_smem_bytes(p.bm, mode, p.stages);
+  p.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
+  p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
+  p.tiles = p.m_tiles * p.n_tiles;
+  p.kb_total = static_cast<int>(K / kStageK);
+  // W4A8 exactness: |a| <= 128 and |v*sg| <= 128 (group) or |v| <= 8
+  // (per-channel) keep every fp32 partial sum of a chunk within 2^24.
+  p.chunk_stages = (gs < K) ? 1024 / kStageK : 16384 / kStageK;
+  const int sms = sm_count();
+  p.decomp = sc.decomp;
+  if (p.tiles * static_cast<size_t>(kConvWarps) * 4 > kCounterBytes) p.decomp = kDataParallel;
+  p.ws_counters = kWsHeader;
+  if (p.decomp == kDataParallel) {
+    p.grid = p.tiles < sms ? p.tiles : sms;
+    p.max_segs = 1;
+    p.ws_partials = p.ws_counters + kCounterBytes;
+  } else {
+    const int64_t T = static_cast<int64_t>(p.tiles) * p.kb_total;
+    int64_t g = T / 4;  // at least 4 stages per CTA
+    if (g > sms) g = sms;
+    if (g < 1) g = 1;
+    p.grid = static_cast<int>(g);
+    int ms = 1;
+    for (int64_t c = 0; c < g; ++c) {
+      int64_t b = c * T / g, e = (c + 1) * T / g;
+      if (e <= b) continue;
+      int segs = static_cast<int>((e - 1) / p.kb_total - b / p.kb_total + 1);
+      if (segs > ms) ms = segs;
+    }
+    p.max_segs = ms;
+    p.ws_partials = p.ws_counters + kCounterBytes;
+  }
+  size_t part = p.decomp == kStreamK
+                    ? static_cast<size_t>(p.grid) * p.max_segs * kTileN * p.bm * 4
+                    : 0;
+  p.ws_act = align256(p.ws_partials + part);
+  size_t act = mode == kW4A8 ? static_cast<size_t>(M) * K * 2 : 0;
+  p.ws_total = align256(p.ws_act + act);
+  return p;
+}
+
+size_t simt_ws_bytes() { return kWsHeader; }
+
+int default_schedule_impl(int mode, int64_t M, int64_t N, bool has_sg) {
+  int bm = 16;
+  while (bm < M && bm < 256) bm *= 2;
+  if (mode == kW4A8 && bm > 128) bm = 128;
+  const int64_t tiles = ((M + bm - 1) / bm) * ((N + kTileN - 1) / kTileN);
+  const bool dp = tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128;
+  for (int si = 1; si < kNumSchedules; ++si) {
+    const Schedule& sc = kSchedules[si];
+    if (sc.bm == bm && (sc.decomp == kDataParallel) == dp && schedule_fits(si, mode, N, has_sg))
+      return si;
+  }
+  for (int si = 1; si < kNumSchedules; ++si)
+    if (kSchedules[si].bm == bm && schedule_fits(si, mode, N, has_sg)) return si;
+  return 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct Problem {
+  int mode;
+  int64_t M, N, K, gs;
+  bool has_sg;
+};
+
+w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                   int wtype, int64_t N, const void* b_scales, int scale_type,
+                   const void* b_zeros, int64_t group_size, const float* s_tok,
+                   const float* s_ch, void* out, int out_type, Problem& pr) {
+  if (M < 0 || N < 0 || K < 0) return fail(W4_ERR_INVALID_ARGUMENT, "negative size");
+  if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8)
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16, W4_BF16 or W4_S8");
+  if (wtype < W4_UINT4B8 || wtype > W4_INT4) return fail(W4_ERR_INVALID_ARGUMENT, "bad wtype");
+  if (K % 8 != 0) return fail(W4_ERR_INVALID_ARGUMENT, "K must be a multiple of 8");
+  const int64_t gs = (group_size == -1) ? K : group_size;
+  if (K > 0 && (gs <= 0 || K % gs != 0))
+    return fail(W4_ERR_INVALID_ARGUMENT, "group_size must be -1 or a positive divisor of K");
+  pr.mode = mode_of(a_type);
+  pr.M = M;
+  pr.N = N;
+  pr.K = K;
+  pr.gs = gs;
+  pr.has_sg = b_scales != nullptr;
+  if (M == 0 || N == 0) return W4_OK;
+  if (!out) return fail(W4_ERR_INVALID_ARGUMENT, "out is null");
+  if (pr.mode != kW4A8) {
+    if (out_type != a_type)
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A16: out_type must equal a_type");
+    if (K > 0 && (!a || !b_packed || !b_scales))
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A16: a, b_packed and b_scales are required");
+    if (scale_type != a_type)
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A16: scale_type must equal a_type");
+    if (s_tok || s_ch)
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A16 takes no token or channel scales");
+  } else {
+    if (wtype == W4_UINT4)
+      return fail(W4_ERR_UNSUPPORTED, "W4A8 supports symmetric weights only (int4 / uint4b8)");
+    if (b_zeros) return fail(W4_ERR_UNSUPPORTED, "W4A8 takes no zero-points");
+    if (out_type == W4_F16) {
+      if (!s_tok || !s_ch)
+        return fail(W4_ERR_INVALID_ARGUMENT, "W4A8 fp16 out needs token and channel scales");
+    } else if (out_type == W4_S32) {
+      if (s_tok || s_ch)
+        return fail(W4_ERR_INVALID_ARGUMENT, "W4A8 int32 out takes no float scales");
+    } else {
+      return fail(W4_ERR_UNSUPPORTED, "W4A8 output must be W4_F16 or W4_S32");
+    }
+    if (b_scales && scale_type != W4_S8)
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A8 group scales must be int8 (W4_S8)");
+    if (!b_scales && gs != K)
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A8 per-group needs int8 group scales");
+    if (K > 0 && (!a || !b_packed))
+      return fail(W4_ERR_INVALID_ARGUMENT, "a and b_packed are required");
+  }
+  if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
+  if (K > 0 && gs % kStageK != 0)
+    return fail(W4_ERR_UNSUPPORTED, "group_size must be a multiple of 64 (or K)");
+  return W4_OK;
+}
+
+size_t ws_needed(int si, const Problem& pr) {
+  if (kSchedules[si].engine == kEngineSimt) return simt_ws_bytes();
+  return make_plan(si, pr.mode, pr.M, pr.N, pr.K, pr.gs).ws_total;
+}
+
+}  // namespace
+}  // namespace w4
+
+using namespace w4;
+
+extern "C" {
+
+int w4_layout_version(void) { return kLayoutVersion; }
+
+size_t w4_prepacked_size(int64_t K, int64_t N) {
+  if (K <= 0 || N <= 0 || K % kStageK != 0) return 0;
+  return static_cast<size_t>((N + kTileN - 1) / kTileN * kTileN) * static_cast<size_t>(K / 2);
+}
+
+w4_status w4_prepack_B(const int32_t* w_q, int wtype, int in_layout, int64_t K, int64_t N,
+                       void* b_packed, void* stream) {
+  if (!w_q || !b_packed) return fail(W4_ERR_INVALID_ARGUMENT, "null pointer");
+  if (wtype < W4_UINT4B8 || wtype > W4_INT4) return fail(W4_ERR_INVALID_ARGUMENT, "bad wtype");
+  if (in_layout < W4_LAYOUT_KN_SEQ || in_layout > W4_LAYOUT_NK_EXLLAMA)
+    return fail(W4_ERR_INVALID_ARGUMENT, "bad layout");
+  if (K <= 0 || N <= 0 || K % 8 != 0)
+    return fail(W4_ERR_INVALID_ARGUMENT, "K and N must be positive, K a multiple of 8");
+  if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
+  cudaError_t e = launch_prepack(w_q, wtype, in_layout, K, N, static_cast<uint8_t*>(b_packed),
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4_OK : cuda_fail(e, "prepack launch");
+}
+
+w4_status w4_unprepack_B(const void* b_packed, int wtype, int out_layout, int64_t K, int64_t N,
+                         int32_t* w_q, void* stream) {
+  if (!w_q || !b_packed) return fail(W4_ERR_INVALID_ARGUMENT, "null pointer");
+  if (wtype < W4_UINT4B8 || wtype > W4_INT4) return fail(W4_ERR_INVALID_ARGUMENT, "bad wtype");
+  if (out_layout < W4_LAYOUT_KN_SEQ || out_layout > W4_LAYOUT_NK_EXLLAMA)
+    return fail(W4_ERR_INVALID_ARGUMENT, "bad layout");
+  if (K <= 0 || N <= 0 || K % 8 != 0)
+    return fail(W4_ERR_INVALID_ARGUMENT, "K and N must be positive, K a multiple of 8");
+  if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
+  cudaError_t e = launch_unprepack(static_cast<const uint8_t*>(b_packed), wtype, out_layout, K,
+                                   N, w_q, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4_OK : cuda_fail(e, "unprepack launch");
+}
+
+int w4_num_schedules(void) { return kNumSchedules; }
+
+const char* w4_schedule_name(int schedule) {
+  if (schedule < 0 || schedule >= kNumSchedules) return nullptr;
+  return kSchedules[schedule].name;
+}
+
+int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % kStageK != 0) return -1;
+  if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8) return -1;
+  const int64_t gs = group_size == -1 ? K : group_size;
+  return default_schedule_impl(mode_of(a_type), M, N, gs != K);
+}
+
+size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size) {
+  Problem pr{};
+  pr.mode = mode_of(a_type);
+  pr.M = M < 0 ? 0 : M;
+  pr.N = N < 0 ? 0 : N;
+  pr.K = K < 0 ? 0 : K;
+  pr.gs = group_size == -1 ? pr.K : group_size;
+  pr.has_sg = pr.gs != pr.K;
+  size_t need = kWsHeader;
+  if (pr.M == 0 || pr.N == 0 || pr.K == 0 || pr.K % kStageK != 0) return need;
+  for (int si = 0; si < kNumSchedules; ++si) {
+    if (!schedule_fits(si, pr.mode, pr.N, pr.has_sg)) continue;
+    size_t b = ws_needed(si, pr);
+    if (b > need) need = b;
+  }
+  return need;
+}
+
+w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                     int wtype, int64_t N, const void* b_scales, int scale_type,
+                     const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                     const float* ch_scales, void* out, int out_type, void* workspace,
+                     size_t workspace_bytes, void* stream, int schedule) {
+  Problem pr{};
+  w4_status st = validate(a, a_type, M, K, b_packed, wtype, N, b_scales, scale_type, b_zeros,
+                          group_size, a_token_scales, ch_scales, out, out_type, pr);
+  if (st != W4_OK) return st;
+  if (schedule >= kNumSchedules) return fail(W4_ERR_INVALID_ARGUMENT, "bad schedule index");
+  if (M == 0 || N == 0) return W4_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    const size_t esz = (pr.mode == kW4A8 && out_type == W4_S32) ? 4 : 2;
+    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(M) * N * esz, s);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "memset");
+  }
+  int si = schedule;
+  const bool forced = schedule >= 0;
+  if (!forced) si = default_schedule_impl(pr.mode, M, N, pr.has_sg);
+  if (!schedule_fits(si, pr.mode, N, pr.has_sg))
+    return fail(W4_ERR_UNSUPPORTED, "schedule %s cannot run this shape", kSchedules[si].name);
+  const bool ptrs_ok = aligned16(a) && aligned16(b_packed) && aligned16(b_scales) &&
+                       aligned16(b_zeros);
+  if (kSchedules[si].engine == kEngineTc && !ptrs_ok) {
+    if (forced) return fail(W4_ERR_UNSUPPORTED, "tc schedules need 16-byte aligned inputs");
+    si = 0;
+  }
+  if (!workspace) return fail(W4_ERR_WORKSPACE, "workspace is null");
+  const size_t need = ws_needed(si, pr);
+  if (workspace_bytes < need)
+    return fail(W4_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+
+  TcArgs args{};
+  args.b_packed = static_cast<const uint8_t*>(b_packed);
+  args.scales = b_scales;
+  args.zeros = b_zeros;
+  args.s_tok = a_token_scales;
+  args.s_ch = ch_scales;
+  args.out = out;
+  args.out_s32 = (pr.mode == kW4A8 && out_type == W4_S32) ? 1 : 0;
+  args.wbias = (wtype == W4_UINT4) ? 0 : 8;
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.group_size = pr.gs;
+  args.status = static_cast<int*>(workspace);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  if (kSchedules[si].engine == kEngineSimt) {
+    cudaError_t e = launch_simt(pr.mode, a, args, s);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "simt launch");
+  }
+
+  TcPlan plan = make_plan(si, pr.mode, M, N, K, pr.gs);
+  args.counters = reinterpret_cast<int*>(ws + plan.ws_counters);
+  args.partials = ws + plan.ws_partials;
+  const void* act = a;
+  if (pr.mode == kW4A8) {
+    cudaError_t e = launch_a8_to_bf16(static_cast<const int8_t*>(a), M * K, ws + plan.ws_act, s);
+    if (e != cudaSuccess) return cuda_fail(e, "int8->bf16 launch");
+    act = ws + plan.ws_act;
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  CUtensorMap amap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(plan.bm)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&amap,
+                   pr.mode == kW4A16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   2, const_cast<void*>(act), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  cudaError_t e = launch_tc(plan, amap, args, s);
+  return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
+}
+
+w4_status w4_gemm(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                  int wtype, int64_t N, const void* b_scales, int scale_type,
+                  const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                  const float* ch_scales, void* out, int out_type, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  return w4_gemm_ex(a, a_type, M, K, b_packed, wtype, N, b_scales, scale_type, b_zeros,
+                    group_size, a_token_scales, ch_scales, out, out_type, workspace,
+                    workspace_bytes, stream, -1);
+}
+
+w4_status w4_check_status(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kWsHeader)
+    return fail(W4_ERR_WORKSPACE, "workspace is null or smaller than its header");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word == 0) return W4_OK;
+  size_t clear = workspace_bytes < kWsHeader + kCounterBytes ? workspace_bytes
+                                                            : kWsHeader + kCounterBytes;
+  e = cudaMemset(workspace, 0, clear);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  return fail(W4_ERR_TIMEOUT, "a device-side wait timed out");
+}
+
+const char* w4_status_string(int status) {
+  switch (status) {
+    case W4_OK: return "W4_OK";
+    case W4_ERR_INVALID_ARGUMENT: return "W4_ERR_INVALID_ARGUMENT";
+    case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED";
+    case W4_ERR_WORKSPACE: return "W4_ERR_WORKSPACE";
+    case W4_ERR_CUDA: return "W4_ERR_CUDA";
+    case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT";
+    default: return "W4_ERR_UNKNOWN";
+  }
+}
+
+const char* w4_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// w4_internal.h — plan and launch interfaces shared by the host library
+// (w4_api.cu) and the kernels (w4_kernels.cu, w4_tc.cu).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+constexpr int kLayoutVersion = 1;
+// Prepacked tile: 128 weight columns (n) x 32 K-values per 16-byte chunk;
+// buffer order [N/128][K/32][128][4 words].  Within each 32-bit word the
+// eight K-values k0..k0+7 sit in ExLlama order: value j at bits
+// (j/2)*4 + (j%2)*16, so bits 0-3/16-19 hold the pair (k0, k0+1), bits
+// 4-7/20-23 the pair (k0+2, k0+3), and so on.
+constexpr int kTileN = 128;
+constexpr int kChunkK = 32;
+constexpr int kStageK = 64;
+constexpr int kMaxStages = 32;
+constexpr int kTmemStages = 4;
+constexpr int kTmemACol = 256;  // first tensor-memory column of the A stages
+constexpr int kConvWarps = 8;
+constexpr int kTcThreads = 64 + 32 * kConvWarps;  // producer, MMA, 8 converter warps
+constexpr size_t kWsHeader = 256;                // status word + spare
+
+enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
+
+enum Engine { kEngineSimt = 0, kEngineTc = 1 };
+enum Decomp { kDataParallel = 0, kStreamK = 1 };
+
+struct Schedule {
+  const char* name;
+  int engine;
+  int bm;      // activation rows per tile (UMMA N)
+  int decomp;  // kDataParallel / kStreamK
+};
+
+// Everything a tc launch needs, computed on the host.
+struct TcPlan {
+  int mode;
+  int bm;
+  int stages;
+  int m_tiles, n_tiles, tiles;
+  int kb_total;        // K / 64
+  int grid;            // CTAs
+  int decomp;
+  int max_segs;        // partial slots per CTA (stream-K)
+  int chunk_stages;    // W4A8: stages per exact fp32 accumulation chunk
+  size_t smem_bytes;
+  size_t ws_counters;  // byte offsets into the workspace
+  size_t ws_partials;
+  size_t ws_act;       // W4A8 bf16 activations
+  size_t ws_total;
+};
+
+struct TcArgs {
+  const uint8_t* b_packed;
+  const void* scales;      // W4A16 [G][N] 16-bit; W4A8 int8 sg [G][N] or null
+  const void* zeros;       // W4A16 [G][N] 16-bit or null
+  const float* s_tok;      // W4A8
+  const float* s_ch;       // W4A8
+  void* out;
+  int out_s32;             // W4A8 raw int32 output
+  int wbias;               // 8 for uint4b8 / int4 (offset binary), 0 for uint4
+  int64_t M, N, K;
+  int64_t group_size;
+  int* status;
+  int* counters;
+  void* partials;
+};
+
+// Host launchers (return cudaError_t of the launch).
+cudaError_t launch_prepack(const int32_t* w_q, int wtype, int layout, int64_t K, int64_t N,
+                           uint8_t* out, cudaStream_t s);
+cudaError_t launch_unprepack(const uint8_t* packed, int wtype, int layout, int64_t K,
+                             int64_t N, int32_t* w_q, cudaStream_t s);
+cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_t s);
+cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s);
+cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const TcArgs& args,
+                      cudaStream_t s);
+size_t tc_smem_bytes(int bm, int mode, int stages);
+int tc_max_stages(int bm, int mode);
+
+}  // namespace w4

@@ -1,0 +1,552 @@
+// w4_tc.cu — the tensor-core schedule of the 4-bit-weight GEMM for sm_103a.
+//
+// Orientation: the weight tile is the 128-row UMMA "A" operand and the
+// activations are the UMMA "B" operand, so each CTA computes
+//   D[n, m] = sum_k w_hat[k, n] * a[m, k]      (n: 128 weight columns,
+//                                               m: BM activation rows)
+// which is the transposed statement of out = a x w_hat (the Machete Readme,
+// "Overview", writes the weight on the left of "@ a").
+//
+// Data flow per 64-wide K stage:
+//   producer warp : TMA tile of the activations (128B-swizzled, K-major)
+//                   + one 4 KB bulk copy of the prepacked nibbles
+//                   + the stage's scale / zero-point rows
+//   8 converter warps : nibbles -> 16-bit weights in registers, one fused
+//                   multiply-add per pair with the scale and pre-scaled
+//                   zero-point (Machete Readme "Overview" NOTE), stored
+//                   straight into tensor memory (tcgen05.st): dequantized
+//                   weights never touch shared memory
+//   MMA thread    : 4 x tcgen05.mma (K = 16) with A from tensor memory and
+//                   B from shared memory, fp32 accumulator in tensor memory
+//   epilogue      : converter warps drain the accumulator (tcgen05.ld),
+//                   convert / scale and store, or write split-K partials and
+//                   let the last arriving warp of each sub-tile reduce them.
+//
+// W4A8 (pytorch/ao PR #1113 "support W4A8 Marlin kernel") runs on the same
+// bf16 tensor cores: int8 activations and int4 (x int8 group scale)
+// weights are exact in bf16, their products are exact in fp32, and the
+// accumulator is drained into an int32 copy in tensor memory before any
+// partial sum can exceed 2^24, so the int32 result is exact.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "w4_internal.h"
+#include "w4_ptx.cuh"
+
+namespace w4 {
+
+namespace {
+
+struct Unit {
+  int tile;
+  int kb0, kb1;
+  int nslots;   // CTAs contributing to this tile
+  int cfirst;   // first contributing CTA (stream-K)
+  int seg;      // index of this tile among the CTA's segments
+};
+
+struct Work {
+  int64_t T, G, kb;
+  int64_t begin, end;  // stream-K range of this CTA
+  int64_t first_tile;
+};
+
+__device__ __forceinline__ int64_t sk_start(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+
+// Stream-K: the CTA that owns linear iteration i.
+__device__ __forceinline__ int64_t sk_owner(int64_t i, int64_t T, int64_t G) {
+  return ((i + 1) * G - 1) / T;
+}
+
+// u-th unit of this CTA; false when there is none.
+__device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
+  if (p.decomp == kDataParallel) {
+    int64_t t = blockIdx.x + static_cast<int64_t>(u) * p.grid;
+    if (t >= p.tiles) return false;
+    out.tile = static_cast<int>(t);
+    out.kb0 = 0;
+    out.kb1 = p.kb_total;
+    out.nslots = 1;
+    out.cfirst = blockIdx.x;
+    out.seg = 0;
+    return true;
+  }
+  int64_t t = w.first_tile + u;
+  int64_t lo = t * w.kb, hi = lo + w.kb;
+  if (lo < w.begin) lo = w.begin;
+  if (hi > w.end) hi = w.end;
+  if (lo >= hi) return false;
+  out.tile = static_cast<int>(t);
+  out.kb0 = static_cast<int>(lo - t * w.kb);
+  out.kb1 = static_cast<int>(hi - t * w.kb);
+  int64_t cf = sk_owner(t * w.kb, w.T, w.G);
+  int64_t cl = sk_owner((t + 1) * w.kb - 1, w.T, w.G);
+  out.cfirst = static_cast<int>(cf);
+  out.nslots = static_cast<int>(cl - cf + 1);
+  out.seg = u;
+  return true;
+}
+
+// Tile -> (m_tile, n_tile), grouped raster: runs of up to 8 m-tiles share
+// each weight tile while it is in L2.
+__device__ __forceinline__ void tile_coords(const TcPlan& p, int t, int& mt, int& nt) {
+  int gm_full = p.m_tiles < 8 ? p.m_tiles : 8;
+  int group = t / (gm_full * p.n_tiles);
+  int local = t - group * gm_full * p.n_tiles;
+  int gm = p.m_tiles - group * gm_full;
+  if (gm > gm_full) gm = gm_full;
+  mt = group * gm_full + local % gm;
+  nt = local / gm;
+}
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+template <typename T2>
+__device__ __forceinline__ T2 as_t2(uint32_t x) {
+  return *reinterpret_cast<T2*>(&x);
+}
+template <typename T2>
+__device__ __forceinline__ uint32_t as_u32(T2 x) {
+  return *reinterpret_cast<uint32_t*>(&x);
+}
+
+// Dequantize the 32 K-values of one 16-byte chunk (4 words, ExLlama order)
+// into 16 packed pairs.  Pair p of word x holds (k0+2p, k0+2p+1) at bits
+// (4p, 16+4p).  OR-ing a nibble into the mantissa of the "magic" constant
+// gives magic+q exactly; subtracting magic+bias is exact; the FMA with the
+// scale and negated zero-point rounds once.
+template <int MODE>
+__device__ __forceinline__ void convert_chunk(const uint4& wv, uint32_t s2u, uint32_t nz2u,
+                                              bool has_z, bool has_s, int wbias,
+                                              uint32_t (&v)[16]) {
+  const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+  if constexpr (MODE == kW4A16_F16) {
+    const __half2 off = __half2half2(__int2half_rn(1024 + wbias));
+    const __half2 s2 = as_t2<__half2>(s2u), nz2 = as_t2<__half2>(nz2u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        __half2 h = as_t2<__half2>(lop_and_or(wd[i] >> (4 * p), 0x000F000Fu, 0x64006400u));
+        __half2 q = __hsub2(h, off);
+        v[4 * i + p] = as_u32(has_z ? __hfma2(q, s2, nz2) : __hmul2(q, s2));
+      }
+  } else {
+    const __nv_bfloat162 off = __bfloat162bfloat162(__int2bfloat16_rn(128 + wbias));
+    const __nv_bfloat162 s2 = as_t2<__nv_bfloat162>(s2u), nz2 = as_t2<__nv_bfloat162>(nz2u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        __nv_bfloat162 h =
+            as_t2<__nv_bfloat162>(lop_and_or(wd[i] >> (4 * p), 0x000F000Fu, 0x43004300u));
+        __nv_bfloat162 q = __hsub2(h, off);
+        if constexpr (MODE == kW4A8) {
+          v[4 * i + p] = as_u32(has_s ? __hmul2(q, s2) : q);
+        } else {
+          v[4 * i + p] = as_u32(has_z ? __hfma2(q, s2, nz2) : __hmul2(q, s2));
+        }
+      }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T to_t16(float x);
+template <>
+__device__ __forceinline__ __half to_t16<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_t16<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+struct Smem {
+  uint8_t* a;      // stages x BM x 128 B
+  uint8_t* w;      // stages x 4096 B
+  uint8_t* s;      // stages x 256 B
+  uint8_t* z;      // stages x 256 B
+  uint64_t* full;  // [stages]
+  uint64_t* empty; // [stages]
+  uint64_t* tfull; // [kTmemStages]
+  uint64_t* tempty;
+  uint64_t* dfull;
+  uint64_t* dempty;
+  uint64_t* fin;
+  uint32_t* tmem_slot;
+  int* abort;
+};
+
+}  // namespace
+
+size_t tc_smem_bytes(int bm, int /*mode*/, int stages) {
+  size_t per_stage = static_cast<size_t>(bm) * 128 + 4096 + 256 + 256;
+  size_t bars = (2 * kMaxStages + 2 * kTmemStages + 3) * 8;
+  return 1024 + per_stage * stages + bars + 64;
+}
+
+int tc_max_stages(int bm, int mode) {
+  const size_t budget = 225 * 1024;
+  int s = kMaxStages;
+  while (s > 2 && tc_smem_bytes(bm, mode, s) > budget) --s;
+  return s;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap amap, const TcPlan p, const TcArgs args) {
+  using T16 = typename std::conditional<MODE == kW4A16_F16, __half, __nv_bfloat16>::type;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages, BM = p.bm;
+  Smem sm;
+  sm.a = base;
+  sm.w = sm.a + static_cast<size_t>(S) * BM * 128;
+  sm.s = sm.w + static_cast<size_t>(S) * 4096;
+  sm.z = sm.s + static_cast<size_t>(S) * 256;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * 256);
+  sm.full = bars;
+  sm.empty = bars + kMaxStages;
+  sm.tfull = bars + 2 * kMaxStages;
+  sm.tempty = sm.tfull + kTmemStages;
+  sm.dfull = sm.tempty + kTmemStages;
+  sm.dempty = sm.dfull + 1;
+  sm.fin = sm.dempty + 1;
+  sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.fin + 1);
+  sm.abort = reinterpret_cast<int*>(sm.tmem_slot + 1);
+  volatile int* abort = sm.abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kConvWarps + 1);
+    }
+    for (int i = 0; i < kTmemStages; ++i) {
+      mbar_init(&sm.tfull[i], kConvWarps);
+      mbar_init(&sm.tempty[i], 1);
+    }
+    mbar_init(sm.dfull, 1);
+    mbar_init(sm.dempty, kConvWarps);
+    mbar_init(sm.fin, 1);
+    *sm.abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&amap);
+  }
+  if (warp == 0) {
+    tmem_alloc(sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_slot;
+
+  Work wk;
+  wk.kb = p.kb_total;
+  wk.T = static_cast<int64_t>(p.tiles) * p.kb_total;
+  wk.G = p.grid;
+  wk.begin = sk_start(blockIdx.x, wk.T, wk.G);
+  wk.end = sk_start(blockIdx.x + 1, wk.T, wk.G);
+  wk.first_tile = wk.begin / wk.kb;
+
+  const int64_t M = args.M, N = args.N, K = args.K;
+  const int gsz = static_cast<int>(args.group_size);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      Unit u;
+      for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+        int mt, nt;
+        tile_coords(p, u.tile, mt, nt);
+        const int64_t n0 = static_cast<int64_t>(nt) * kTileN;
+        const int valid_n = static_cast<int>(N - n0 < kTileN ? N - n0 : kTileN);
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
+          const int64_t g = static_cast<int64_t>(kb) * kStageK / gsz;
+          uint32_t sbytes = 0, zbytes = 0;
+          if (MODE == kW4A8) {
+            if (args.scales) sbytes = valid_n;
+          } else {
+            sbytes = valid_n * 2;
+            if (args.zeros) zbytes = valid_n * 2;
+          }
+          mbar_arrive_expect_tx(&sm.full[s], BM * 128 + 4096 + sbytes + zbytes);
+          tma_load_2d(sm.a + static_cast<size_t>(s) * BM * 128, &amap, kb * kStageK, mt * BM,
+                      &sm.full[s]);
+          const uint8_t* wsrc =
+              args.b_packed + ((static_cast<int64_t>(nt) * (K / kChunkK) + kb * 2) * kTileN) * 16;
+          bulk_g2s(sm.w + static_cast<size_t>(s) * 4096, wsrc, 4096, &sm.full[s]);
+          if (sbytes) {
+            const uint8_t* src = static_cast<const uint8_t*>(args.scales) +
+                                 (g * N + n0) * (MODE == kW4A8 ? 1 : 2);
+            bulk_g2s(sm.s + s * 256, src, sbytes, &sm.full[s]);
+          }
+          if (zbytes) {
+            const uint8_t* src = static_cast<const uint8_t*>(args.zeros) + (g * N + n0) * 2;
+            bulk_g2s(sm.z + s * 256, src, zbytes, &sm.full[s]);
+          }
+        }
+      }
+      // Let every copy issued land before the CTA can exit.
+      const uint32_t issued = it;
+      for (uint32_t j = (issued > static_cast<uint32_t>(S) ? issued - S : 0); j < issued; ++j) {
+        volatile int no_abort = 0;
+        mbar_wait(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
+      uint32_t it = 0, ev = 0;
+      bool ok = true;
+      Unit u;
+      for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+        bool chunk_start = true;
+        const int nkb = u.kb1 - u.kb0;
+        for (int j = 0; j < nkb; ++j, ++it) {
+          if (chunk_start && ev > 0) {
+            if (!mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) { ok = false; break; }
+          }
+          const int s = it % S, ts = it % kTmemStages;
+          if (!mbar_wait(&sm.tfull[ts], (it / kTmemStages) & 1, abort, args.status) ||
+              !mbar_wait(&sm.full[s], (it / S) & 1, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(sm.a + static_cast<size_t>(s) * BM * 128);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_ts(tmem, tmem + kTmemACol + ts * 32 + kk * 8, sw128_kmajor_desc(a_base + kk * 32),
+                   idesc, (chunk_start && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(&sm.tempty[ts]);
+          mma_commit(&sm.empty[s]);
+          chunk_start = false;
+          const bool chunk_end =
+              (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
+          if (chunk_end) {
+            mma_commit(sm.dfull);
+            ++ev;
+            chunk_start = true;
+          }
+        }
+      }
+      // All issued MMAs complete before tensor memory is released.
+      mma_commit(sm.fin);
+      volatile int no_abort = 0;
+      mbar_wait(sm.fin, 0, &no_abort, args.status);
+    }
+  } else {
+    // ----------------------------------------------- converters + epilogue
+    const int q = warp & 3;            // tensor-memory lane quadrant
+    const int c = (warp - 2) >> 2;     // which 32-K chunk of a stage, and which column half
+    const int r = q * 32 + lane;       // weight row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int cols_half = BM / 2;
+    const int col0 = c * cols_half;
+    const int sub = warp - 2;          // sub-tile id (quadrant x column half)
+    uint32_t it = 0, ev = 0;
+    bool ok = true;
+    Unit u;
+    for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+      int mt, nt;
+      tile_coords(p, u.tile, mt, nt);
+      const int64_t n0 = static_cast<int64_t>(nt) * kTileN;
+      const int valid_n = static_cast<int>(N - n0 < kTileN ? N - n0 : kTileN);
+      const int64_t m0 = static_cast<int64_t>(mt) * BM;
+      const bool row_ok = r < valid_n;
+      const int nkb = u.kb1 - u.kb0;
+      bool first_chunk = true;
+      for (int j = 0; j < nkb; ++j, ++it) {
+        const int s = it % S, ts = it % kTmemStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], (it / S) & 1, abort, args.status))) {
+          ok = false;
+          break;
+        }
+        const uint4 wv =
+            *reinterpret_cast<const uint4*>(sm.w + static_cast<size_t>(s) * 4096 + (c * 128 + r) * 16);
+        uint32_t s2 = 0, nz2 = 0;
+        bool has_s = true;
+        if (MODE == kW4A8) {
+          has_s = args.scales != nullptr;
+          if (has_s && row_ok) {
+            const float sg = static_cast<float>(reinterpret_cast<const int8_t*>(sm.s + s * 256)[r]);
+            s2 = as_u32(__float2bfloat162_rn(sg));
+          }
+        } else if (row_ok) {
+          const uint16_t sv = reinterpret_cast<const uint16_t*>(sm.s + s * 256)[r];
+          s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
+          if (args.zeros) {
+            const uint16_t zv = reinterpret_cast<const uint16_t*>(sm.z + s * 256)[r] ^ 0x8000u;
+            nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
+          }
+        }
+        uint32_t v[16];
+        convert_chunk<MODE>(wv, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v);
+        if (!row_ok) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0;
+        }
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&sm.tempty[ts], ((it / kTmemStages) & 1) ^ 1, abort, args.status))) {
+          ok = false;
+          break;
+        }
+        tmem_st16(tmem + lane_base + kTmemACol + ts * 32 + c * 16, v);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.tfull[ts]);
+          mbar_arrive(&sm.empty[s]);
+        }
+        const bool chunk_end =
+            (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
+        if (!chunk_end) continue;
+
+        // ------------------------------------------------ drain an event
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.dfull, ev & 1, abort, args.status))) {
+          ok = false;
+          break;
+        }
+        ++ev;
+        tc_fence_after();
+        const bool final_ev = (j == nkb - 1);
+        const uint32_t dcol = tmem + lane_base + col0;
+        const uint32_t icol = dcol + BM;  // W4A8 int32 accumulator
+        float* partf = static_cast<float*>(args.partials);
+        int32_t* parti = static_cast<int32_t*>(args.partials);
+        const size_t slot_elems = static_cast<size_t>(kTileN) * BM;
+        const size_t my_slot = (static_cast<size_t>(blockIdx.x) * p.max_segs + u.seg) * slot_elems;
+        for (int cc = 0; cc < cols_half; cc += 8) {
+          uint32_t d[8];
+          tmem_ld8(dcol + cc, d);
+          tmem_wait_ld();
+          int32_t iv[8];
+          if (MODE == kW4A8) {
+            uint32_t prev[8];
+            if (!first_chunk) {
+              tmem_ld8(icol + cc, prev);
+              tmem_wait_ld();
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              iv[i] = __float2int_rn(__uint_as_float(d[i])) +
+                      (first_chunk ? 0 : static_cast<int32_t>(prev[i]));
+            if (!final_ev) {
+              uint32_t st[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) st[i] = static_cast<uint32_t>(iv[i]);
+              tmem_st8(icol + cc, st);
+              tmem_wait_st();
+              continue;
+            }
+          }
+          // final event: outputs or partials
+          for (int i = 0; i < 8; ++i) {
+            const int col = col0 + cc + i;
+            if (u.nslots > 1) {
+              const size_t off = my_slot + static_cast<size_t>(col) * kTileN + r;
+              if (MODE == kW4A8) parti[off] = iv[i];
+              else partf[off] = __uint_as_float(d[i]);
+            } else {
+              const int64_t m = m0 + col;
+              if (row_ok && m < M) {
+                const int64_t o = m * N + n0 + r;
+                if (MODE == kW4A8) {
+                  if (args.out_s32) static_cast<int32_t*>(args.out)[o] = iv[i];
+                  else
+                    static_cast<__half*>(args.out)[o] = __float2half_rn(
+                        static_cast<float>(iv[i]) * args.s_tok[m] * args.s_ch[n0 + r]);
+                } else {
+                  static_cast<T16*>(args.out)[o] = to_t16<T16>(__uint_as_float(d[i]));
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.dempty);
+        first_chunk = false;
+        if (!final_ev || u.nslots == 1) continue;
+
+        // ------------------------- split-K fix-up, per 32 x BM/2 sub-tile
+        __threadfence();
+        __syncwarp();
+        int prev_count = 0;
+        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + sub;
+        if (lane == 0) prev_count = atomicAdd(ctr, 1);
+        prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
+        if (prev_count != u.nslots - 1) continue;
+        __threadfence();
+        for (int cc = 0; cc < cols_half; ++cc) {
+          const int col = col0 + cc;
+          float accf = 0.f;
+          int32_t acci = 0;
+          for (int sl = 0; sl < u.nslots; ++sl) {
+            const int64_t cpr = u.cfirst + sl;
+            const int64_t seg = u.tile - sk_start(cpr, wk.T, wk.G) / wk.kb;
+            const size_t off = (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems +
+                               static_cast<size_t>(col) * kTileN + r;
+            if (MODE == kW4A8) acci += __ldcg(parti + off);
+            else accf = sl == 0 ? __ldcg(partf + off) : accf + __ldcg(partf + off);
+          }
+          const int64_t m = m0 + col;
+          if (row_ok && m < M) {
+            const int64_t o = m * N + n0 + r;
+            if (MODE == kW4A8) {
+              if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci;
+              else
+                static_cast<__half*>(args.out)[o] = __float2half_rn(
+                    static_cast<float>(acci) * args.s_tok[m] * args.s_ch[n0 + r]);
+            } else {
+              static_cast<T16*>(args.out)[o] = to_t16<T16>(accf);
+            }
+          }
+        }
+        if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const TcArgs& args,
+                      cudaStream_t s) {
+  const void* fn;
+  if (plan.mode == kW4A16_F16) fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_F16>);
+  else if (plan.mode == kW4A16_BF16)
+    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_BF16>);
+  else fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A8>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(plan.smem_bytes));
+  if (e != cudaSuccess) return e;
+  if (plan.mode == kW4A16_F16)
+    tc_gemm_kernel<kW4A16_F16><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, plan, args);
+  else if (plan.mode == kW4A16_BF16)
+    tc_gemm_kernel<kW4A16_BF16><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, plan, args);
+  else
+    tc_gemm_kernel<kW4A8><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, plan, args);
+  return cudaGetLastError();
+}
+
+}  // namespace w4

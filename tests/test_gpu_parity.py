@@ -1,0 +1,291 @@
+"""GPU parity: libw4 (through the C ABI) against the CPU oracle.
+
+Float outputs: every element within 4e-3 * sum_k|a_k w_k| + 1 ulp of the
+output type.  W4A8 int32 accumulators: bit-exact.  W4A8 fp16 outputs:
+within 1 fp16 ulp of the fp64 reference.  Small cases compare every
+element; full-size cases compare sampled elements that the oracle computes
+one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4synth
+from parity import assert_fp16_within_ulp, assert_within
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp"]
+
+
+def sched(w4, name):
+    return w4.schedule_names().index(name)
+
+
+def fmt(dt):
+    return "f16" if dt == torch.float16 else "bf16"
+
+
+def run_w4a16(w4, d, schedule=-1):
+    b = w4.prepack_B(d["w"].to(DEV), d["wtype"], d["layout"], d["K"], d["N"])
+    z = None if d["z"] is None else d["z"].to(DEV)
+    out = w4.gemm(d["a"].to(DEV), b, d["wtype"], d["N"], scales=d["s"].to(DEV), zeros=z,
+                  group_size=d["group_size"], schedule=schedule)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def oracle_w4a16(d):
+    return oracle.w4a16(d["a"], d["w"], d["layout"], d["wtype"], d["s"], d["z"], d["group_size"],
+                        d["K"], d["N"])
+
+
+def samples(M, N, count=384, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = np.concatenate([[0, M - 1, M // 2], rng.integers(0, M, count)])
+    cols = np.concatenate([[0, N - 1, min(127, N - 1)], rng.integers(0, N, count)])
+    return rows.astype(np.int64), cols.astype(np.int64)
+
+
+# ----------------------------------------------------------------- prepack ---
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_prepack_round_trip(gpu_lib, layout):
+    w4 = gpu_lib
+    K, N = 512, 200
+    w = w4synth.random_words(w4synth.packed_shape(layout, K, N), torch.Generator().manual_seed(1))
+    wd = w.to(DEV)
+    packs = {}
+    for wtype in (w4.UINT4B8, w4.UINT4, w4.INT4):
+        b = w4.prepack_B(wd, wtype, layout, K, N)
+        assert b.numel() == w4.prepacked_size(K, N)
+        back = w4.unprepack_B(b, wtype, layout, K, N)
+        assert torch.equal(back.cpu(), w)
+        packs[wtype] = b.cpu()
+    # uint4 and uint4b8 prepack identically; int4 flips the top bit of each nibble
+    assert torch.equal(packs[w4.UINT4], packs[w4.UINT4B8])
+    flipped = (packs[w4.UINT4B8].view(torch.int32) ^ int(np.int32(np.uint32(0x88888888))))
+    n_pad_words = packs[w4.INT4].view(torch.int32)
+    valid = torch.zeros(256 // 128, K // 32, 128, 4, dtype=torch.bool)
+    valid[:, :, :, :] = True
+    valid[1, :, 200 - 128:, :] = False  # padding rows stay zero
+    assert torch.equal(n_pad_words.view(2, K // 32, 128, 4)[valid],
+                       flipped.view(2, K // 32, 128, 4)[valid])
+    assert int(n_pad_words.view(2, K // 32, 128, 4)[~valid].abs().sum()) == 0
+
+
+def test_prepack_layouts_agree(gpu_lib):
+    w4 = gpu_lib
+    K, N = 256, 384
+    rng = np.random.default_rng(2)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    bufs = [w4.prepack_B(torch.from_numpy(oracle.pack(q, L)).to(DEV), w4.UINT4, L, K, N).cpu()
+            for L in (0, 1, 2)]
+    assert torch.equal(bufs[0], bufs[1]) and torch.equal(bufs[0], bufs[2])
+
+
+# ------------------------------------------------------------------- W4A16 ---
+
+@pytest.mark.parametrize("name", ALL)
+def test_tiny_w4a16_every_schedule(gpu_lib, name):
+    w4 = gpu_lib
+    d = w4synth.tiny_w4a16(seed=0)
+    got = run_w4a16(w4, d, sched(w4, name))
+    ref, absref = oracle_w4a16(d)
+    assert_within(got.double().numpy(), ref, absref, "f16", f"tiny {name}")
+
+
+@pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("zeros", [False, True])
+def test_w4a16_bf16_several_tiles(gpu_lib, name, zeros):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(40, 384, 1024, act_dtype=torch.bfloat16,
+                          wtype=w4.UINT4 if zeros else w4.UINT4B8, layout=w4.KN_SEQ,
+                          group_size=128, zeros=zeros, seed=3)
+    got = run_w4a16(w4, d, sched(w4, name))
+    ref, absref = oracle_w4a16(d)
+    assert_within(got.double().numpy(), ref, absref, "bf16", f"bf16 {name} zeros={zeros}")
+
+
+@pytest.mark.parametrize("M,N,K,gs,dt", [
+    (1, 8, 576, -1, torch.float16),       # smallest tc tile row, K not a multiple of 128
+    (3, 200, 640, 128, torch.bfloat16),   # ragged N inside a 128 tile
+    (17, 136, 512, 64, torch.bfloat16),   # group 64, ragged M and N
+    (100, 13, 256, 128, torch.float16),   # N % 8 != 0 -> CUDA-core schedule
+    (300, 256, 192, -1, torch.bfloat16),  # M spanning two 256-row tiles
+])
+def test_w4a16_ragged(gpu_lib, M, N, K, gs, dt):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=dt, wtype=w4.UINT4, layout=w4.NK_EXLLAMA,
+                          group_size=gs, zeros=True, seed=M + N)
+    got = run_w4a16(w4, d)
+    ref, absref = oracle_w4a16(d)
+    assert_within(got.double().numpy(), ref, absref, fmt(dt), f"ragged {M}x{N}x{K}")
+
+
+def test_w4a16_power_of_two_scales_exact(gpu_lib):
+    # exact products and sums: the GPU result must equal the oracle exactly
+    w4 = gpu_lib
+    M, N, K = 16, 256, 512
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4B8, group_size=128,
+                          seed=5)
+    d["s"] = torch.full_like(d["s"], 0.0625)
+    d["a"] = torch.randint(-4, 5, (M, K), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    got = run_w4a16(w4, d)
+    ref, _ = oracle_w4a16(d)
+    assert np.array_equal(got.double().numpy(), ref)
+
+
+def test_w4a16_zero_point_eight_equals_symmetric(gpu_lib):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(16, 256, 512, act_dtype=torch.bfloat16, wtype=w4.UINT4B8,
+                          group_size=128, seed=6)
+    sym = run_w4a16(w4, d)
+    d2 = dict(d, wtype=w4.UINT4, z=(d["s"].float() * 8).to(torch.bfloat16))
+    asym = run_w4a16(w4, d2)
+    assert torch.equal(sym, asym)
+
+
+@pytest.mark.parametrize("N,K", w4synth.DECODE_SHAPES)
+@pytest.mark.parametrize("M", w4synth.DECODE_M)
+def test_decode_sweep_llama3_8b(gpu_lib, N, K, M):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4,
+                          layout=w4.NK_EXLLAMA, group_size=128, zeros=True, seed=0)
+    got = run_w4a16(w4, d).double().numpy()
+    rows, cols = samples(M, N, seed=M)
+    ref, absref = oracle.w4a16_elems(d["a"], d["w"], d["layout"], d["wtype"], d["s"], d["z"], 128,
+                                     K, N, rows, cols)
+    assert_within(got[rows, cols], ref, absref, "bf16", f"decode {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("N,K,M", [(57344, 8192, 4096), (8192, 28672, 4096),
+                                   (57344, 8192, 16384)])
+def test_prefill_llama3_70b(gpu_lib, N, K, M):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4B8,
+                          layout=w4.NK_EXLLAMA, group_size=128, zeros=False, seed=0)
+    got = run_w4a16(w4, d)
+    rows, cols = samples(M, N, count=192, seed=N)
+    sub = got[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
+    ref, absref = oracle.w4a16_elems(d["a"], d["w"], d["layout"], d["wtype"], d["s"], None, 128,
+                                     K, N, rows, cols)
+    assert_within(sub, ref, absref, "bf16", f"prefill {M}x{N}x{K}")
+
+
+# -------------------------------------------------------------------- W4A8 ---
+
+def run_w4a8(w4, e, out_dtype, schedule=-1):
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], e["K"], e["N"])
+    sg = None if e["sg"] is None else e["sg"].to(DEV)
+    kw = {}
+    if out_dtype == torch.float16:
+        kw = dict(token_scales=e["s_tok"].to(DEV), channel_scales=e["s_ch"].to(DEV))
+    out = w4.gemm(e["a"].to(DEV), b, e["wtype"], e["N"], scales=sg, group_size=e["group_size"],
+                  out_dtype=out_dtype, schedule=schedule, **kw)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp"])
+@pytest.mark.parametrize("gs", [-1, 128])
+def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
+    w4 = gpu_lib
+    e = w4synth.gen_w4a8(40, 384, 2048, group_size=gs, seed=7)
+    acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
+    ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, e["K"], e["N"])
+    assert np.array_equal(acc.numpy().astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("gs", [-1, 128])
+def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
+    """Largest |partial sums| the QQQ shapes allow: int8 -128/127 against
+    int4 -8 (x group scale 16), K = 21760."""
+    w4 = gpu_lib
+    M, N, K = 4, 256, 21760
+    q = np.full((K, N), 8, dtype=np.uint8)           # int4 -8 everywhere
+    q[:, 1::2] = 7                                   # and +7 in odd columns
+    w = torch.from_numpy(oracle.pack(q, oracle.NK_EXLLAMA))
+    a = torch.full((M, K), -128, dtype=torch.int8)
+    a[1] = 127
+    a[2, ::2] = 127
+    a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(0)).to(torch.int8)
+    sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
+    e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
+    for name in ("tc16_sk", "tc128_dp", "simt"):
+        acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
+        ref = oracle.w4a8(a, w, oracle.NK_EXLLAMA, w4.INT4, sg, gs, K, N)
+        assert np.array_equal(acc.numpy().astype(np.int64), ref), name
+
+
+@pytest.mark.parametrize("M", w4synth.QQQ_CH_M)
+def test_w4a8_qqq_per_channel(gpu_lib, M):
+    w4 = gpu_lib
+    e = w4synth.gen_w4a8(M, w4synth.QQQ_N, w4synth.QQQ_K, group_size=-1, seed=0)
+    out = run_w4a8(w4, e, torch.float16).double().numpy()
+    acc = run_w4a8(w4, e, torch.int32).numpy().astype(np.int64)
+    rows, cols = samples(M, e["N"], count=256, seed=M)
+    ref_acc = oracle.w4a8_elems(e["a"], e["w"], e["layout"], e["wtype"], None, -1, e["K"],
+                                e["N"], rows, cols)
+    assert np.array_equal(acc[rows, cols], ref_acc)
+    ref = oracle.w4a8_scale(ref_acc, rows, cols, e["s_tok"], e["s_ch"])
+    assert_fp16_within_ulp(out[rows, cols], ref, f"qqq per-channel M={M}")
+
+
+@pytest.mark.parametrize("M", w4synth.QQQ_G128_M)
+def test_w4a8_qqq_g128(gpu_lib, M):
+    w4 = gpu_lib
+    e = w4synth.gen_w4a8(M, w4synth.QQQ_N, w4synth.QQQ_K, group_size=128, seed=0)
+    out = run_w4a8(w4, e, torch.float16).double().numpy()
+    acc = run_w4a8(w4, e, torch.int32).numpy().astype(np.int64)
+    rows, cols = samples(M, e["N"], count=256, seed=M)
+    ref_acc = oracle.w4a8_elems(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], 128, e["K"],
+                                e["N"], rows, cols)
+    assert np.array_equal(acc[rows, cols], ref_acc)
+    ref = oracle.w4a8_scale(ref_acc, rows, cols, e["s_tok"], e["s_ch"])
+    assert_fp16_within_ulp(out[rows, cols], ref, f"qqq g128 M={M}")
+
+
+# ------------------------------------------------------------ edge cases ---
+
+def test_empty_and_k_zero(gpu_lib):
+    w4 = gpu_lib
+    b = torch.zeros(1, dtype=torch.uint8, device=DEV)
+    s = torch.ones(1, 8, dtype=torch.float16, device=DEV)
+    out = w4.gemm(torch.empty(0, 64, dtype=torch.float16, device=DEV), b, w4.UINT4B8, 8,
+                  scales=s, group_size=-1)
+    assert out.shape == (0, 8)
+    out = torch.full((3, 8), 7.0, dtype=torch.float16, device=DEV)
+    w4.gemm(torch.empty(3, 0, dtype=torch.float16, device=DEV), b, w4.UINT4B8, 8, scales=s,
+            group_size=-1, out=out)
+    torch.cuda.synchronize()
+    assert int(out.abs().sum()) == 0
+
+
+def test_deterministic_stream_k(gpu_lib):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(16, 4096, 4096, act_dtype=torch.bfloat16, wtype=w4.UINT4,
+                          group_size=128, zeros=True, seed=9)
+    a = run_w4a16(w4, d)
+    b = run_w4a16(w4, d)
+    assert torch.equal(a, b)
+
+
+def test_check_status_clean(gpu_lib):
+    w4 = gpu_lib
+    d = w4synth.tiny_w4a16(seed=1)
+    run_w4a16(w4, d)
+    ws = w4.workspace(DEV, 256)
+    assert w4.check_status(ws) == w4.OK
+
+
+def test_invalid_on_device_pointers(gpu_lib):
+    w4 = gpu_lib
+    d = w4synth.tiny_w4a16(seed=0)
+    b = w4.prepack_B(d["w"].to(DEV), d["wtype"], d["layout"], d["K"], d["N"])
+    with pytest.raises(w4.W4Error) as ei:
+        w4.gemm(d["a"].to(DEV), b, d["wtype"], d["N"], scales=d["s"].to(DEV).bfloat16(),
+                group_size=128)
+    assert ei.value.status == w4.ERR_INVALID_ARGUMENT
