@@ -1,0 +1,444 @@
+"""Benchmark of the 4-bit-weight GEMM hot path on GB300.
+
+Workload (one "step"): the QQQ-style W4A8 per-channel sweep at N=8192,
+K=21760 — one GEMM for each M in {1, 8, 32, 128, 512, 1024} (int8
+activations with per-token fp32 scales, int4 weights with per-channel fp32
+scales, fp16 output), the shape of the pytorch/ao PR #1113 "support W4A8
+Marlin kernel" speedup sweep.  Weights are prepacked once (offline step,
+timed separately under "prepack").  Four copies of every input are rotated
+so that no launch finds its operands in L2 (4 x 89 MB > 2 x 129 MB L2).
+
+metric: TFLOP/s of the whole sweep (sum 2*M*N*K / step time); the per-M
+breakdown (microseconds, TFLOP/s, weight GB/s, roofline fraction) is in
+"sweep".  --impl reference times the CPU oracle (plain fp64/int64 C) on a
+bounded sample of the same workload.
+
+Multi-GPU (torchrun): replicas only; every rank runs the same sweep on its
+own GPU and value = all ranks' flops / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import w4synth  # noqa: E402
+
+N, K = w4synth.QQQ_N, w4synth.QQQ_K
+M_SWEEP = w4synth.QQQ_CH_M
+ROTATE = 4
+METRIC = "int4-weight GEMM TFLOP/s & weight GB/s vs M (N=8192,K=21760), % roofline"
+UNIT = "TFLOP/s"
+WORKLOAD = "W4A8 QQQ per-channel sweep M in {1,8,32,128,512,1024}, N=8192, K=21760"
+
+
+def flops(M):
+    return 2.0 * M * N * K
+
+
+def weight_bytes():
+    return K * N // 2 + 4 * N  # packed int4 + fp32 channel scales
+
+
+def algo_bytes(M):
+    # weights + int8 activations + token scales + fp16 output
+    return weight_bytes() + M * K + 4 * M + 2 * M * N
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
+                    bf16_sus=p.get("bf16_tflops_sustained", p["bf16_tflops"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen between t0 and t1
+        (time.time() values; all samples when not given)."""
+        import datetime
+
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            sms.append(sm)
+            maxes.append(mx)
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def make_inputs(dev):
+    """ROTATE copies of every input, resident in HBM (prepacked weights)."""
+    import int4_weight_mixed_gb300 as w4
+
+    sets = []
+    for r in range(ROTATE):
+        e = w4synth.gen_w4a8(1, N, K, group_size=-1, seed=100 + r)
+        w_dev = e["w"].to(dev)
+        b = w4.prepack_B(w_dev, e["wtype"], e["layout"], K, N)
+        del w_dev
+        acts = {}
+        for M in M_SWEEP:
+            x = w4synth.gen_w4a8(M, 8, K, seed=1000 * r + M)  # its a [M,K] and s_tok [M]
+            acts[M] = (x["a"].to(dev), x["s_tok"].to(dev))
+        sets.append(dict(b=b, s_ch=e["s_ch"].to(dev), acts=acts, wq=e["w"], wtype=e["wtype"]))
+    return sets
+
+
+def run_gpu(args):
+    import int4_weight_mixed_gb300 as w4
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w4.load()
+    sets = make_inputs(dev)
+    outs = {M: torch.empty((M, N), dtype=torch.float16, device=dev) for M in M_SWEEP}
+    ws = w4.workspace(dev, w4.workspace_size(max(M_SWEEP), N, K, torch.int8, -1))
+    stream = torch.cuda.current_stream(dev)
+
+    def gemm(r, M):
+        st = sets[r]
+        a, s_tok = st["acts"][M]
+        w4.gemm(a, st["b"], st["wtype"], N, scales=None, group_size=-1, token_scales=s_tok,
+                channel_scales=st["s_ch"], out=outs[M], ws=ws)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # prepack timing (offline step, not part of a step)
+    wq = sets[0]["wq"].to(dev)
+    pre_b = torch.empty_like(sets[0]["b"])
+    for _ in range(3):
+        w4.prepack_B(wq, sets[0]["wtype"], w4synth.NK_EXLLAMA, K, N, out=pre_b)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        w4.prepack_B(wq, sets[0]["wtype"], w4synth.NK_EXLLAMA, K, N, out=pre_b)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prepack_us = e0.elapsed_time(e1) * 1e3 / 10
+    del wq, pre_b
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    # eager warm-up (sets kernel attributes), then one graph per input rotation
+    for i in range(args.warmup):
+        for M in M_SWEEP:
+            gemm(i % ROTATE, M)
+    barrier()
+    step_graphs = [capture(lambda r=r: [gemm(r, M) for M in M_SWEEP]) for r in range(ROTATE)]
+    for i in range(args.warmup):
+        step_graphs[i % ROTATE].replay()
+    barrier()
+
+    # timed region: K steps of the whole sweep, graph replays on one stream
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step_graphs[i % ROTATE].replay()
+    t_end.record(stream)
+    barrier()
+    wall1 = time.time()
+    time.sleep(0.2)
+    clk = clocks.stop(wall0, wall1)
+    total_ms = t_start.elapsed_time(t_end)
+
+    # per-M launch durations: graphs of one GEMM per rotation, events on the
+    # launching stream around `reps` replays
+    per_m = {}
+    reps = max(8, min(args.steps, 100))
+    for M in M_SWEEP:
+        gs_m = [capture(lambda r=r, M=M: gemm(r, M)) for r in range(ROTATE)]
+        for r in range(ROTATE):
+            gs_m[r].replay()
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(reps):
+            gs_m[i % ROTATE].replay()
+        a1.record(stream)
+        barrier()
+        per_m[M] = [a0.elapsed_time(a1) * 1e3 / reps]
+        del gs_m
+    if w4.check_status(ws) != w4.OK:
+        raise RuntimeError("a device-side wait timed out during the benchmark")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end-to-end through the public API from pinned host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        host_a = {M: sets[0]["acts"][M][0].cpu().pin_memory() for M in M_SWEEP}
+        host_s = {M: sets[0]["acts"][M][1].cpu().pin_memory() for M in M_SWEEP}
+        host_o = {M: torch.empty((M, N), dtype=torch.float16).pin_memory() for M in M_SWEEP}
+        h2d = sum(host_a[M].numel() + 4 * host_s[M].numel() for M in M_SWEEP)
+        d2h = sum(2 * M * N for M in M_SWEEP)
+        e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for M in M_SWEEP:
+                a = host_a[M].to(dev, non_blocking=True)
+                s = host_s[M].to(dev, non_blocking=True)
+                o = w4.gemm(a, sets[0]["b"], sets[0]["wtype"], N, scales=None, group_size=-1,
+                            token_scales=s, channel_scales=sets[0]["s_ch"], ws=ws)
+                host_o[M].copy_(o, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        x1.record(stream)
+        barrier()
+        e2e_ms = x0.elapsed_time(x1) / e2e_steps
+        e2e = {"value": sum(flops(M) for M in M_SWEEP) * world / (e2e_ms * 1e-3) / 1e12,
+               "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    step_flops = sum(flops(M) for M in M_SWEEP)
+    ms_per_step = total_ms / args.steps
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    sweep = []
+    for M in M_SWEEP:
+        us = statistics.median(per_m[M])
+        tf = flops(M) / (us * 1e-6) / 1e12
+        gbs = weight_bytes() / (us * 1e-6) / 1e9
+        t_hbm = algo_bytes(M) / (pk["hbm"] * 1e9)
+        t_tc = flops(M) / (pk["bf16_sus"] * 1e12)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        frac = max(t_hbm, t_tc) / (us * 1e-6)
+        sweep.append({"M": M, "us": round(us, 2), "tflops": round(tf, 1),
+                      "weight_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(frac, 3)})
+    # dominant kernel: the largest share of the step
+    dom = max(M_SWEEP, key=lambda M: statistics.mean(per_m[M]))
+    dom_us = statistics.mean(per_m[dom])
+    roofline = {"kernel": "tc_gemm_kernel<W4A8> (+ its int8->bf16 staging launch)",
+                "M": dom, "bound": "tensor", "achieved": round(flops(dom) / (dom_us * 1e-6) / 1e12, 1),
+                "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                "peak_source": f"{pk['src']} bf16 dense, sustained",
+                "traffic": None}
+    roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 3)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": f"{ROTATE} rotated input copies > 2x L2",
+                   "parallelism": f"replicas x{world}"},
+        "sweep": sweep, "roofline": roofline, "e2e": e2e,
+        "prepack": {"us": round(prepack_us, 1),
+                    "gbs": round(2 * K * N // 2 / (prepack_us * 1e-6) / 1e9, 1)},
+        "gpu_launches": 2 * len(M_SWEEP) * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(target_s=args.cpu_seconds)
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_single(args):
+    """One GEMM of the sweep (M = args.single), eager launches: the small
+    case for ncu captures (one weight copy, ~0.2 GB on the device)."""
+    import int4_weight_mixed_gb300 as w4
+
+    dev = torch.device("cuda", 0)
+    M = args.single
+    e = w4synth.gen_w4a8(M, N, K, group_size=-1, seed=0)
+    b = w4.prepack_B(e["w"].to(dev), e["wtype"], e["layout"], K, N)
+    a, s_tok, s_ch = e["a"].to(dev), e["s_tok"].to(dev), e["s_ch"].to(dev)
+    ws = w4.workspace(dev, w4.workspace_size(M, N, K, torch.int8, -1))
+    out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    for _ in range(args.warmup + args.steps):
+        w4.gemm(a, b, e["wtype"], N, scales=None, group_size=-1, token_scales=s_tok,
+                channel_scales=s_ch, out=out, ws=ws, schedule=args.schedule)
+    torch.cuda.synchronize()
+    st = w4.check_status(ws)
+    print(json.dumps({"single_M": M, "launches": args.warmup + args.steps, "status": st}))
+    if st != w4.OK:
+        sys.exit(1)
+
+
+def oracle_sample(rows_per_m, cols, seed=0):
+    """Time the oracle on rows_per_m sampled rows x `cols` columns of every
+    M of the sweep (full K).  Returns (seconds, flops)."""
+    import oracle
+
+    e = w4synth.gen_w4a8(1, N, K, group_size=-1, seed=seed)
+    total_flops, total_s = 0.0, 0.0
+    for M in M_SWEEP:
+        g = torch.Generator().manual_seed(M)
+        rows_n = min(rows_per_m, M)
+        a = torch.randint(-127, 128, (rows_n, K), generator=g, dtype=torch.int32).to(torch.int8)
+        rows = np.repeat(np.arange(rows_n), cols.size)
+        cc = np.tile(cols, rows_n)
+        t0 = time.perf_counter()
+        acc = oracle.w4a8_elems(a, e["w"], e["layout"], e["wtype"], None, -1, K, N, rows, cc)
+        oracle.w4a8_scale(acc, rows, cc, np.ones(rows_n), e["s_ch"])
+        total_s += time.perf_counter() - t0
+        total_flops += 2.0 * K * rows.size
+    return total_s, total_flops
+
+
+def cpu_baseline(target_s=10.0):
+    """The oracle, as it stands, on a bounded sample sized to ~target_s."""
+    import oracle
+
+    cols = np.arange(0, N, 64, dtype=np.int64)  # 128 columns
+    s, f = oracle_sample(1, cols)
+    rate = f / max(s, 1e-6)
+    per_row = 2.0 * K * N  # flops of one row x all columns
+    rows = 1
+    while rows < 64 and (rows * 2) * per_row * 5 / rate <= target_s:
+        rows *= 2
+    cols2 = np.arange(N, dtype=np.int64)
+    s2, f2 = oracle_sample(rows, cols2)
+    return {"value": f2 / s2 / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"min(M,{rows}) rows of each M x all {N} columns x full K={K} "
+                      f"({f2 / 2:.3g} MACs in {s2:.1f} s)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    cols = np.arange(0, N, 512, dtype=np.int64)  # 16 columns per M per step
+    for _ in range(args.warmup):
+        oracle_sample(1, cols[:2])
+    times, fl = [], 0.0
+    for i in range(args.steps):
+        s, f = oracle_sample(1, cols, seed=i % 2)
+        times.append(s)
+        fl = f
+    ms = 1e3 * sum(times) / len(times)
+    value = fl / (ms * 1e-3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "per step: 1 row of "
+                                            "each M x 16 columns x full K"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "1 row of each M x 16 columns x full K per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--single", type=int, default=0, help="run only the GEMM with this M")
+    ap.add_argument("--schedule", type=int, default=-1)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.single:
+        run_single(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
