@@ -162,6 +162,36 @@ int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t gro
  * timeout the split-K counters are zeroed again. */
 w4_status w4_check_status(void* workspace, size_t workspace_bytes, void* stream);
 
+/* w4_gemm without a workspace argument.  The source pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory where they run the GEMM (a plug-in inside a
+ * framework that owns all device memory and offers its extensions no
+ * allocator, or a latency-critical loop that must not call cudaMalloc,
+ * which can synchronize the whole device).
+ *
+ * Arguments and results are those of w4_gemm; the caller still passes every
+ * input and the output.  Instead of a workspace, the call uses a scratch
+ * array of W4_NOALLOC_SCRATCH_BYTES compiled into the library: it exists once
+ * on every GPU that loads libw4 and stays allocated until the process exits.
+ * The call allocates and frees nothing (no cudaMalloc, no allocating library
+ * routine).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call clears the status word and split-K counters of the scratch
+ *     on `stream`, then runs exactly what w4_gemm would.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, other host
+ *     threads) race and may corrupt each other's results.  Order them.
+ *   - A problem whose scratch need is above W4_NOALLOC_SCRATCH_BYTES is
+ *     rejected before anything runs, with W4_ERR_WORKSPACE (w4_last_error()
+ *     names the bytes it would need); use w4_gemm with a workspace then. */
+#define W4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+w4_status w4_gemm_noalloc(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                          int wtype, int64_t N, const void* b_scales, int scale_type,
+                          const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                          const float* ch_scales, void* out, int out_type, void* stream);
+
 /* Static text for a status code; message of the last failed call on this
  * host thread ("" when none). */
 const char* w4_status_string(int status);
