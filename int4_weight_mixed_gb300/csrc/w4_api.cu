@@ -77,15 +77,32 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   TcPlan p{};
   p.mode = mode;
   p.bm = sc.bm;
-  p.stages = tc_max_stages(p.bm, mode);
-  p.smem_bytes = tc_smem_bytes(p.bm, mode, p.stages);
+  // K depth of a pipeline stage: skinny tiles need >= 8 KB of nibbles per
+  // stage to hide the per-stage cost of the producer; wide tiles are
+  // compute-bound and take shallower stages so that several fit in shared
+  // memory.
+  int nsub = p.bm <= 64 ? 4 : (p.bm <= 128 ? 2 : 1);
+  const int64_t G = K / gs;
+  if (G > 1)  // a stage must cover whole groups or lie inside one group
+    while (nsub > 1 && (nsub * kStageK) % gs != 0 && gs % (nsub * kStageK) != 0) nsub /= 2;
+  p.nsub = nsub;
+  p.gps = (G > 1 && gs < nsub * kStageK) ? static_cast<int>(nsub * kStageK / gs) : 1;
+  p.stages = tc_max_stages(p.bm, nsub);
+  p.smem_bytes = tc_smem_bytes(p.bm, nsub, p.stages);
+  const int dcols = p.bm * (mode == kW4A8 ? 2 : 1);  // W4A8 keeps an int32 copy beside D
+  p.acol = (dcols + 31) / 32 * 32;
+  int ts = (512 - p.acol) / (nsub * 32);
+  if (ts > kMaxTmemStages) ts = kMaxTmemStages;
+  if (ts > p.stages - 1) ts = p.stages - 1;
+  p.tstages = ts;
   p.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
   p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
   p.tiles = p.m_tiles * p.n_tiles;
-  p.kb_total = static_cast<int>(K / kStageK);
+  p.k64 = static_cast<int>(K / kStageK);
+  p.kb_total = (p.k64 + nsub - 1) / nsub;
   // W4A8 exactness: |a| <= 128 and |v*sg| <= 128 (group) or |v| <= 8
   // (per-channel) keep every fp32 partial sum of a chunk within 2^24.
-  p.chunk_stages = (gs < K) ? 1024 / kStageK : 16384 / kStageK;
+  p.chunk_stages = static_cast<int>(((gs < K) ? 1024 : 16384) / (kStageK * nsub));
   const int sms = sm_count();
   p.decomp = sc.decomp;
   if (p.tiles * static_cast<size_t>(kConvWarps) * 4 > kCounterBytes) p.decomp = kDataParallel;
@@ -96,7 +113,7 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
     p.ws_partials = p.ws_counters + kCounterBytes;
   } else {
     const int64_t T = static_cast<int64_t>(p.tiles) * p.kb_total;
-    int64_t g = T / 4;  // at least 4 stages per CTA
+    int64_t g = T / 2;  // at least 2 stages per CTA
     if (g > sms) g = sms;
     if (g < 1) g = 1;
     p.grid = static_cast<int>(g);
@@ -358,19 +375,46 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   }
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  CUtensorMap amap;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(plan.bm)};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&amap,
-                   pr.mode == kW4A16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   2, const_cast<void*>(act), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  cudaError_t e = launch_tc(plan, amap, args, s);
+  CUtensorMap amap, smap, zmap;
+  memset(&smap, 0, sizeof(smap));
+  memset(&zmap, 0, sizeof(zmap));
+  const CUtensorMapDataType t16 =
+      pr.mode == kW4A16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(plan.bm)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&amap, t16, 2, const_cast<void*>(act), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed (%d)", (int)r);
+  }
+  // [G][N] scale / zero-point rows: one box of 128 columns x gps groups per stage
+  auto row_map = [&](CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz,
+                     const char* what) -> w4_status {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / pr.gs)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * esz};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(plan.gps)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled (%s) failed (%d)", what, (int)r);
+    return W4_OK;
+  };
+  if (b_scales) {
+    w4_status st2 = pr.mode == kW4A8
+                        ? row_map(&smap, b_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, "group scales")
+                        : row_map(&smap, b_scales, t16, 2, "scales");
+    if (st2 != W4_OK) return st2;
+  }
+  if (b_zeros) {
+    w4_status st2 = row_map(&zmap, b_zeros, t16, 2, "zero-points");
+    if (st2 != W4_OK) return st2;
+  }
+  cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
 }
 

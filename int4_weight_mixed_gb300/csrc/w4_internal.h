@@ -16,12 +16,15 @@ constexpr int kLayoutVersion = 1;
 // 4-7/20-23 the pair (k0+2, k0+3), and so on.
 constexpr int kTileN = 128;
 constexpr int kChunkK = 32;
-constexpr int kStageK = 64;
+constexpr int kStageK = 64;   // K granularity: one 128-byte swizzled activation row
 constexpr int kMaxStages = 32;
-constexpr int kTmemStages = 4;
-constexpr int kTmemACol = 256;  // first tensor-memory column of the A stages
-constexpr int kConvWarps = 8;
-constexpr int kTcThreads = 64 + 32 * kConvWarps;  // producer, MMA, 8 converter warps
+constexpr int kMaxTmemStages = 8;
+// Converter warps work in groups of four (one warp per tensor-memory lane
+// quadrant); group g converts the pipeline stages it with
+// it % kConvGroups == g, so kConvGroups stages are in conversion at once.
+constexpr int kConvGroups = 4;
+constexpr int kConvWarps = 4 * kConvGroups;
+constexpr int kTcThreads = 64 + 32 * kConvWarps;  // producer, MMA, converter warps
 constexpr size_t kWsHeader = 256;                // status word + spare
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
@@ -40,9 +43,14 @@ struct Schedule {
 struct TcPlan {
   int mode;
   int bm;
-  int stages;
+  int nsub;            // 64-wide K blocks per pipeline stage (1, 2 or 4)
+  int stages;          // shared-memory pipeline stages
+  int tstages;         // tensor-memory A stages (nsub * 32 columns each)
+  int acol;            // first tensor-memory column of the A stages
+  int gps;             // scale / zero-point rows per stage (groups it spans)
   int m_tiles, n_tiles, tiles;
-  int kb_total;        // K / 64
+  int kb_total;        // pipeline stages per tile: ceil(K / (64 * nsub))
+  int k64;             // K / 64
   int grid;            // CTAs
   int decomp;
   int max_segs;        // partial slots per CTA (stream-K)
@@ -77,9 +85,10 @@ cudaError_t launch_unprepack(const uint8_t* packed, int wtype, int layout, int64
                              int64_t N, int32_t* w_q, cudaStream_t s);
 cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_t s);
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s);
-cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const TcArgs& args,
-                      cudaStream_t s);
-size_t tc_smem_bytes(int bm, int mode, int stages);
-int tc_max_stages(int bm, int mode);
+cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                      const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
+size_t tc_stage_bytes(int bm, int nsub);
+size_t tc_smem_bytes(int bm, int nsub, int stages);
+int tc_max_stages(int bm, int nsub);
 
 }  // namespace w4

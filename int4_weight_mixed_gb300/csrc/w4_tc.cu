@@ -7,17 +7,21 @@
 // which is the transposed statement of out = a x w_hat (the Machete Readme,
 // "Overview", writes the weight on the left of "@ a").
 //
-// Data flow per 64-wide K stage:
-//   producer warp : TMA tile of the activations (128B-swizzled, K-major)
-//                   + one 4 KB bulk copy of the prepacked nibbles
-//                   + the stage's scale / zero-point rows
+// Data flow per pipeline stage (nsub = 1, 2 or 4 blocks of 64 K; the
+// stage is sized so that every stage moves >= 8 KB of nibbles for skinny
+// tiles, because each stage costs the single producer thread a few hundred
+// cycles whatever its size):
+//   producer warp : nsub TMA tiles of the activations (128B-swizzled,
+//                   K-major) + one bulk copy of the stage's prepacked nibbles
+//                   + one TMA box each of scale / zero-point rows
 //   8 converter warps : nibbles -> 16-bit weights in registers, one fused
 //                   multiply-add per pair with the scale and pre-scaled
 //                   zero-point (Machete Readme "Overview" NOTE), stored
 //                   straight into tensor memory (tcgen05.st): dequantized
 //                   weights never touch shared memory
-//   MMA thread    : 4 x tcgen05.mma (K = 16) with A from tensor memory and
-//                   B from shared memory, fp32 accumulator in tensor memory
+//   MMA thread    : 4 * nsub tcgen05.mma (K = 16) with A from tensor memory
+//                   and B from shared memory, fp32 accumulator in tensor
+//                   memory; one commit per stage releases the stage
 //   epilogue      : converter warps drain the accumulator (tcgen05.ld),
 //                   convert / scale and store, or write split-K partials and
 //                   let the last arriving warp of each sub-tile reduce them.
@@ -164,55 +168,59 @@ __device__ __forceinline__ __nv_bfloat16 to_t16<__nv_bfloat16>(float x) {
 }
 
 struct Smem {
-  uint8_t* a;      // stages x BM x 128 B
-  uint8_t* w;      // stages x 4096 B
-  uint8_t* s;      // stages x 256 B
-  uint8_t* z;      // stages x 256 B
-  uint64_t* full;  // [stages]
-  uint64_t* empty; // [stages]
-  uint64_t* tfull; // [kTmemStages]
-  uint64_t* tempty;
-  uint64_t* dfull;
-  uint64_t* dempty;
-  uint64_t* fin;
+  uint8_t* a;       // stages x nsub x BM x 128 B  (128B-swizzled activation tiles)
+  uint8_t* w;       // stages x nsub x 4096 B      (prepacked nibbles)
+  uint8_t* s;       // stages x nsub x 256 B       (scale rows, up to nsub groups)
+  uint8_t* z;       // stages x nsub x 256 B       (zero-point rows)
+  uint64_t* full;   // [kMaxStages]  TMA bytes landed
+  uint64_t* empty;  // [kMaxStages]  stage consumed (converter group + MMA commit)
+  uint64_t* tfull;  // [kMaxTmemStages] converted weights stored in tensor memory
+  uint64_t* dfull;  // accumulator ready for the epilogue
+  uint64_t* dempty; // accumulator drained
+  uint64_t* fin;    // all MMAs retired (before tensor memory is freed)
   uint32_t* tmem_slot;
   int* abort;
 };
 
 }  // namespace
 
-size_t tc_smem_bytes(int bm, int /*mode*/, int stages) {
-  size_t per_stage = static_cast<size_t>(bm) * 128 + 4096 + 256 + 256;
-  size_t bars = (2 * kMaxStages + 2 * kTmemStages + 3) * 8;
-  return 1024 + per_stage * stages + bars + 64;
+size_t tc_stage_bytes(int bm, int nsub) {
+  return static_cast<size_t>(nsub) * (static_cast<size_t>(bm) * 128 + 4096 + 256 + 256);
 }
 
-int tc_max_stages(int bm, int mode) {
+size_t tc_smem_bytes(int bm, int nsub, int stages) {
+  const size_t bars = (2 * kMaxStages + kMaxTmemStages + 3) * 8;
+  return 1024 + tc_stage_bytes(bm, nsub) * stages + bars + 64;
+}
+
+int tc_max_stages(int bm, int nsub) {
   const size_t budget = 225 * 1024;
   int s = kMaxStages;
-  while (s > 2 && tc_smem_bytes(bm, mode, s) > budget) --s;
+  while (s > 2 && tc_smem_bytes(bm, nsub, s) > budget) --s;
   return s;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap amap, const TcPlan p, const TcArgs args) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                   const __grid_constant__ CUtensorMap smap,
+                   const __grid_constant__ CUtensorMap zmap, const TcPlan p, const TcArgs args) {
   using T16 = typename std::conditional<MODE == kW4A16_F16, __half, __nv_bfloat16>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int S = p.stages, BM = p.bm;
+  const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages;
+  const uint32_t a_sub = static_cast<uint32_t>(BM) * 128;  // bytes of one 64-K activation tile
   Smem sm;
   sm.a = base;
-  sm.w = sm.a + static_cast<size_t>(S) * BM * 128;
-  sm.s = sm.w + static_cast<size_t>(S) * 4096;
-  sm.z = sm.s + static_cast<size_t>(S) * 256;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * 256);
+  sm.w = sm.a + static_cast<size_t>(S) * NS * a_sub;
+  sm.s = sm.w + static_cast<size_t>(S) * NS * 4096;
+  sm.z = sm.s + static_cast<size_t>(S) * NS * 256;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * NS * 256);
   sm.full = bars;
   sm.empty = bars + kMaxStages;
   sm.tfull = bars + 2 * kMaxStages;
-  sm.tempty = sm.tfull + kTmemStages;
-  sm.dfull = sm.tempty + kTmemStages;
+  sm.dfull = sm.tfull + kMaxTmemStages;
   sm.dempty = sm.dfull + 1;
   sm.fin = sm.dempty + 1;
   sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.fin + 1);
@@ -224,18 +232,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kConvWarps + 1);
+      mbar_init(&sm.empty[i], 4 + 1);  // one converter group + the MMA commit
     }
-    for (int i = 0; i < kTmemStages; ++i) {
-      mbar_init(&sm.tfull[i], kConvWarps);
-      mbar_init(&sm.tempty[i], 1);
-    }
+    for (int i = 0; i < TS; ++i) mbar_init(&sm.tfull[i], 4);
     mbar_init(sm.dfull, 1);
     mbar_init(sm.dempty, kConvWarps);
     mbar_init(sm.fin, 1);
     *sm.abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&amap);
+    if (args.scales) prefetch_tensormap(&smap);
+    if (args.zeros) prefetch_tensormap(&zmap);
   }
   if (warp == 0) {
     tmem_alloc(sm.tmem_slot, 512);
@@ -256,44 +263,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int64_t M = args.M, N = args.N, K = args.K;
   const int gsz = static_cast<int>(args.group_size);
+  const int sub_per_group = gsz / kStageK;  // 64-K blocks per scale group
+  const int esz = MODE == kW4A8 ? 1 : 2;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Per stage: one wait, one expect-tx, nsub activation boxes, one bulk
+    // copy of the stage's nibbles and one box per scale / zero-point map.
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       Unit u;
+      const uint32_t a0 = smem_addr(sm.a), w0 = smem_addr(sm.w);
+      const uint32_t s0 = smem_addr(sm.s), z0 = smem_addr(sm.z);
+      const uint32_t full0 = smem_addr(sm.full);
+      const uint32_t sc_bytes = args.scales ? static_cast<uint32_t>(128 * p.gps * esz) : 0;
+      const uint32_t zp_bytes = args.zeros ? static_cast<uint32_t>(128 * p.gps * 2) : 0;
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         int mt, nt;
         tile_coords(p, u.tile, mt, nt);
-        const int64_t n0 = static_cast<int64_t>(nt) * kTileN;
-        const int valid_n = static_cast<int>(N - n0 < kTileN ? N - n0 : kTileN);
+        const int32_t n0 = nt * kTileN;
+        const int32_t y = mt * BM;
+        const uint8_t* wsrc =
+            args.b_packed +
+            ((static_cast<int64_t>(nt) * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * 2) *
+             kTileN) * 16;
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
           if (!mbar_wait(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
-          const int64_t g = static_cast<int64_t>(kb) * kStageK / gsz;
-          uint32_t sbytes = 0, zbytes = 0;
-          if (MODE == kW4A8) {
-            if (args.scales) sbytes = valid_n;
-          } else {
-            sbytes = valid_n * 2;
-            if (args.zeros) zbytes = valid_n * 2;
+          const int k64_0 = kb * NS;
+          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
+          const uint32_t fb = full0 + s * 8;
+          mbar_arrive_expect_tx_a(fb, nv * (a_sub + 4096) + sc_bytes + zp_bytes);
+          for (int j = 0; j < nv; ++j)
+            tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * kStageK, y, fb);
+          bulk_g2s_a(w0 + s * NS * 4096, wsrc, nv * 4096, fb);
+          if (sc_bytes || zp_bytes) {
+            const int g0 = k64_0 / sub_per_group;
+            if (sc_bytes) tma_load_2d_a(s0 + s * NS * 256, &smap, n0, g0, fb);
+            if (zp_bytes) tma_load_2d_a(z0 + s * NS * 256, &zmap, n0, g0, fb);
           }
-          mbar_arrive_expect_tx(&sm.full[s], BM * 128 + 4096 + sbytes + zbytes);
-          tma_load_2d(sm.a + static_cast<size_t>(s) * BM * 128, &amap, kb * kStageK, mt * BM,
-                      &sm.full[s]);
-          const uint8_t* wsrc =
-              args.b_packed + ((static_cast<int64_t>(nt) * (K / kChunkK) + kb * 2) * kTileN) * 16;
-          bulk_g2s(sm.w + static_cast<size_t>(s) * 4096, wsrc, 4096, &sm.full[s]);
-          if (sbytes) {
-            const uint8_t* src = static_cast<const uint8_t*>(args.scales) +
-                                 (g * N + n0) * (MODE == kW4A8 ? 1 : 2);
-            bulk_g2s(sm.s + s * 256, src, sbytes, &sm.full[s]);
-          }
-          if (zbytes) {
-            const uint8_t* src = static_cast<const uint8_t*>(args.zeros) + (g * N + n0) * 2;
-            bulk_g2s(sm.z + s * 256, src, zbytes, &sm.full[s]);
+          wsrc += NS * 4096;
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1;
           }
         }
       }
@@ -308,30 +320,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
-      uint32_t it = 0, ev = 0;
+      const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
+      const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
+      uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0;
       bool ok = true;
       Unit u;
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         bool chunk_start = true;
         const int nkb = u.kb1 - u.kb0;
-        for (int j = 0; j < nkb; ++j, ++it) {
+        for (int j = 0; j < nkb; ++j) {
           if (chunk_start && ev > 0) {
             if (!mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) { ok = false; break; }
           }
-          const int s = it % S, ts = it % kTmemStages;
-          if (!mbar_wait(&sm.tfull[ts], (it / kTmemStages) & 1, abort, args.status) ||
-              !mbar_wait(&sm.full[s], (it / S) & 1, abort, args.status)) {
+          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status) ||
+              !mbar_wait(&sm.full[s], ph, abort, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_addr(sm.a + static_cast<size_t>(s) * BM * 128);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_ts(tmem, tmem + kTmemACol + ts * 32 + kk * 8, sw128_kmajor_desc(a_base + kk * 32),
-                   idesc, (chunk_start && kk == 0) ? 0u : 1u);
-          }
-          mma_commit(&sm.tempty[ts]);
+          const int k64_0 = (u.kb0 + j) * NS;
+          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+          const uint32_t acol = tmem + p.acol + ts * NS * 32;
+          const uint64_t dsc = desc0 + s * NS * sub16;
+          mma_ts_stage(tmem, acol, dsc, idesc, chunk_start ? 0u : 1u);
+          for (int q = 1; q < nv; ++q) mma_ts_stage(tmem, acol + q * 32, dsc + q * sub16, idesc, 1u);
           mma_commit(&sm.empty[s]);
           chunk_start = false;
           const bool chunk_end =
@@ -340,6 +352,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_commit(sm.dfull);
             ++ev;
             chunk_start = true;
+          }
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1;
+          }
+          if (++ts == static_cast<uint32_t>(TS)) {
+            ts = 0;
+            tph ^= 1;
           }
         }
       }
@@ -350,13 +370,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ----------------------------------------------- converters + epilogue
-    const int q = warp & 3;            // tensor-memory lane quadrant
-    const int c = (warp - 2) >> 2;     // which 32-K chunk of a stage, and which column half
+    const int cw = warp - 2;           // converter warp index 0..kConvWarps-1
+    const int grp = cw >> 2;           // group: converts stages it % kConvGroups == grp
+    const int q = warp & 3;            // tensor-memory lane quadrant of this warp
     const int r = q * 32 + lane;       // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const int cols_half = BM / 2;
-    const int col0 = c * cols_half;
-    const int sub = warp - 2;          // sub-tile id (quadrant x column half)
+    const int nblk = BM / 8;           // 8-column blocks of the accumulator
     uint32_t it = 0, ev = 0;
     bool ok = true;
     Unit u;
@@ -370,52 +389,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nkb = u.kb1 - u.kb0;
       bool first_chunk = true;
       for (int j = 0; j < nkb; ++j, ++it) {
-        const int s = it % S, ts = it % kTmemStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], (it / S) & 1, abort, args.status))) {
-          ok = false;
-          break;
-        }
-        const uint4 wv =
-            *reinterpret_cast<const uint4*>(sm.w + static_cast<size_t>(s) * 4096 + (c * 128 + r) * 16);
-        uint32_t s2 = 0, nz2 = 0;
-        bool has_s = true;
-        if (MODE == kW4A8) {
-          has_s = args.scales != nullptr;
-          if (has_s && row_ok) {
-            const float sg = static_cast<float>(reinterpret_cast<const int8_t*>(sm.s + s * 256)[r]);
-            s2 = as_u32(__float2bfloat162_rn(sg));
+        if (static_cast<int>(it % kConvGroups) == grp) {
+          const uint32_t s = it % S, ts = it % TS;
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], (it / S) & 1, abort, args.status))) {
+            ok = false;
+            break;
           }
-        } else if (row_ok) {
-          const uint16_t sv = reinterpret_cast<const uint16_t*>(sm.s + s * 256)[r];
-          s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
-          if (args.zeros) {
-            const uint16_t zv = reinterpret_cast<const uint16_t*>(sm.z + s * 256)[r] ^ 0x8000u;
-            nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
+          if (it >= static_cast<uint32_t>(TS)) {
+            // the tensor-memory slot is free once the MMA of stage it-TS retired
+            const uint32_t pit = it - TS;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&sm.empty[pit % S], (pit / S) & 1, abort, args.status))) {
+              ok = false;
+              break;
+            }
           }
-        }
-        uint32_t v[16];
-        convert_chunk<MODE>(wv, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v);
-        if (!row_ok) {
+          tc_fence_after();
+          const int k64_0 = (u.kb0 + j) * NS;
+          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+          const int g0 = k64_0 / sub_per_group;
+          const uint8_t* wst = sm.w + static_cast<size_t>(s) * NS * 4096;
+          const uint8_t* sst = sm.s + static_cast<size_t>(s) * NS * 256;
+          const uint8_t* zst = sm.z + static_cast<size_t>(s) * NS * 256;
+          const uint32_t tcol = tmem + lane_base + p.acol + ts * NS * 32;
+          for (int qq = 0; qq < nv; ++qq) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
+            const int grow = (k64_0 + qq) / sub_per_group - g0;
+            uint32_t s2 = 0, nz2 = 0;
+            bool has_s = true;
+            if (MODE == kW4A8) {
+              has_s = args.scales != nullptr;
+              if (has_s) {
+                const float sg = static_cast<float>(
+                    reinterpret_cast<const int8_t*>(sst + grow * 128)[r]);
+                s2 = as_u32(__float2bfloat162_rn(sg));
+              }
+            } else {
+              const uint16_t sv = reinterpret_cast<const uint16_t*>(sst + grow * 256)[r];
+              s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
+              if (args.zeros) {
+                const uint16_t zv = reinterpret_cast<const uint16_t*>(zst + grow * 256)[r] ^ 0x8000u;
+                nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
+              }
+            }
+            uint32_t v[32];
+            uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+            uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
+            convert_chunk<MODE>(w0, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v0);
+            convert_chunk<MODE>(w1, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v1);
+            if (!row_ok) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0;
-        }
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&sm.tempty[ts], ((it / kTmemStages) & 1) ^ 1, abort, args.status))) {
-          ok = false;
-          break;
-        }
-        tmem_st16(tmem + lane_base + kTmemACol + ts * 32 + c * 16, v);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm.tfull[ts]);
-          mbar_arrive(&sm.empty[s]);
+              for (int i = 0; i < 32; ++i) v[i] = 0;
+            }
+            tmem_st32(tcol + qq * 32, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sm.tfull[ts]);
+            mbar_arrive(&sm.empty[s]);
+          }
         }
         const bool chunk_end =
             (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
         if (!chunk_end) continue;
-
         // ------------------------------------------------ drain an event
         if (!__all_sync(0xffffffffu, mbar_wait(sm.dfull, ev & 1, abort, args.status))) {
           ok = false;
@@ -424,21 +463,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ++ev;
         tc_fence_after();
         const bool final_ev = (j == nkb - 1);
-        const uint32_t dcol = tmem + lane_base + col0;
-        const uint32_t icol = dcol + BM;  // W4A8 int32 accumulator
         float* partf = static_cast<float*>(args.partials);
         int32_t* parti = static_cast<int32_t*>(args.partials);
         const size_t slot_elems = static_cast<size_t>(kTileN) * BM;
         const size_t my_slot = (static_cast<size_t>(blockIdx.x) * p.max_segs + u.seg) * slot_elems;
-        for (int cc = 0; cc < cols_half; cc += 8) {
+        for (int b = grp; b < nblk; b += kConvGroups) {
+          const int cc = b * 8;
+          const uint32_t dcol = tmem + lane_base + cc;
           uint32_t d[8];
-          tmem_ld8(dcol + cc, d);
+          tmem_ld8(dcol, d);
           tmem_wait_ld();
           int32_t iv[8];
           if (MODE == kW4A8) {
+            const uint32_t icol = dcol + BM;  // int32 running sum of earlier chunks
             uint32_t prev[8];
             if (!first_chunk) {
-              tmem_ld8(icol + cc, prev);
+              tmem_ld8(icol, prev);
               tmem_wait_ld();
             }
 #pragma unroll
@@ -449,14 +489,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               uint32_t st[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) st[i] = static_cast<uint32_t>(iv[i]);
-              tmem_st8(icol + cc, st);
+              tmem_st8(icol, st);
               tmem_wait_st();
               continue;
             }
           }
           // final event: outputs or partials
+#pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int col = col0 + cc + i;
+            const int col = cc + i;
             if (u.nslots > 1) {
               const size_t off = my_slot + static_cast<size_t>(col) * kTileN + r;
               if (MODE == kW4A8) parti[off] = iv[i];
@@ -483,37 +524,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         first_chunk = false;
         if (!final_ev || u.nslots == 1) continue;
 
-        // ------------------------- split-K fix-up, per 32 x BM/2 sub-tile
+        // ------------------- split-K fix-up, per (lane quadrant, group) sub-tile
         __threadfence();
         __syncwarp();
         int prev_count = 0;
-        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + sub;
+        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + cw;
         if (lane == 0) prev_count = atomicAdd(ctr, 1);
         prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
         if (prev_count != u.nslots - 1) continue;
         __threadfence();
-        for (int cc = 0; cc < cols_half; ++cc) {
-          const int col = col0 + cc;
-          float accf = 0.f;
-          int32_t acci = 0;
-          for (int sl = 0; sl < u.nslots; ++sl) {
-            const int64_t cpr = u.cfirst + sl;
-            const int64_t seg = u.tile - sk_start(cpr, wk.T, wk.G) / wk.kb;
-            const size_t off = (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems +
-                               static_cast<size_t>(col) * kTileN + r;
-            if (MODE == kW4A8) acci += __ldcg(parti + off);
-            else accf = sl == 0 ? __ldcg(partf + off) : accf + __ldcg(partf + off);
-          }
-          const int64_t m = m0 + col;
-          if (row_ok && m < M) {
-            const int64_t o = m * N + n0 + r;
-            if (MODE == kW4A8) {
-              if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci;
-              else
-                static_cast<__half*>(args.out)[o] = __float2half_rn(
-                    static_cast<float>(acci) * args.s_tok[m] * args.s_ch[n0 + r]);
-            } else {
-              static_cast<T16*>(args.out)[o] = to_t16<T16>(accf);
+        for (int b = grp; b < nblk; b += kConvGroups) {
+          for (int i = 0; i < 8; ++i) {
+            const int col = b * 8 + i;
+            float accf = 0.f;
+            int32_t acci = 0;
+            for (int sl = 0; sl < u.nslots; ++sl) {
+              const int64_t cpr = u.cfirst + sl;
+              const int64_t seg = u.tile - sk_start(cpr, wk.T, wk.G) / wk.kb;
+              const size_t off = (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems +
+                                 static_cast<size_t>(col) * kTileN + r;
+              if (MODE == kW4A8) acci += __ldcg(parti + off);
+              else accf = sl == 0 ? __ldcg(partf + off) : accf + __ldcg(partf + off);
+            }
+            const int64_t m = m0 + col;
+            if (row_ok && m < M) {
+              const int64_t o = m * N + n0 + r;
+              if (MODE == kW4A8) {
+                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci;
+                else
+                  static_cast<__half*>(args.out)[o] = __float2half_rn(
+                      static_cast<float>(acci) * args.s_tok[m] * args.s_ch[n0 + r]);
+              } else {
+                static_cast<T16*>(args.out)[o] = to_t16<T16>(accf);
+              }
             }
           }
         }
@@ -530,8 +573,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const TcArgs& args,
-                      cudaStream_t s) {
+
+cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                      const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
   const void* fn;
   if (plan.mode == kW4A16_F16) fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_F16>);
   else if (plan.mode == kW4A16_BF16)
@@ -541,11 +585,14 @@ cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const TcArgs&
                                        static_cast<int>(plan.smem_bytes));
   if (e != cudaSuccess) return e;
   if (plan.mode == kW4A16_F16)
-    tc_gemm_kernel<kW4A16_F16><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, plan, args);
+    tc_gemm_kernel<kW4A16_F16>
+        <<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
   else if (plan.mode == kW4A16_BF16)
-    tc_gemm_kernel<kW4A16_BF16><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, plan, args);
+    tc_gemm_kernel<kW4A16_BF16>
+        <<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
   else
-    tc_gemm_kernel<kW4A8><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, plan, args);
+    tc_gemm_kernel<kW4A8><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, smap, zmap, plan,
+                                                                          args);
   return cudaGetLastError();
 }
 
