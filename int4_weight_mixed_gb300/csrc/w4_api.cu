@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -381,15 +382,31 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   const CUtensorMapDataType t16 =
       pr.mode == kW4A16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(plan.bm)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&amap, t16, 2, const_cast<void*>(act), dims, strides, box, estr,
+    // Preferred: one 3-D box {64, BM, nsub} per stage over the view
+    // (k % 64, m, k / 64); strides K*2 and 128 bytes.  Fallback: 2-D boxes.
+    const cuuint64_t dims3[3] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(M),
+                                 static_cast<cuuint64_t>(K / kStageK)};
+    const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    const cuuint32_t box3[3] = {static_cast<cuuint32_t>(kStageK),
+                                static_cast<cuuint32_t>(plan.bm),
+                                static_cast<cuuint32_t>(plan.nsub)};
+    const cuuint32_t estr3[3] = {1, 1, 1};
+    CUresult r = enc(&amap, t16, 3, const_cast<void*>(act), dims3, strides3, box3, estr3,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-      return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed (%d)", (int)r);
+    plan.a3d = r == CUDA_SUCCESS ? 1 : 0;
+    if (!plan.a3d) {
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK),
+                                 static_cast<cuuint32_t>(plan.bm)};
+      const cuuint32_t estr[2] = {1, 1};
+      r = enc(&amap, t16, 2, const_cast<void*>(act), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS)
+        return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed (%d)", (int)r);
+    }
   }
   // [G][N] scale / zero-point rows: one box of 128 columns x gps groups per stage
   auto row_map = [&](CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esz,
@@ -414,6 +431,14 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
     w4_status st2 = row_map(&zmap, b_zeros, t16, 2, "zero-points");
     if (st2 != W4_OK) return st2;
   }
+  static const bool debug = getenv("W4_DEBUG") != nullptr;
+  if (debug)
+    fprintf(stderr,
+            "w4: %s M=%lld N=%lld K=%lld bm=%d nsub=%d stages=%d tstages=%d acol=%d gps=%d "
+            "a3d=%d tiles=%d kb=%d grid=%d decomp=%d segs=%d smem=%zu\n",
+            kSchedules[si].name, (long long)M, (long long)N, (long long)K, plan.bm, plan.nsub,
+            plan.stages, plan.tstages, plan.acol, plan.gps, plan.a3d, plan.tiles, plan.kb_total,
+            plan.grid, plan.decomp, plan.max_segs, plan.smem_bytes);
   cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
 }

@@ -24,7 +24,10 @@ constexpr int kMaxTmemStages = 8;
 // it % kConvGroups == g, so kConvGroups stages are in conversion at once.
 constexpr int kConvGroups = 4;
 constexpr int kConvWarps = 4 * kConvGroups;
-constexpr int kTcThreads = 64 + 32 * kConvWarps;  // producer, MMA, converter warps
+// warp 0: weight producer + tensor-memory allocation; warp 1: MMA issue;
+// warps 2..kConvWarps+1: converters / epilogue; last warp: activation producer
+constexpr int kTcThreads = 64 + 32 * kConvWarps + 32;
+constexpr int kActWarp = kTcThreads / 32 - 1;
 constexpr size_t kWsHeader = 256;                // status word + spare
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
@@ -48,6 +51,7 @@ struct TcPlan {
   int tstages;         // tensor-memory A stages (nsub * 32 columns each)
   int acol;            // first tensor-memory column of the A stages
   int gps;             // scale / zero-point rows per stage (groups it spans)
+  int a3d;             // activations as one 3-D box {64, BM, nsub} per stage
   int m_tiles, n_tiles, tiles;
   int kb_total;        // pipeline stages per tile: ceil(K / (64 * nsub))
   int k64;             // K / 64

@@ -169,12 +169,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Four MMAs covering one 64-wide K stage: A columns a0, a0+8, a0+16, a0+24
-// (16 K-values each, packed pairs), B descriptors desc, desc+2, desc+4,
-// desc+6 (32 bytes further along the 128-byte swizzled rows each).  The first
-// MMA overwrites D when `accumulate` is 0.
+// Four MMAs covering one 64-wide K block: A columns a0 + 8*kk, B
+// descriptors desc + 2*kk (32 bytes further along the 128-byte swizzled rows
+// each).  Operands are formed before the asm block; the first MMA
+// overwrites D when `accumulate` is 0.
 __device__ __forceinline__ void mma_ts_stage(uint32_t d_tmem, uint32_t a0, uint64_t desc,
                                              uint32_t idesc, uint32_t accumulate) {
+  const uint32_t a1 = a0 + 8, a2 = a0 + 16, a3 = a0 + 24;
+  const uint64_t d1 = desc + 2, d2 = desc + 4, d3 = desc + 6;
   asm volatile(
       "{\n\t.reg .pred p, t;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -183,8 +185,61 @@ __device__ __forceinline__ void mma_ts_stage(uint32_t d_tmem, uint32_t a0, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, t;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, t;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, t;\n\t}" ::"r"(d_tmem),
-      "r"(a0), "l"(desc), "r"(idesc), "r"(accumulate), "r"(a0 + 8), "l"(desc + 2),
-      "r"(a0 + 16), "l"(desc + 4), "r"(a0 + 24), "l"(desc + 6)
+      "r"(a0), "l"(desc), "r"(idesc), "r"(accumulate), "r"(a1), "l"(d1), "r"(a2), "l"(d2),
+      "r"(a3), "l"(d3)
+      : "memory");
+}
+
+// Sixteen MMAs covering a 256-wide K stage made of four 64-wide blocks:
+// A columns a0 + 8*i (i = 0..15); B descriptors desc + j*sub + 2*kk for
+// block j and 16-wide step kk.  All 32 operands are formed first (independent
+// adds from three registers), then the 16 MMAs issue back to back: an add
+// between two MMAs that depends on the previous operand stalls the issue.
+__device__ __forceinline__ void mma_ts_stage16(uint32_t d_tmem, uint32_t a0, uint64_t desc,
+                                               uint64_t sub, uint32_t idesc,
+                                               uint32_t accumulate) {
+  uint32_t a[16];
+  uint64_t b[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = a0 + 8 * i;
+    b[i] = desc + static_cast<uint64_t>(i >> 2) * sub + 2 * (i & 3);
+  }
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %19, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %20, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %21, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %22, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %23, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %24, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %25, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %26, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %27, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%12], %28, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %29, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%14], %30, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %31, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%16], %32, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%17], %33, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%18], %34, %1, t;\n\t}" ::"r"(d_tmem),
+      "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
+      "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]),
+      "r"(a[13]), "r"(a[14]), "r"(a[15]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]),
+      "l"(b[5]), "l"(b[6]), "l"(b[7]), "l"(b[8]), "l"(b[9]), "l"(b[10]), "l"(b[11]), "l"(b[12]),
+      "l"(b[13]), "l"(b[14]), "l"(b[15])
+      : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared.
+__device__ __forceinline__ void tma_load_3d_a(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                              int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.full[i], 2);  // weight producer + activation producer
       mbar_init(&sm.empty[i], 4 + 1);  // one converter group + the MMA commit
     }
     for (int i = 0; i < TS; ++i) mbar_init(&sm.tfull[i], 4);
@@ -266,11 +266,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int sub_per_group = gsz / kStageK;  // 64-K blocks per scale group
   const int esz = MODE == kW4A8 ? 1 : 2;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Per stage: one wait, one expect-tx, nsub activation boxes, one bulk
-    // copy of the stage's nibbles and one box per scale / zero-point map.
+  if (warp == 0 || warp == kActWarp) {
+    // ----------------------------------------------------------- producers
+    // Two single-thread producers fill each stage in parallel, each with its
+    // own expect-tx on the stage's full barrier: warp 0 the bulk copy of the
+    // stage's nibbles and the scale / zero-point boxes, the last warp the
+    // activation tile(s).
     if (lane == 0) {
+      const bool wprod = warp == 0;
       uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       Unit u;
@@ -293,16 +296,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int k64_0 = kb * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
           const uint32_t fb = full0 + s * 8;
-          mbar_arrive_expect_tx_a(fb, nv * (a_sub + 4096) + sc_bytes + zp_bytes);
-          for (int j = 0; j < nv; ++j)
-            tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * kStageK, y, fb);
-          bulk_g2s_a(w0 + s * NS * 4096, wsrc, nv * 4096, fb);
-          if (sc_bytes || zp_bytes) {
-            const int g0 = k64_0 / sub_per_group;
-            if (sc_bytes) tma_load_2d_a(s0 + s * NS * 256, &smap, n0, g0, fb);
-            if (zp_bytes) tma_load_2d_a(z0 + s * NS * 256, &zmap, n0, g0, fb);
+          if (wprod) {
+            mbar_arrive_expect_tx_a(fb, nv * 4096 + sc_bytes + zp_bytes);
+            bulk_g2s_a(w0 + s * NS * 4096, wsrc, nv * 4096, fb);
+            if (sc_bytes || zp_bytes) {
+              const int g0 = k64_0 / sub_per_group;
+              if (sc_bytes) tma_load_2d_a(s0 + s * NS * 256, &smap, n0, g0, fb);
+              if (zp_bytes) tma_load_2d_a(z0 + s * NS * 256, &zmap, n0, g0, fb);
+            }
+            wsrc += NS * 4096;
+          } else if (p.a3d) {
+            mbar_arrive_expect_tx_a(fb, NS * a_sub);
+            tma_load_3d_a(a0 + s * NS * a_sub, &amap, 0, y, k64_0, fb);
+          } else {
+            mbar_arrive_expect_tx_a(fb, nv * a_sub);
+            for (int j = 0; j < nv; ++j)
+              tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * kStageK, y, fb);
           }
-          wsrc += NS * 4096;
           if (++s == static_cast<uint32_t>(S)) {
             s = 0;
             ph ^= 1;
@@ -332,8 +342,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (chunk_start && ev > 0) {
             if (!mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) { ok = false; break; }
           }
-          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status) ||
-              !mbar_wait(&sm.full[s], ph, abort, args.status)) {
+          // The converter group arrives on tfull only after it observed the
+          // stage's full barrier, so tfull also orders the activation tile.
+          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
             ok = false;
             break;
           }
@@ -342,8 +353,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
           const uint32_t acol = tmem + p.acol + ts * NS * 32;
           const uint64_t dsc = desc0 + s * NS * sub16;
-          mma_ts_stage(tmem, acol, dsc, idesc, chunk_start ? 0u : 1u);
-          for (int q = 1; q < nv; ++q) mma_ts_stage(tmem, acol + q * 32, dsc + q * sub16, idesc, 1u);
+          if (nv == 4) {
+            mma_ts_stage16(tmem, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+          } else {
+            mma_ts_stage(tmem, acol, dsc, idesc, chunk_start ? 0u : 1u);
+            for (int q = 1; q < nv; ++q)
+              mma_ts_stage(tmem, acol + q * 32, dsc + q * sub16, idesc, 1u);
+          }
           mma_commit(&sm.empty[s]);
           chunk_start = false;
           const bool chunk_end =
