@@ -42,6 +42,7 @@ const Schedule kSchedules[] = {
     {"tc32_sk", kEngineTc, 32, kStreamK},          {"tc64_sk", kEngineTc, 64, kStreamK},
     {"tc128_sk", kEngineTc, 128, kStreamK},        {"tc128_dp", kEngineTc, 128, kDataParallel},
     {"tc256_sk", kEngineTc, 256, kStreamK},        {"tc256_dp", kEngineTc, 256, kDataParallel},
+    {"dk8_sk", kEngineDk, 8, kStreamK},            {"dk16_sk", kEngineDk, 16, kStreamK},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 constexpr size_t kCounterBytes = 64 * 1024;
@@ -63,9 +64,11 @@ int mode_of(int a_type) {
 }
 
 // Whether schedule `si` can run this (already validated) problem shape.
-bool schedule_fits(int si, int mode, int64_t N, bool has_sg) {
+bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
   const Schedule& sc = kSchedules[si];
   if (sc.engine == kEngineSimt) return true;
+  if (sc.engine == kEngineDk)  // M rows in 8-row tiles; a 128-wide K block in one group
+    return M <= sc.bm && (gs == K || gs % 128 == 0);
   if (N % 8 != 0) return false;                      // 16-byte scale rows
   if (mode == kW4A8 && has_sg && N % 16 != 0) return false;
   if (mode == kW4A8 && sc.bm > 128) return false;    // D + int32 copy in tensor memory
@@ -139,7 +142,48 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
 
 size_t simt_ws_bytes() { return kWsHeader; }
 
-int default_schedule_impl(int mode, int64_t M, int64_t N, bool has_sg) {
+// Plan of the skinny-M (mma.sync) schedule: 128-column tiles x K splits,
+// two CTAs per SM; the split count minimizes waves x blocks per unit with a
+// small penalty per split (partials and the reduction).
+DkPlan make_dk_plan(int si, int mode, int64_t M, int64_t N, int64_t K, size_t* ws_partials,
+                    size_t* ws_total) {
+  DkPlan p{};
+  p.mode = mode;
+  p.nj = kSchedules[si].bm / 8;
+  p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
+  p.kblocks = static_cast<int>((K + 127) / 128);
+  const int slots = 2 * sm_count();
+  double best = 1e30;
+  int best_s = 1;
+  for (int ks = 1; ks <= 64 && ks <= p.kblocks; ++ks) {
+    const int kbu = (p.kblocks + ks - 1) / ks;
+    if (dk_smem_bytes(p.nj, kbu) > 100 * 1024) continue;
+    const int64_t units = static_cast<int64_t>(p.n_tiles) * ks;
+    const int64_t waves = (units + slots - 1) / slots;
+    const double cost = static_cast<double>(waves) * kbu * (1.0 + 0.02 * ks);
+    if (cost < best) {
+      best = cost;
+      best_s = ks;
+    }
+  }
+  p.ksplit = best_s;
+  p.kbu_max = (p.kblocks + p.ksplit - 1) / p.ksplit;
+  p.grid = p.n_tiles * p.ksplit;
+  p.smem_bytes = dk_smem_bytes(p.nj, p.kbu_max);
+  (void)M;
+  const size_t part = p.ksplit > 1 ? static_cast<size_t>(p.ksplit) * p.n_tiles * 8 * p.nj *
+                                         kTileN * 4
+                                   : 0;
+  *ws_partials = kWsHeader + kCounterBytes;
+  *ws_total = align256(*ws_partials + part);
+  return p;
+}
+
+int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
+  // skinny M: warp-level MMAs on register-dequantized weights
+  for (int si = 1; si < kNumSchedules; ++si)
+    if (kSchedules[si].engine == kEngineDk && schedule_fits(si, mode, M, N, K, gs, has_sg))
+      return si;
   int bm = 16;
   while (bm < M && bm < 256) bm *= 2;
   if (mode == kW4A8 && bm > 128) bm = 128;
@@ -147,11 +191,14 @@ int default_schedule_impl(int mode, int64_t M, int64_t N, bool has_sg) {
   const bool dp = tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128;
   for (int si = 1; si < kNumSchedules; ++si) {
     const Schedule& sc = kSchedules[si];
-    if (sc.bm == bm && (sc.decomp == kDataParallel) == dp && schedule_fits(si, mode, N, has_sg))
+    if (sc.engine == kEngineTc && sc.bm == bm && (sc.decomp == kDataParallel) == dp &&
+        schedule_fits(si, mode, M, N, K, gs, has_sg))
       return si;
   }
   for (int si = 1; si < kNumSchedules; ++si)
-    if (kSchedules[si].bm == bm && schedule_fits(si, mode, N, has_sg)) return si;
+    if (kSchedules[si].engine == kEngineTc && kSchedules[si].bm == bm &&
+        schedule_fits(si, mode, M, N, K, gs, has_sg))
+      return si;
   return 0;
 }
 
@@ -234,6 +281,11 @@ w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* 
 
 size_t ws_needed(int si, const Problem& pr) {
   if (kSchedules[si].engine == kEngineSimt) return simt_ws_bytes();
+  if (kSchedules[si].engine == kEngineDk) {
+    size_t wp, wt;
+    make_dk_plan(si, pr.mode, pr.M, pr.N, pr.K, &wp, &wt);
+    return wt;
+  }
   return make_plan(si, pr.mode, pr.M, pr.N, pr.K, pr.gs).ws_total;
 }
 
@@ -290,7 +342,7 @@ int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t gro
   if (M <= 0 || N <= 0 || K <= 0 || K % kStageK != 0) return -1;
   if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8) return -1;
   const int64_t gs = group_size == -1 ? K : group_size;
-  return default_schedule_impl(mode_of(a_type), M, N, gs != K);
+  return default_schedule_impl(mode_of(a_type), M, N, K, gs, gs != K);
 }
 
 size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size) {
@@ -304,7 +356,7 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
   size_t need = kWsHeader;
   if (pr.M == 0 || pr.N == 0 || pr.K == 0 || pr.K % kStageK != 0) return need;
   for (int si = 0; si < kNumSchedules; ++si) {
-    if (!schedule_fits(si, pr.mode, pr.N, pr.has_sg)) continue;
+    if (!schedule_fits(si, pr.mode, pr.M, pr.N, pr.K, pr.gs, pr.has_sg)) continue;
     size_t b = ws_needed(si, pr);
     if (b > need) need = b;
   }
@@ -330,13 +382,14 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   }
   int si = schedule;
   const bool forced = schedule >= 0;
-  if (!forced) si = default_schedule_impl(pr.mode, M, N, pr.has_sg);
-  if (!schedule_fits(si, pr.mode, N, pr.has_sg))
+  if (!forced) si = default_schedule_impl(pr.mode, M, N, K, pr.gs, pr.has_sg);
+  if (!schedule_fits(si, pr.mode, M, N, K, pr.gs, pr.has_sg))
     return fail(W4_ERR_UNSUPPORTED, "schedule %s cannot run this shape", kSchedules[si].name);
   const bool ptrs_ok = aligned16(a) && aligned16(b_packed) && aligned16(b_scales) &&
                        aligned16(b_zeros);
-  if (kSchedules[si].engine == kEngineTc && !ptrs_ok) {
-    if (forced) return fail(W4_ERR_UNSUPPORTED, "tc schedules need 16-byte aligned inputs");
+  if (kSchedules[si].engine != kEngineSimt && !ptrs_ok) {
+    if (forced)
+      return fail(W4_ERR_UNSUPPORTED, "tensor-core schedules need 16-byte aligned inputs");
     si = 0;
   }
   if (!workspace) return fail(W4_ERR_WORKSPACE, "workspace is null");
@@ -363,6 +416,19 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   if (kSchedules[si].engine == kEngineSimt) {
     cudaError_t e = launch_simt(pr.mode, a, args, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "simt launch");
+  }
+  if (kSchedules[si].engine == kEngineDk) {
+    size_t wp, wt;
+    DkPlan dp = make_dk_plan(si, pr.mode, M, N, K, &wp, &wt);
+    args.counters = reinterpret_cast<int*>(ws + kWsHeader);
+    args.partials = ws + wp;
+    static const bool debug = getenv("W4_DEBUG") != nullptr;
+    if (debug)
+      fprintf(stderr, "w4: %s M=%lld N=%lld K=%lld nj=%d tiles=%d kblocks=%d ksplit=%d grid=%d smem=%zu\n",
+              kSchedules[si].name, (long long)M, (long long)N, (long long)K, dp.nj, dp.n_tiles,
+              dp.kblocks, dp.ksplit, dp.grid, dp.smem_bytes);
+    cudaError_t e = launch_dk(dp, a, args, s);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "dk launch");
   }
 
   TcPlan plan = make_plan(si, pr.mode, M, N, K, pr.gs);

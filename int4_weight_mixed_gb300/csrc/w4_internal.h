@@ -32,7 +32,7 @@ constexpr size_t kWsHeader = 256;                // status word + spare
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
 
-enum Engine { kEngineSimt = 0, kEngineTc = 1 };
+enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2 };
 enum Decomp { kDataParallel = 0, kStreamK = 1 };
 
 struct Schedule {
@@ -82,6 +82,18 @@ struct TcArgs {
   void* partials;
 };
 
+// Skinny-M schedule (mma.sync, weights dequantized into register fragments).
+struct DkPlan {
+  int mode;
+  int nj;        // 8-row activation tiles: M <= 8 * nj
+  int n_tiles;   // 128-column weight tiles
+  int kblocks;   // 128-wide K blocks: ceil(K / 128)
+  int ksplit;    // K splits per tile (units = n_tiles * ksplit = grid)
+  int kbu_max;   // largest number of K blocks in one unit
+  int grid;
+  size_t smem_bytes;
+};
+
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_prepack(const int32_t* w_q, int wtype, int layout, int64_t K, int64_t N,
                            uint8_t* out, cudaStream_t s);
@@ -91,6 +103,8 @@ cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s);
 cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                       const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
+cudaError_t launch_dk(const DkPlan& plan, const void* a, const TcArgs& args, cudaStream_t s);
+size_t dk_smem_bytes(int nj, int kbu_max);
 size_t tc_stage_bytes(int bm, int nsub);
 size_t tc_smem_bytes(int bm, int nsub, int stages);
 int tc_max_stages(int bm, int nsub);

@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp"]
+DK = ["dk8_sk", "dk16_sk"]
 
 
 def sched(w4, name):
@@ -88,7 +89,7 @@ def test_prepack_layouts_agree(gpu_lib):
 
 # ------------------------------------------------------------------- W4A16 ---
 
-@pytest.mark.parametrize("name", ALL)
+@pytest.mark.parametrize("name", ALL + ["dk16_sk"])
 def test_tiny_w4a16_every_schedule(gpu_lib, name):
     w4 = gpu_lib
     d = w4synth.tiny_w4a16(seed=0)
@@ -114,6 +115,8 @@ def test_w4a16_bf16_several_tiles(gpu_lib, name, zeros):
     (3, 200, 640, 128, torch.bfloat16),   # ragged N inside a 128 tile
     (17, 136, 512, 64, torch.bfloat16),   # group 64, ragged M and N
     (100, 13, 256, 128, torch.float16),   # N % 8 != 0 -> CUDA-core schedule
+    (5, 13, 256, 128, torch.bfloat16),    # N % 8 != 0, skinny M -> mma.sync schedule
+    (12, 200, 576, -1, torch.float16),    # skinny M, ragged N, K not a multiple of 128
     (300, 256, 192, -1, torch.bfloat16),  # M spanning two 256-row tiles
 ])
 def test_w4a16_ragged(gpu_lib, M, N, K, gs, dt):
@@ -123,6 +126,21 @@ def test_w4a16_ragged(gpu_lib, M, N, K, gs, dt):
     got = run_w4a16(w4, d)
     ref, absref = oracle_w4a16(d)
     assert_within(got.double().numpy(), ref, absref, fmt(dt), f"ragged {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("name", DK)
+@pytest.mark.parametrize("M", [1, 3, 8, 13, 16])
+@pytest.mark.parametrize("dt,zeros,gs", [(torch.bfloat16, True, 128), (torch.float16, False, 128),
+                                          (torch.bfloat16, False, -1), (torch.float16, True, 256)])
+def test_dk_w4a16(gpu_lib, name, M, dt, zeros, gs):
+    w4 = gpu_lib
+    if M > (8 if name == "dk8_sk" else 16):
+        pytest.skip("more rows than the schedule's tile")
+    d = w4synth.gen_w4a16(M, 392, 1280, act_dtype=dt, wtype=w4.UINT4 if zeros else w4.UINT4B8,
+                          layout=w4.NK_EXLLAMA, group_size=gs, zeros=zeros, seed=M)
+    got = run_w4a16(w4, d, sched(w4, name))
+    ref, absref = oracle_w4a16(d)
+    assert_within(got.double().numpy(), ref, absref, fmt(dt), f"{name} M={M}")
 
 
 def test_w4a16_power_of_two_scales_exact(gpu_lib):
@@ -190,11 +208,13 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
     return out.cpu()
 
 
-@pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp"])
+@pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
+                                  "dk8_sk", "dk16_sk"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
-    e = w4synth.gen_w4a8(40, 384, 2048, group_size=gs, seed=7)
+    M = {"dk8_sk": 8, "dk16_sk": 13}.get(name, 40)
+    e = w4synth.gen_w4a8(M, 384, 2048, group_size=gs, seed=7)
     acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
     ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, e["K"], e["N"])
     assert np.array_equal(acc.numpy().astype(np.int64), ref)
@@ -215,7 +235,7 @@ def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
     a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(0)).to(torch.int8)
     sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
     e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
-    for name in ("tc16_sk", "tc128_dp", "simt"):
+    for name in ("tc16_sk", "tc128_dp", "simt", "dk8_sk"):
         acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
         ref = oracle.w4a8(a, w, oracle.NK_EXLLAMA, w4.INT4, sg, gs, K, N)
         assert np.array_equal(acc.numpy().astype(np.int64), ref), name
