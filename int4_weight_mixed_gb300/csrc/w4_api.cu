@@ -160,7 +160,8 @@ DkPlan make_dk_plan(int si, int mode, int64_t M, int64_t N, int64_t K, size_t* w
     if (dk_smem_bytes(p.nj, kbu) > 100 * 1024) continue;
     const int64_t units = static_cast<int64_t>(p.n_tiles) * ks;
     const int64_t waves = (units + slots - 1) / slots;
-    const double cost = static_cast<double>(waves) * kbu * (1.0 + 0.02 * ks);
+    // a wave costs its K blocks plus a fixed prologue / epilogue (~6 blocks)
+    const double cost = static_cast<double>(waves) * (kbu + 6) * (1.0 + 0.01 * ks);
     if (cost < best) {
       best = cost;
       best_s = ks;

@@ -122,6 +122,76 @@ __global__ void __launch_bounds__(kDkThreads, 2)
   float* ssum = reinterpret_cast<float*>(smem + static_cast<size_t>(p.kbu_max) * 8 * NJ * 32 * 8);
   int* isum = reinterpret_cast<int*>(ssum);                              // [nkb][8*NJ]
 
+  // ---- weight stream: kPrefetch 128-wide K blocks of weights (and their
+  // scale / zero rows) in flight per thread; the first loads are issued
+  // before the activations are staged, so their latency overlaps staging.
+  // Every per-load index advances incrementally (no multiplies, no
+  // divisions in the loop).
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int ra = warp * 16 + g, rb = ra + 8;                  // rows within the tile
+  const int64_t na = static_cast<int64_t>(nt) * kTileN + ra, nb = na + 8;
+  const int64_t chunks = K / kChunkK;
+  const int full_blocks = static_cast<int>(chunks >> 2);      // blocks with all 4 chunks
+  const bool t_in_last = t < static_cast<int>(chunks & 3);    // chunk t of a partial last block
+  const int kb_per_g = args.group_size >= K ? (1 << 30) : static_cast<int>(args.group_size / kBlockK);
+  const bool pc = args.group_size >= K;                       // one group per column
+  constexpr float kMagic = F16 ? 1024.f : 128.f;
+  constexpr bool kSubMagic = F16;  // f16: subtract magic+bias exactly before the MMA
+  const bool rowa_ok = na < N, rowb_ok = nb < N;
+  const uint8_t* wptr = args.b_packed +
+                        ((static_cast<int64_t>(nt) * chunks + static_cast<int64_t>(kb0) * 4 + t) *
+                             kTileN + ra) * 16;
+  constexpr int64_t kWStep = 4 * kTileN * 16;  // bytes from one K block to the next
+  // scale / zero-point row pointers of the current group (column na; nb is +8)
+  const int64_t g0 = pc ? 0 : kb0 / kb_per_g;
+  const T16* scp = static_cast<const T16*>(args.scales) + g0 * N + na;
+  const T16* zpp = static_cast<const T16*>(args.zeros) + g0 * N + na;
+  const int8_t* sgp = static_cast<const int8_t*>(args.scales) + g0 * N + na;
+  int gleft = pc ? (1 << 30) : kb_per_g - kb0 % kb_per_g;     // blocks left in this group
+  int kb_next = kb0;
+
+  auto rd_s = [&](float& va, float& vb, float& wz_a, float& wz_b) {
+    if (MODE == kW4A8) {
+      va = (args.scales && rowa_ok) ? static_cast<float>(sgp[0]) : 1.f;
+      vb = (args.scales && rowb_ok) ? static_cast<float>(sgp[8]) : 1.f;
+    } else {
+      va = rowa_ok ? to_f32(scp[0]) : 0.f;
+      vb = rowb_ok ? to_f32(scp[8]) : 0.f;
+      wz_a = (args.zeros && rowa_ok) ? to_f32(zpp[0]) : 0.f;
+      wz_b = (args.zeros && rowb_ok) ? to_f32(zpp[8]) : 0.f;
+    }
+  };
+  // one group per column: the scale / zero rows never change
+  float pc_sa = 1.f, pc_sb = 1.f, pc_za = 0.f, pc_zb = 0.f;
+  if (pc) rd_s(pc_sa, pc_sb, pc_za, pc_zb);
+
+  uint4 wa[kPrefetch], wb[kPrefetch];
+  float sa[kPrefetch], sb[kPrefetch], za[kPrefetch], zb[kPrefetch];
+  auto load = [&](int slot) {
+    if (kb_next < full_blocks || (kb_next == full_blocks && t_in_last)) {
+      wa[slot] = ldg_nc_v4(wptr);
+      wb[slot] = ldg_nc_v4(wptr + 8 * 16);
+    } else {
+      wa[slot] = make_uint4(0, 0, 0, 0);
+      wb[slot] = make_uint4(0, 0, 0, 0);
+    }
+    wptr += kWStep;
+    ++kb_next;
+    if (!pc) {
+      rd_s(sa[slot], sb[slot], za[slot], zb[slot]);
+      if (--gleft == 0) {
+        gleft = kb_per_g;
+        scp += N;
+        zpp += N;
+        sgp += N;
+      }
+    }
+  };
+#pragma unroll
+  for (int q = 0; q < kPrefetch; ++q)
+    if (q < nkb) load(q);
+
   // ---- stage this unit's activations, K-permuted to match the weight
   // fragments.  One task = 8 consecutive K values of one row (one prepacked
   // word's K range): a single 16-byte (8-byte for int8) load, scattered as
@@ -198,44 +268,6 @@ __global__ void __launch_bounds__(kDkThreads, 2)
   }
   __syncthreads();
 
-  // ---- main loop: one 128-wide K block per step, kPrefetch blocks of
-  // weights (and their scale / zero rows) in flight per thread
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int ra = warp * 16 + g, rb = ra + 8;                  // rows within the tile
-  const int64_t na = static_cast<int64_t>(nt) * kTileN + ra, nb = na + 8;
-  const int64_t chunks = K / kChunkK;
-  const uint8_t* wtile = args.b_packed + static_cast<int64_t>(nt) * chunks * kTileN * 16;
-  const int gs = static_cast<int>(args.group_size);
-  constexpr float kMagic = F16 ? 1024.f : 128.f;
-  constexpr bool kSubMagic = F16;  // f16: subtract magic+bias exactly before the MMA
-
-  uint4 wa[kPrefetch], wb[kPrefetch];
-  float sa[kPrefetch], sb[kPrefetch], za[kPrefetch], zb[kPrefetch];
-  auto load = [&](int kb, int slot) {
-    const int64_t c = static_cast<int64_t>(kb) * 4 + t;
-    if (c < chunks) {
-      wa[slot] = ldg_nc_v4(wtile + (c * kTileN + ra) * 16);
-      wb[slot] = ldg_nc_v4(wtile + (c * kTileN + rb) * 16);
-    } else {
-      wa[slot] = make_uint4(0, 0, 0, 0);
-      wb[slot] = make_uint4(0, 0, 0, 0);
-    }
-    const int64_t gi = static_cast<int64_t>(kb) * kBlockK / gs;
-    if (MODE == kW4A8) {
-      const int8_t* sg = static_cast<const int8_t*>(args.scales);
-      sa[slot] = (sg && na < N) ? static_cast<float>(sg[gi * N + na]) : 1.f;
-      sb[slot] = (sg && nb < N) ? static_cast<float>(sg[gi * N + nb]) : 1.f;
-    } else {
-      const T16* sc = static_cast<const T16*>(args.scales);
-      const T16* zp = static_cast<const T16*>(args.zeros);
-      sa[slot] = na < N ? to_f32(sc[gi * N + na]) : 0.f;
-      sb[slot] = nb < N ? to_f32(sc[gi * N + nb]) : 0.f;
-      za[slot] = (zp && na < N) ? to_f32(zp[gi * N + na]) : 0.f;
-      zb[slot] = (zp && nb < N) ? to_f32(zp[gi * N + nb]) : 0.f;
-    }
-  };
-
   float res[NJ][4];
   int32_t ires[NJ][4];
 #pragma unroll
@@ -245,10 +277,6 @@ __global__ void __launch_bounds__(kDkThreads, 2)
       res[j][e] = 0.f;
       ires[j][e] = 0;
     }
-
-#pragma unroll
-  for (int q = 0; q < kPrefetch; ++q)
-    if (q < nkb) load(kb0 + q, q);
 
   const uint32_t off2 = kSubMagic ? [&] {
     __half2 h = __float2half2_rn(kMagic + static_cast<float>(args.wbias));
@@ -285,13 +313,17 @@ __global__ void __launch_bounds__(kDkThreads, 2)
           }
         }
       }
-      const float s_a = sa[q], s_b = sb[q], z_a = za[q], z_b = zb[q];
-      if (kbl + kPrefetch < nkb) load(kb0 + kbl + kPrefetch, q);
-      float acc[NJ][4];
+      const float s_a = pc ? pc_sa : sa[q], s_b = pc ? pc_sb : sb[q];
+      const float z_a = pc ? pc_za : za[q], z_b = pc ? pc_zb : zb[q];
+      if (kbl + kPrefetch < nkb) load(q);
+      float acc[NJ][4], acc2[NJ][4];  // two independent MMA chains (even / odd i)
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          acc[j][e] = 0.f;
+          acc2[j][e] = 0.f;
+        }
       const uint2* bp = sact + static_cast<size_t>(kbl) * 8 * NJ * 32 + lane;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -299,31 +331,44 @@ __global__ void __launch_bounds__(kDkThreads, 2)
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           const uint2 bv = bp[(i * NJ + j) * 32];
-          mma16816<F16>(acc[j], afr, bv.x, bv.y);
+          mma16816<F16>((i & 1) ? acc2[j] : acc[j], afr, bv.x, bv.y);
         }
       }
-      // fold the block into the running result
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = j * 8 + 2 * t + (e & 1);
-          const bool rowa = e < 2;
-          if (MODE == kW4A8) {
-            const int sum = isum[kbl * 8 * NJ + m];
-            const int32_t blk = __float2int_rn(acc[j][e]) - (128 + 8) * sum;
-            ires[j][e] += static_cast<int32_t>(rowa ? s_a : s_b) * blk;
-          } else {
-            const float S = ssum[kbl * 8 * NJ + m];
-            const float sr = rowa ? s_a : s_b, zr = rowa ? z_a : z_b;
-            if (kSubMagic) {
-              res[j][e] = fmaf(sr, acc[j][e], fmaf(-zr, S, res[j][e]));
-            } else {
-              const float cr = fmaf(kMagic + static_cast<float>(args.wbias), sr, zr);
-              res[j][e] = fmaf(sr, acc[j][e], fmaf(-cr, S, res[j][e]));
-            }
+        for (int e = 0; e < 4; ++e) acc[j][e] += acc2[j][e];
+      // fold the block into the running result
+      if (MODE == kW4A8) {
+        // block sums are integers below 2^22: adding 1.5*2^23 puts them in the
+        // low mantissa bits, read back exactly as an int
+        const int isa = static_cast<int>(s_a), isb = static_cast<int>(s_b);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int2 S2 = *reinterpret_cast<const int2*>(&isum[kbl * 8 * NJ + j * 8 + 2 * t]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int bi = __float_as_int(acc[j][e] + 12582912.0f) - 0x4B400000;
+            const int blk = bi - (128 + 8) * ((e & 1) ? S2.y : S2.x);
+            if (pc) ires[j][e] += blk;
+            else ires[j][e] += (e < 2 ? isa : isb) * blk;
           }
         }
+      } else {
+        const float mb = kMagic + static_cast<float>(args.wbias);
+        const float c_a = kSubMagic ? z_a : fmaf(mb, s_a, z_a);
+        const float c_b = kSubMagic ? z_b : fmaf(mb, s_b, z_b);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const float2 S2 = *reinterpret_cast<const float2*>(&ssum[kbl * 8 * NJ + j * 8 + 2 * t]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float S = (e & 1) ? S2.y : S2.x;
+            const float sr = e < 2 ? s_a : s_b, cr = e < 2 ? c_a : c_b;
+            res[j][e] = fmaf(sr, acc[j][e], fmaf(-cr, S, res[j][e]));
+          }
+        }
+      }
     }
   }
 
