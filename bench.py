@@ -65,6 +65,24 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def measured_traffic(kernel, M):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+        if not rec or rec.get("M") != M:
+            return None
+        with open(os.path.join(ROOT, rec["src"]), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+        return rec["dram_bytes_per_launch"] if sha.startswith(rec["src_sha1_prefix"]) else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -147,6 +165,17 @@ def make_inputs(dev):
     return sets
 
 
+def launches_per_step(w4):
+    """Kernels of this library one step launches: the skinny-M schedule is
+    one launch; the tensor-core W4A8 schedule adds its int8->bf16 staging."""
+    names = w4.schedule_names()
+    n = 0
+    for M in M_SWEEP:
+        name = names[w4.default_schedule(M, N, K, torch.int8, -1)]
+        n += 2 if name.startswith("tc") else 1
+    return n
+
+
 def run_gpu(args):
     import int4_weight_mixed_gb300 as w4
 
@@ -199,7 +228,17 @@ def run_gpu(args):
         for M in M_SWEEP:
             gemm(i % ROTATE, M)
     barrier()
-    step_graphs = [capture(lambda r=r: [gemm(r, M) for M in M_SWEEP]) for r in range(ROTATE)]
+    if args.eager:  # plain launches (for profilers that do not follow graphs)
+        class _Eager:
+            def __init__(self, r):
+                self.r = r
+
+            def replay(self):
+                for M in M_SWEEP:
+                    gemm(self.r, M)
+        step_graphs = [_Eager(r) for r in range(ROTATE)]
+    else:
+        step_graphs = [capture(lambda r=r: [gemm(r, M) for M in M_SWEEP]) for r in range(ROTATE)]
     for i in range(args.warmup):
         step_graphs[i % ROTATE].replay()
     barrier()
@@ -226,6 +265,8 @@ def run_gpu(args):
     per_m = {}
     reps = max(8, min(args.steps, 100))
     for M in M_SWEEP:
+        if args.eager:
+            break
         gs_m = [capture(lambda r=r, M=M: gemm(r, M)) for r in range(ROTATE)]
         for r in range(ROTATE):
             gs_m[r].replay()
@@ -291,6 +332,8 @@ def run_gpu(args):
     value = step_flops * world / (ms_per_step * 1e-3) / 1e12
     sweep = []
     for M in M_SWEEP:
+        if M not in per_m:
+            per_m[M] = [ms_per_step * 1e3 / len(M_SWEEP)]
         us = statistics.median(per_m[M])
         tf = flops(M) / (us * 1e-6) / 1e12
         gbs = weight_bytes() / (us * 1e-6) / 1e9
@@ -307,7 +350,7 @@ def run_gpu(args):
                 "M": dom, "bound": "tensor", "achieved": round(flops(dom) / (dom_us * 1e-6) / 1e12, 1),
                 "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                 "peak_source": f"{pk['src']} bf16 dense, sustained",
-                "traffic": None}
+                "traffic": measured_traffic("tc_gemm_kernel<W4A8>", dom)}
     roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 3)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -319,7 +362,7 @@ def run_gpu(args):
         "sweep": sweep, "roofline": roofline, "e2e": e2e,
         "prepack": {"us": round(prepack_us, 1),
                     "gbs": round(2 * K * N // 2 / (prepack_us * 1e-6) / 1e9, 1)},
-        "gpu_launches": 2 * len(M_SWEEP) * args.steps,
+        "gpu_launches": launches_per_step(w4) * args.steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -426,9 +469,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--single", type=int, default=0, help="run only the GEMM with this M")
     ap.add_argument("--schedule", type=int, default=-1)
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the step without CUDA graphs (profiler launch lists)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
