@@ -38,11 +38,13 @@ w4_status cuda_fail(cudaError_t e, const char* what) {
 // Schedules ("Machete Readme", "Code Generation": a set of schedule configs
 // with a default heuristic and an optional explicit choice).
 const Schedule kSchedules[] = {
-    {"simt", kEngineSimt, 0, kDataParallel},       {"tc16_sk", kEngineTc, 16, kStreamK},
-    {"tc32_sk", kEngineTc, 32, kStreamK},          {"tc64_sk", kEngineTc, 64, kStreamK},
-    {"tc128_sk", kEngineTc, 128, kStreamK},        {"tc128_dp", kEngineTc, 128, kDataParallel},
-    {"tc256_sk", kEngineTc, 256, kStreamK},        {"tc256_dp", kEngineTc, 256, kDataParallel},
-    {"dk8_sk", kEngineDk, 8, kStreamK},            {"dk16_sk", kEngineDk, 16, kStreamK},
+    {"simt", kEngineSimt, 0, kDataParallel, 1},       {"tc16_sk", kEngineTc, 16, kStreamK, 1},
+    {"tc32_sk", kEngineTc, 32, kStreamK, 1},          {"tc64_sk", kEngineTc, 64, kStreamK, 1},
+    {"tc128_sk", kEngineTc, 128, kStreamK, 1},        {"tc128_dp", kEngineTc, 128, kDataParallel, 1},
+    {"tc256_sk", kEngineTc, 256, kStreamK, 1},        {"tc256_dp", kEngineTc, 256, kDataParallel, 1},
+    {"dk8_sk", kEngineDk, 8, kStreamK, 1},            {"dk16_sk", kEngineDk, 16, kStreamK, 1},
+    {"tc128x2_sk", kEngineTc, 128, kStreamK, 2},      {"tc128x2_dp", kEngineTc, 128, kDataParallel, 2},
+    {"tc128x2_kp", kEngineTc, 128, kSplitK, 2},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 constexpr size_t kCounterBytes = 64 * 1024;
@@ -63,6 +65,8 @@ int mode_of(int a_type) {
   return a_type == W4_F16 ? kW4A16_F16 : a_type == W4_BF16 ? kW4A16_BF16 : kW4A8;
 }
 
+TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs);
+
 // Whether schedule `si` can run this (already validated) problem shape.
 bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
   const Schedule& sc = kSchedules[si];
@@ -71,8 +75,9 @@ bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs
     return M <= sc.bm && (gs == K || gs % 128 == 0);
   if (N % 8 != 0) return false;                      // 16-byte scale rows
   if (mode == kW4A8 && has_sg && N % 16 != 0) return false;
-  if (mode == kW4A8 && sc.bm > 128) return false;    // D + int32 copy in tensor memory
-  return true;
+  // tensor memory must hold the accumulators (and the W4A8 int32 copies)
+  // beside at least one stage of converted weights
+  return make_plan(si, mode, M, N, K, gs).tstages >= 1;
 }
 
 // Build the launch plan of a tc schedule.
@@ -81,26 +86,23 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   TcPlan p{};
   p.mode = mode;
   p.bm = sc.bm;
+  p.nt = sc.nt;
   // K depth of a pipeline stage: skinny tiles need >= 8 KB of nibbles per
   // stage to hide the per-stage cost of the producer; wide tiles are
   // compute-bound and take shallower stages so that several fit in shared
   // memory.
   int nsub = p.bm <= 64 ? 4 : (p.bm <= 128 ? 2 : 1);
+  nsub = nsub / p.nt > 0 ? nsub / p.nt : 1;
   const int64_t G = K / gs;
   if (G > 1)  // a stage must cover whole groups or lie inside one group
     while (nsub > 1 && (nsub * kStageK) % gs != 0 && gs % (nsub * kStageK) != 0) nsub /= 2;
   p.nsub = nsub;
   p.gps = (G > 1 && gs < nsub * kStageK) ? static_cast<int>(nsub * kStageK / gs) : 1;
-  p.stages = tc_max_stages(p.bm, nsub);
-  p.smem_bytes = tc_smem_bytes(p.bm, nsub, p.stages);
-  const int dcols = p.bm * (mode == kW4A8 ? 2 : 1);  // W4A8 keeps an int32 copy beside D
-  p.acol = (dcols + 31) / 32 * 32;
-  int ts = (512 - p.acol) / (nsub * 32);
-  if (ts > kMaxTmemStages) ts = kMaxTmemStages;
-  if (ts > p.stages - 1) ts = p.stages - 1;
-  p.tstages = ts;
+  p.stages = tc_max_stages(p.bm, nsub, p.nt);
+  p.smem_bytes = tc_smem_bytes(p.bm, nsub, p.nt, p.stages);
   p.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
-  p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
+  p.n128 = static_cast<int>((N + kTileN - 1) / kTileN);
+  p.n_tiles = (p.n128 + p.nt - 1) / p.nt;
   p.tiles = p.m_tiles * p.n_tiles;
   p.k64 = static_cast<int>(K / kStageK);
   p.kb_total = (p.k64 + nsub - 1) / nsub;
@@ -111,10 +113,36 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   p.decomp = sc.decomp;
   if (p.tiles * static_cast<size_t>(kConvWarps) * 4 > kCounterBytes) p.decomp = kDataParallel;
   p.ws_counters = kWsHeader;
+  p.ws_partials = p.ws_counters + kCounterBytes;
+  p.ksplit = 1;
+  p.max_segs = 1;
+  size_t part = 0;
+  const size_t slot_bytes = static_cast<size_t>(p.nt) * kTileN * p.bm * 4;
   if (p.decomp == kDataParallel) {
     p.grid = p.tiles < sms ? p.tiles : sms;
-    p.max_segs = 1;
-    p.ws_partials = p.ws_counters + kCounterBytes;
+  } else if (p.decomp == kSplitK) {
+    // K splits: W4A8 splits at least until no unit is longer than one exact
+    // chunk; then the split count minimizes waves x stages per unit, with a
+    // charge for writing the partial sums when there is more than one split.
+    int ks_min = 1;
+    if (mode == kW4A8) ks_min = (p.kb_total + p.chunk_stages - 1) / p.chunk_stages;
+    double best = 1e30;
+    int best_ks = ks_min;
+    for (int ks = ks_min; ks <= 16 && ks <= p.kb_total; ++ks) {
+      const int64_t units = static_cast<int64_t>(p.tiles) * ks;
+      const int64_t waves = (units + sms - 1) / sms;
+      const int kbu = (p.kb_total + ks - 1) / ks;
+      // a partial-sum slot costs about as much as a dozen stages to write
+      const double cost = static_cast<double>(waves) * (kbu + 8 + (ks > 1 ? 12 : 0));
+      if (cost < best) {
+        best = cost;
+        best_ks = ks;
+      }
+    }
+    p.ksplit = best_ks;
+    const int64_t units = static_cast<int64_t>(p.tiles) * p.ksplit;
+    p.grid = static_cast<int>(units < sms ? units : sms);
+    if (p.ksplit > 1) part = static_cast<size_t>(p.tiles) * p.ksplit * slot_bytes;
   } else {
     const int64_t T = static_cast<int64_t>(p.tiles) * p.kb_total;
     int64_t g = T / 2;  // at least 2 stages per CTA
@@ -129,11 +157,22 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
       if (segs > ms) ms = segs;
     }
     p.max_segs = ms;
-    p.ws_partials = p.ws_counters + kCounterBytes;
+    part = static_cast<size_t>(p.grid) * p.max_segs * slot_bytes;
   }
-  size_t part = p.decomp == kStreamK
-                    ? static_cast<size_t>(p.grid) * p.max_segs * kTileN * p.bm * 4
-                    : 0;
+  // Tensor memory: accumulators (NT x BM columns), the W4A8 int32 copies
+  // when a unit can span several exact chunks, then the converted-weight
+  // stages (NT x nsub x 32 columns each).
+  bool long_units = p.kb_total > p.chunk_stages;
+  if (p.decomp == kSplitK) long_units = (p.kb_total + p.ksplit - 1) / p.ksplit > p.chunk_stages;
+  const int dcols = p.nt * p.bm;
+  p.icol = (mode == kW4A8 && long_units) ? dcols : 0;
+  const int used = (p.icol ? 2 * dcols : dcols);
+  p.acol = (used + 31) / 32 * 32;
+  int ts = p.acol >= 512 ? 0 : (512 - p.acol) / (p.nt * nsub * 32);
+  if (p.ksplit > 16) ts = 0;  // too many partial sums to be worth it: not offered
+  if (ts > kMaxTmemStages) ts = kMaxTmemStages;
+  if (ts > p.stages - 1) ts = p.stages - 1;
+  p.tstages = ts;
   p.ws_act = align256(p.ws_partials + part);
   size_t act = mode == kW4A8 ? static_cast<size_t>(M) * K * 2 : 0;
   p.ws_total = align256(p.ws_act + act);
@@ -141,7 +180,6 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
 }
 
 size_t simt_ws_bytes() { return kWsHeader; }
-
 // Plan of the skinny-M (mma.sync) schedule: 128-column tiles x K splits,
 // two CTAs per SM; the split count minimizes waves x blocks per unit with a
 // small penalty per split (partials and the reduction).
@@ -501,11 +539,12 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   static const bool debug = getenv("W4_DEBUG") != nullptr;
   if (debug)
     fprintf(stderr,
-            "w4: %s M=%lld N=%lld K=%lld bm=%d nsub=%d stages=%d tstages=%d acol=%d gps=%d "
-            "a3d=%d tiles=%d kb=%d grid=%d decomp=%d segs=%d smem=%zu\n",
-            kSchedules[si].name, (long long)M, (long long)N, (long long)K, plan.bm, plan.nsub,
-            plan.stages, plan.tstages, plan.acol, plan.gps, plan.a3d, plan.tiles, plan.kb_total,
-            plan.grid, plan.decomp, plan.max_segs, plan.smem_bytes);
+            "w4: %s M=%lld N=%lld K=%lld bm=%d nt=%d nsub=%d stages=%d tstages=%d icol=%d "
+            "acol=%d gps=%d a3d=%d tiles=%d kb=%d grid=%d decomp=%d ksplit=%d segs=%d smem=%zu\n",
+            kSchedules[si].name, (long long)M, (long long)N, (long long)K, plan.bm, plan.nt,
+            plan.nsub, plan.stages, plan.tstages, plan.icol, plan.acol, plan.gps, plan.a3d,
+            plan.tiles, plan.kb_total, plan.grid, plan.decomp, plan.ksplit, plan.max_segs,
+            plan.smem_bytes);
   cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
 }

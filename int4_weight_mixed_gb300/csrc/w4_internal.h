@@ -33,19 +33,24 @@ constexpr size_t kWsHeader = 256;                // status word + spare
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
 
 enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2 };
-enum Decomp { kDataParallel = 0, kStreamK = 1 };
+enum Decomp { kDataParallel = 0, kStreamK = 1, kSplitK = 2 };
 
 struct Schedule {
   const char* name;
   int engine;
   int bm;      // activation rows per tile (UMMA N)
-  int decomp;  // kDataParallel / kStreamK
+  int decomp;  // kDataParallel / kStreamK / kSplitK
+  int nt;      // 128-column weight tiles per CTA (tc): 1, or 2 to share each activation tile
 };
 
 // Everything a tc launch needs, computed on the host.
 struct TcPlan {
   int mode;
   int bm;
+  int nt;              // 128-column weight tiles per CTA tile (1 or 2)
+  int n128;            // ceil(N / 128): prepacked weight tiles that exist
+  int ksplit;          // kSplitK: K splits per tile
+  int icol;            // W4A8: first tensor-memory column of the int32 copies (0 = none)
   int nsub;            // 64-wide K blocks per pipeline stage (1, 2 or 4)
   int stages;          // shared-memory pipeline stages
   int tstages;         // tensor-memory A stages (nsub * 32 columns each)
@@ -105,8 +110,8 @@ cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtenso
                       const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
 cudaError_t launch_dk(const DkPlan& plan, const void* a, const TcArgs& args, cudaStream_t s);
 size_t dk_smem_bytes(int nj, int kbu_max);
-size_t tc_stage_bytes(int bm, int nsub);
-size_t tc_smem_bytes(int bm, int nsub, int stages);
-int tc_max_stages(int bm, int nsub);
+size_t tc_stage_bytes(int bm, int nsub, int nt);
+size_t tc_smem_bytes(int bm, int nsub, int nt, int stages);
+int tc_max_stages(int bm, int nsub, int nt);
 
 }  // namespace w4

@@ -44,9 +44,10 @@ namespace {
 struct Unit {
   int tile;
   int kb0, kb1;
-  int nslots;   // CTAs contributing to this tile
+  int nslots;   // units contributing to this tile
   int cfirst;   // first contributing CTA (stream-K)
-  int seg;      // index of this tile among the CTA's segments
+  int seg;      // index of this tile among the CTA's segments (stream-K)
+  int split;    // K split of this unit (split-K)
 };
 
 struct Work {
@@ -64,6 +65,21 @@ __device__ __forceinline__ int64_t sk_owner(int64_t i, int64_t T, int64_t G) {
 
 // u-th unit of this CTA; false when there is none.
 __device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
+  if (p.decomp == kSplitK) {
+    // units (tile, split), c, c+G, ...: split j covers stages
+    // [j*kb/ks, (j+1)*kb/ks) of its tile
+    const int64_t v = blockIdx.x + static_cast<int64_t>(u) * p.grid;
+    if (v >= static_cast<int64_t>(p.tiles) * p.ksplit) return false;
+    const int t = static_cast<int>(v / p.ksplit), j = static_cast<int>(v % p.ksplit);
+    out.tile = t;
+    out.split = j;
+    out.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kb_total / p.ksplit);
+    out.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kb_total / p.ksplit);
+    out.nslots = p.ksplit;
+    out.cfirst = 0;
+    out.seg = 0;
+    return true;
+  }
   if (p.decomp == kDataParallel) {
     int64_t t = blockIdx.x + static_cast<int64_t>(u) * p.grid;
     if (t >= p.tiles) return false;
@@ -73,6 +89,7 @@ __device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
     out.nslots = 1;
     out.cfirst = blockIdx.x;
     out.seg = 0;
+    out.split = 0;
     return true;
   }
   int64_t t = w.first_tile + u;
@@ -88,7 +105,21 @@ __device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
   out.cfirst = static_cast<int>(cf);
   out.nslots = static_cast<int>(cl - cf + 1);
   out.seg = u;
+  out.split = 0;
   return true;
+}
+
+// Partial-sum slot of contributor sl (0-based, in K order) of the unit's tile.
+__device__ __forceinline__ size_t slot_index(const TcPlan& p, const Work& w, const Unit& u,
+                                             int sl) {
+  if (p.decomp == kSplitK) return static_cast<size_t>(u.tile) * p.ksplit + sl;
+  const int64_t cpr = u.cfirst + sl;
+  const int64_t seg = u.tile - sk_start(cpr, w.T, w.G) / w.kb;
+  return static_cast<size_t>(cpr) * p.max_segs + seg;
+}
+__device__ __forceinline__ size_t own_slot(const TcPlan& p, const Unit& u) {
+  if (p.decomp == kSplitK) return static_cast<size_t>(u.tile) * p.ksplit + u.split;
+  return static_cast<size_t>(blockIdx.x) * p.max_segs + u.seg;
 }
 
 // Tile -> (m_tile, n_tile), grouped raster: runs of up to 8 m-tiles share
@@ -184,19 +215,20 @@ struct Smem {
 
 }  // namespace
 
-size_t tc_stage_bytes(int bm, int nsub) {
-  return static_cast<size_t>(nsub) * (static_cast<size_t>(bm) * 128 + 4096 + 256 + 256);
+size_t tc_stage_bytes(int bm, int nsub, int nt) {
+  return static_cast<size_t>(nsub) *
+         (static_cast<size_t>(bm) * 128 + static_cast<size_t>(nt) * (4096 + 256 + 256));
 }
 
-size_t tc_smem_bytes(int bm, int nsub, int stages) {
+size_t tc_smem_bytes(int bm, int nsub, int nt, int stages) {
   const size_t bars = (2 * kMaxStages + kMaxTmemStages + 3) * 8;
-  return 1024 + tc_stage_bytes(bm, nsub) * stages + bars + 64;
+  return 1024 + tc_stage_bytes(bm, nsub, nt) * stages + bars + 64;
 }
 
-int tc_max_stages(int bm, int nsub) {
+int tc_max_stages(int bm, int nsub, int nt) {
   const size_t budget = 225 * 1024;
   int s = kMaxStages;
-  while (s > 2 && tc_smem_bytes(bm, nsub, s) > budget) --s;
+  while (s > 2 && tc_smem_bytes(bm, nsub, nt, s) > budget) --s;
   return s;
 }
 
@@ -209,14 +241,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages;
+  const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages, NT = p.nt;
   const uint32_t a_sub = static_cast<uint32_t>(BM) * 128;  // bytes of one 64-K activation tile
   Smem sm;
   sm.a = base;
-  sm.w = sm.a + static_cast<size_t>(S) * NS * a_sub;
-  sm.s = sm.w + static_cast<size_t>(S) * NS * 4096;
-  sm.z = sm.s + static_cast<size_t>(S) * NS * 256;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * NS * 256);
+  sm.w = sm.a + static_cast<size_t>(S) * NS * a_sub;             // [S][NT][NS][4096]
+  sm.s = sm.w + static_cast<size_t>(S) * NT * NS * 4096;          // [S][NT][NS * 256]
+  sm.z = sm.s + static_cast<size_t>(S) * NT * NS * 256;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * NT * NS * 256);
   sm.full = bars;
   sm.empty = bars + kMaxStages;
   sm.tfull = bars + 2 * kMaxStages;
@@ -285,24 +317,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         int mt, nt;
         tile_coords(p, u.tile, mt, nt);
-        const int32_t n0 = nt * kTileN;
+        const int32_t n0 = nt * NT * kTileN;       // first weight column of the CTA tile
         const int32_t y = mt * BM;
+        int ntv = p.n128 - nt * NT;                 // weight tiles that exist (ragged N)
+        if (ntv > NT) ntv = NT;
         const uint8_t* wsrc =
             args.b_packed +
-            ((static_cast<int64_t>(nt) * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * 2) *
+            ((static_cast<int64_t>(nt) * NT * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * 2) *
              kTileN) * 16;
+        const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           if (!mbar_wait(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
           const int k64_0 = kb * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
           const uint32_t fb = full0 + s * 8;
           if (wprod) {
-            mbar_arrive_expect_tx_a(fb, nv * 4096 + sc_bytes + zp_bytes);
-            bulk_g2s_a(w0 + s * NS * 4096, wsrc, nv * 4096, fb);
+            mbar_arrive_expect_tx_a(fb, ntv * nv * 4096 + NT * (sc_bytes + zp_bytes));
+            for (int t = 0; t < ntv; ++t)
+              bulk_g2s_a(w0 + (s * NT + t) * NS * 4096, wsrc + t * tile_stride, nv * 4096, fb);
             if (sc_bytes || zp_bytes) {
               const int g0 = k64_0 / sub_per_group;
-              if (sc_bytes) tma_load_2d_a(s0 + s * NS * 256, &smap, n0, g0, fb);
-              if (zp_bytes) tma_load_2d_a(z0 + s * NS * 256, &zmap, n0, g0, fb);
+              for (int t = 0; t < NT; ++t) {
+                if (sc_bytes)
+                  tma_load_2d_a(s0 + (s * NT + t) * NS * 256, &smap, n0 + t * kTileN, g0, fb);
+                if (zp_bytes)
+                  tma_load_2d_a(z0 + (s * NT + t) * NS * 256, &zmap, n0 + t * kTileN, g0, fb);
+              }
             }
             wsrc += NS * 4096;
           } else if (p.a3d) {
@@ -351,14 +391,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           const int k64_0 = (u.kb0 + j) * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
-          const uint32_t acol = tmem + p.acol + ts * NS * 32;
-          const uint64_t dsc = desc0 + s * NS * sub16;
-          if (nv == 4) {
-            mma_ts_stage16(tmem, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
-          } else {
-            mma_ts_stage(tmem, acol, dsc, idesc, chunk_start ? 0u : 1u);
-            for (int q = 1; q < nv; ++q)
-              mma_ts_stage(tmem, acol + q * 32, dsc + q * sub16, idesc, 1u);
+          for (int t = 0; t < NT; ++t) {
+            const uint32_t dcol = tmem + t * BM;
+            const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
+            const uint64_t dsc = desc0 + s * NS * sub16;
+            if (nv == 4) {
+              mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+            } else {
+              mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
+              for (int q = 1; q < nv; ++q)
+                mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
+            }
           }
           mma_commit(&sm.empty[s]);
           chunk_start = false;
@@ -398,10 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
       int mt, nt;
       tile_coords(p, u.tile, mt, nt);
-      const int64_t n0 = static_cast<int64_t>(nt) * kTileN;
-      const int valid_n = static_cast<int>(N - n0 < kTileN ? N - n0 : kTileN);
+      const int64_t n0 = static_cast<int64_t>(nt) * NT * kTileN;  // first weight column
       const int64_t m0 = static_cast<int64_t>(mt) * BM;
-      const bool row_ok = r < valid_n;
       const int nkb = u.kb1 - u.kb0;
       bool first_chunk = true;
       for (int j = 0; j < nkb; ++j, ++it) {
@@ -424,41 +465,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int k64_0 = (u.kb0 + j) * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
           const int g0 = k64_0 / sub_per_group;
-          const uint8_t* wst = sm.w + static_cast<size_t>(s) * NS * 4096;
-          const uint8_t* sst = sm.s + static_cast<size_t>(s) * NS * 256;
-          const uint8_t* zst = sm.z + static_cast<size_t>(s) * NS * 256;
-          const uint32_t tcol = tmem + lane_base + p.acol + ts * NS * 32;
-          for (int qq = 0; qq < nv; ++qq) {
-            const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
-            const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
-            const int grow = (k64_0 + qq) / sub_per_group - g0;
-            uint32_t s2 = 0, nz2 = 0;
-            bool has_s = true;
-            if (MODE == kW4A8) {
-              has_s = args.scales != nullptr;
-              if (has_s) {
-                const float sg = static_cast<float>(
-                    reinterpret_cast<const int8_t*>(sst + grow * 128)[r]);
-                s2 = as_u32(__float2bfloat162_rn(sg));
+          for (int t = 0; t < NT; ++t) {
+            const size_t st_idx = static_cast<size_t>(s) * NT + t;
+            const uint8_t* wst = sm.w + st_idx * NS * 4096;
+            const uint8_t* sst = sm.s + st_idx * NS * 256;
+            const uint8_t* zst = sm.z + st_idx * NS * 256;
+            const uint32_t tcol = tmem + lane_base + p.acol + (ts * NT + t) * NS * 32;
+            const bool row_ok = n0 + t * kTileN + r < N;
+            for (int qq = 0; qq < nv; ++qq) {
+              const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
+              const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
+              const int grow = (k64_0 + qq) / sub_per_group - g0;
+              uint32_t s2 = 0, nz2 = 0;
+              bool has_s = true;
+              if (MODE == kW4A8) {
+                has_s = args.scales != nullptr;
+                if (has_s) {
+                  const float sg = static_cast<float>(
+                      reinterpret_cast<const int8_t*>(sst + grow * 128)[r]);
+                  s2 = as_u32(__float2bfloat162_rn(sg));
+                }
+              } else {
+                const uint16_t sv = reinterpret_cast<const uint16_t*>(sst + grow * 256)[r];
+                s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
+                if (args.zeros) {
+                  const uint16_t zv =
+                      reinterpret_cast<const uint16_t*>(zst + grow * 256)[r] ^ 0x8000u;
+                  nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
+                }
               }
-            } else {
-              const uint16_t sv = reinterpret_cast<const uint16_t*>(sst + grow * 256)[r];
-              s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
-              if (args.zeros) {
-                const uint16_t zv = reinterpret_cast<const uint16_t*>(zst + grow * 256)[r] ^ 0x8000u;
-                nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
-              }
-            }
-            uint32_t v[32];
-            uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
-            uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
-            convert_chunk<MODE>(w0, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v0);
-            convert_chunk<MODE>(w1, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v1);
-            if (!row_ok) {
+              uint32_t v[32];
+              uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+              uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
+              convert_chunk<MODE>(w0, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v0);
+              convert_chunk<MODE>(w1, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v1);
+              if (!row_ok) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0;
+                for (int i = 0; i < 32; ++i) v[i] = 0;
+              }
+              tmem_st32(tcol + qq * 32, v);
             }
-            tmem_st32(tcol + qq * 32, v);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -481,17 +527,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool final_ev = (j == nkb - 1);
         float* partf = static_cast<float*>(args.partials);
         int32_t* parti = static_cast<int32_t*>(args.partials);
-        const size_t slot_elems = static_cast<size_t>(kTileN) * BM;
-        const size_t my_slot = (static_cast<size_t>(blockIdx.x) * p.max_segs + u.seg) * slot_elems;
-        for (int b = grp; b < nblk; b += kConvGroups) {
-          const int cc = b * 8;
-          const uint32_t dcol = tmem + lane_base + cc;
+        const size_t slot_elems = static_cast<size_t>(NT) * kTileN * BM;
+        const size_t my_slot = own_slot(p, u) * slot_elems;
+        // blocks of 8 accumulator columns over all weight tiles, round-robin
+        // over the converter groups
+        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+          const uint32_t dcol = tmem + lane_base + t * BM + cc;
+          const int64_t nrow = n0 + t * kTileN + r;  // output column
           uint32_t d[8];
           tmem_ld8(dcol, d);
           tmem_wait_ld();
           int32_t iv[8];
           if (MODE == kW4A8) {
-            const uint32_t icol = dcol + BM;  // int32 running sum of earlier chunks
+            // int32 running sum of the earlier chunks of this unit
+            const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
             uint32_t prev[8];
             if (!first_chunk) {
               tmem_ld8(icol, prev);
@@ -515,18 +565,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int i = 0; i < 8; ++i) {
             const int col = cc + i;
             if (u.nslots > 1) {
-              const size_t off = my_slot + static_cast<size_t>(col) * kTileN + r;
+              const size_t off = my_slot + static_cast<size_t>(t * BM + col) * kTileN + r;
               if (MODE == kW4A8) parti[off] = iv[i];
               else partf[off] = __uint_as_float(d[i]);
             } else {
               const int64_t m = m0 + col;
-              if (row_ok && m < M) {
-                const int64_t o = m * N + n0 + r;
+              if (nrow < N && m < M) {
+                const int64_t o = m * N + nrow;
                 if (MODE == kW4A8) {
                   if (args.out_s32) static_cast<int32_t*>(args.out)[o] = iv[i];
                   else
                     static_cast<__half*>(args.out)[o] = __float2half_rn(
-                        static_cast<float>(iv[i]) * args.s_tok[m] * args.s_ch[n0 + r]);
+                        static_cast<float>(iv[i]) * args.s_tok[m] * args.s_ch[nrow]);
                 } else {
                   static_cast<T16*>(args.out)[o] = to_t16<T16>(__uint_as_float(d[i]));
                 }
@@ -549,27 +599,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
         if (prev_count != u.nslots - 1) continue;
         __threadfence();
-        for (int b = grp; b < nblk; b += kConvGroups) {
+        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+          const int64_t nrow = n0 + t * kTileN + r;
           for (int i = 0; i < 8; ++i) {
-            const int col = b * 8 + i;
+            const int col = cc + i;
             float accf = 0.f;
             int32_t acci = 0;
             for (int sl = 0; sl < u.nslots; ++sl) {
-              const int64_t cpr = u.cfirst + sl;
-              const int64_t seg = u.tile - sk_start(cpr, wk.T, wk.G) / wk.kb;
-              const size_t off = (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems +
-                                 static_cast<size_t>(col) * kTileN + r;
+              const size_t off = slot_index(p, wk, u, sl) * slot_elems +
+                                 static_cast<size_t>(t * BM + col) * kTileN + r;
               if (MODE == kW4A8) acci += __ldcg(parti + off);
               else accf = sl == 0 ? __ldcg(partf + off) : accf + __ldcg(partf + off);
             }
             const int64_t m = m0 + col;
-            if (row_ok && m < M) {
-              const int64_t o = m * N + n0 + r;
+            if (nrow < N && m < M) {
+              const int64_t o = m * N + nrow;
               if (MODE == kW4A8) {
                 if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci;
                 else
                   static_cast<__half*>(args.out)[o] = __float2half_rn(
-                      static_cast<float>(acci) * args.s_tok[m] * args.s_ch[n0 + r]);
+                      static_cast<float>(acci) * args.s_tok[m] * args.s_ch[nrow]);
               } else {
                 static_cast<T16*>(args.out)[o] = to_t16<T16>(accf);
               }

@@ -17,7 +17,8 @@ from parity import assert_fp16_within_ulp, assert_within
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp"]
+ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp",
+       "tc128x2_sk", "tc128x2_dp", "tc128x2_kp"]
 DK = ["dk8_sk", "dk16_sk"]
 
 
@@ -194,6 +195,23 @@ def test_prefill_llama3_70b(gpu_lib, N, K, M):
     assert_within(sub, ref, absref, "bf16", f"prefill {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("name", ["tc128x2_sk", "tc128x2_dp", "tc128x2_kp"])
+def test_prefill_two_weight_tiles(gpu_lib, name):
+    """CTAs covering two 128-column weight tiles at a full prefill shape
+    (ragged last weight tile: N = 8192 + 128 is an odd number of tiles)."""
+    w4 = gpu_lib
+    M, N, K = 1000, 8320, 8192
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4,
+                          layout=w4.NK_EXLLAMA, group_size=128, zeros=True, seed=5)
+    got = run_w4a16(w4, d, sched(w4, name))
+    rows, cols = samples(M, N, count=192, seed=N)
+    cols[:64] = N - 1 - np.arange(64)  # the lone last tile
+    sub = got[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
+    ref, absref = oracle.w4a16_elems(d["a"], d["w"], d["layout"], d["wtype"], d["s"], d["z"], 128,
+                                     K, N, rows, cols)
+    assert_within(sub, ref, absref, "bf16", f"two tiles {name}")
+
+
 # -------------------------------------------------------------------- W4A8 ---
 
 def run_w4a8(w4, e, out_dtype, schedule=-1):
@@ -209,7 +227,7 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 
 
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
-                                  "dk8_sk", "dk16_sk"])
+                                  "tc128x2_kp", "dk8_sk", "dk16_sk"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
@@ -235,7 +253,8 @@ def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
     a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(0)).to(torch.int8)
     sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
     e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
-    for name in ("tc16_sk", "tc128_dp", "simt", "dk8_sk"):
+    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk") + (("tc128x2_kp",) if gs == -1 else ())
+    for name in names:
         acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
         ref = oracle.w4a8(a, w, oracle.NK_EXLLAMA, w4.INT4, sg, gs, K, N)
         assert np.array_equal(acc.numpy().astype(np.int64), ref), name
@@ -253,6 +272,19 @@ def test_w4a8_qqq_per_channel(gpu_lib, M):
     assert np.array_equal(acc[rows, cols], ref_acc)
     ref = oracle.w4a8_scale(ref_acc, rows, cols, e["s_tok"], e["s_ch"])
     assert_fp16_within_ulp(out[rows, cols], ref, f"qqq per-channel M={M}")
+
+
+@pytest.mark.parametrize("M", [128, 1024])
+def test_w4a8_qqq_per_channel_split_k(gpu_lib, M):
+    """Two weight tiles per CTA, K split so that no unit passes one exact
+    fp32 chunk: bit-exact int32 at the full QQQ shape."""
+    w4 = gpu_lib
+    e = w4synth.gen_w4a8(M, w4synth.QQQ_N, w4synth.QQQ_K, group_size=-1, seed=1)
+    acc = run_w4a8(w4, e, torch.int32, sched(w4, "tc128x2_kp")).numpy().astype(np.int64)
+    rows, cols = samples(M, e["N"], count=256, seed=M + 1)
+    ref_acc = oracle.w4a8_elems(e["a"], e["w"], e["layout"], e["wtype"], None, -1, e["K"],
+                                e["N"], rows, cols)
+    assert np.array_equal(acc[rows, cols], ref_acc)
 
 
 @pytest.mark.parametrize("M", w4synth.QQQ_G128_M)
