@@ -45,6 +45,7 @@ const Schedule kSchedules[] = {
     {"dk8_sk", kEngineDk, 8, kStreamK, 1},            {"dk16_sk", kEngineDk, 16, kStreamK, 1},
     {"tc128x2_sk", kEngineTc, 128, kStreamK, 2},      {"tc128x2_dp", kEngineTc, 128, kDataParallel, 2},
     {"tc128x2_kp", kEngineTc, 128, kSplitK, 2},
+    {"ds8_sk", kEngineDs, 8, kStreamK, 1},            {"ds16_sk", kEngineDs, 16, kStreamK, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 constexpr size_t kCounterBytes = 64 * 1024;
@@ -73,6 +74,10 @@ bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs
   if (sc.engine == kEngineSimt) return true;
   if (sc.engine == kEngineDk)  // M rows in 8-row tiles; a 128-wide K block in one group
     return M <= sc.bm && (gs == K || gs % 128 == 0);
+  if (sc.engine == kEngineDs)  // also bulk copies of 16-byte-multiple scale rows
+    return M <= sc.bm && (gs == K || gs % 128 == 0) && N % 8 == 0 &&
+           !(mode == kW4A8 && has_sg && N % 16 != 0) &&
+           (N + kTileN - 1) / kTileN * 4 * 4 <= static_cast<int64_t>(kCounterBytes);
   if (N % 8 != 0) return false;                      // 16-byte scale rows
   if (mode == kW4A8 && has_sg && N % 16 != 0) return false;
   // tensor memory must hold the accumulators (and the W4A8 int32 copies)
@@ -218,11 +223,51 @@ DkPlan make_dk_plan(int si, int mode, int64_t M, int64_t N, int64_t K, size_t* w
   return p;
 }
 
+// Plan of the streamed skinny-M schedule: two persistent CTAs per SM over a
+// stream-K split of the (128-column tile, 128-K block) iterations.
+DsPlan make_ds_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
+  DsPlan p{};
+  p.mode = mode;
+  p.nj = kSchedules[si].bm / 8;
+  p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
+  p.kblocks = static_cast<int>((K + 127) / 128);
+  // two K blocks (16 KB of nibbles) per stage: each stage costs its producer
+  // thread a fixed few hundred nanoseconds, so stages must not be smaller
+  p.sb = 2;
+  p.stages = 16;
+  while (p.stages > 2 &&
+         ds_smem_bytes(p.sb, p.nj, static_cast<int>(M), p.stages) > kDsSmemBudget)
+    --p.stages;
+  p.smem_bytes = ds_smem_bytes(p.sb, p.nj, static_cast<int>(M), p.stages);
+  const int64_t T = static_cast<int64_t>(p.n_tiles) * p.kblocks;
+  // every CTA streams at least eight blocks (four stages): a CTA has a fixed
+  // start-up cost, and a tile split over many CTAs a long reduction
+  int64_t g = kDsCtasPerSm * static_cast<int64_t>(sm_count());
+  if (g > (T + 7) / 8) g = (T + 7) / 8;
+  if (g < 1) g = 1;
+  p.grid = static_cast<int>(g);
+  int ms = 1;
+  for (int64_t c = 0; c < g; ++c) {
+    const int64_t b = c * T / g, e = (c + 1) * T / g;
+    if (e <= b) continue;
+    const int segs = static_cast<int>((e - 1) / p.kblocks - b / p.kblocks + 1);
+    if (segs > ms) ms = segs;
+  }
+  p.max_segs = ms;
+  p.ws_partials = kWsHeader + kCounterBytes;
+  const size_t part = static_cast<size_t>(p.grid) * p.max_segs * 8 * p.nj * kTileN * 4;
+  p.ws_prep = align256(p.ws_partials + part);
+  p.ws_total = align256(p.ws_prep + ds_prep_bytes(p.nj, static_cast<int>(M), p.kblocks));
+  return p;
+}
+
 int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
-  // skinny M: warp-level MMAs on register-dequantized weights
-  for (int si = 1; si < kNumSchedules; ++si)
-    if (kSchedules[si].engine == kEngineDk && schedule_fits(si, mode, M, N, K, gs, has_sg))
-      return si;
+  // skinny M: warp-level MMAs on dequantized weights; the streamed schedule
+  // first, the register-fed one where it cannot run (N not a multiple of 8)
+  for (int eng : {kEngineDs, kEngineDk})
+    for (int si = 1; si < kNumSchedules; ++si)
+      if (kSchedules[si].engine == eng && schedule_fits(si, mode, M, N, K, gs, has_sg))
+        return si;
   int bm = 16;
   while (bm < M && bm < 256) bm *= 2;
   if (mode == kW4A8 && bm > 128) bm = 128;
@@ -325,6 +370,7 @@ size_t ws_needed(int si, const Problem& pr) {
     make_dk_plan(si, pr.mode, pr.M, pr.N, pr.K, &wp, &wt);
     return wt;
   }
+  if (kSchedules[si].engine == kEngineDs) return make_ds_plan(si, pr.mode, pr.M, pr.N, pr.K).ws_total;
   return make_plan(si, pr.mode, pr.M, pr.N, pr.K, pr.gs).ws_total;
 }
 
@@ -468,6 +514,20 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
               dp.kblocks, dp.ksplit, dp.grid, dp.smem_bytes);
     cudaError_t e = launch_dk(dp, a, args, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "dk launch");
+  }
+  if (kSchedules[si].engine == kEngineDs) {
+    DsPlan dp = make_ds_plan(si, pr.mode, M, N, K);
+    args.counters = reinterpret_cast<int*>(ws + kWsHeader);
+    args.partials = ws + dp.ws_partials;
+    static const bool debug = getenv("W4_DEBUG") != nullptr;
+    if (debug)
+      fprintf(stderr,
+              "w4: %s M=%lld N=%lld K=%lld nj=%d tiles=%d kblocks=%d sb=%d stages=%d grid=%d "
+              "segs=%d smem=%zu\n",
+              kSchedules[si].name, (long long)M, (long long)N, (long long)K, dp.nj, dp.n_tiles,
+              dp.kblocks, dp.sb, dp.stages, dp.grid, dp.max_segs, dp.smem_bytes);
+    cudaError_t e = launch_ds(dp, a, args, ws + dp.ws_prep, s);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "ds launch");
   }
 
   TcPlan plan = make_plan(si, pr.mode, M, N, K, pr.gs);

@@ -32,7 +32,7 @@ constexpr size_t kWsHeader = 256;                // status word + spare
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
 
-enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2 };
+enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2, kEngineDs = 3 };
 enum Decomp { kDataParallel = 0, kStreamK = 1, kSplitK = 2 };
 
 struct Schedule {
@@ -99,6 +99,22 @@ struct DkPlan {
   size_t smem_bytes;
 };
 
+// Streamed skinny-M schedule (bulk-copied weight stages, mma.sync, stream-K).
+constexpr int kDsCtasPerSm = 2;
+constexpr size_t kDsSmemBudget = 108 * 1024;  // per CTA: two CTAs share an SM
+struct DsPlan {
+  int mode;
+  int nj;          // 8-row activation tiles: M <= 8 * nj
+  int n_tiles;     // 128-column weight tiles
+  int kblocks;     // 128-wide K blocks: ceil(K / 128)
+  int sb;          // K blocks per pipeline stage
+  int stages;      // shared-memory pipeline stages
+  int grid;        // persistent CTAs (two per SM)
+  int max_segs;    // tiles touched by one CTA (partial slots per CTA)
+  size_t smem_bytes;
+  size_t ws_partials, ws_prep, ws_total;  // workspace byte offsets / size
+};
+
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_prepack(const int32_t* w_q, int wtype, int layout, int64_t K, int64_t N,
                            uint8_t* out, cudaStream_t s);
@@ -110,6 +126,10 @@ cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtenso
                       const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
 cudaError_t launch_dk(const DkPlan& plan, const void* a, const TcArgs& args, cudaStream_t s);
 size_t dk_smem_bytes(int nj, int kbu_max);
+cudaError_t launch_ds(const DsPlan& plan, const void* a, const TcArgs& args, uint8_t* prep,
+                      cudaStream_t s);
+size_t ds_smem_bytes(int sb, int nj, int m, int stages);
+size_t ds_prep_bytes(int nj, int m, int kblocks);
 size_t tc_stage_bytes(int bm, int nsub, int nt);
 size_t tc_smem_bytes(int bm, int nsub, int nt, int stages);
 int tc_max_stages(int bm, int nsub, int nt);

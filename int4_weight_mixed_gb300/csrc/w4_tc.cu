@@ -599,6 +599,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
         if (prev_count != u.nslots - 1) continue;
         __threadfence();
+        // slot of contributor sl, computed once: lane sl holds it (broadcast
+        // by shuffle) when there are at most 32 contributors
+        const size_t lane_slot =
+            lane < u.nslots ? slot_index(p, wk, u, lane) * slot_elems : 0;
         for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
           const int t = bb / nblk, cc = (bb - t * nblk) * 8;
           const int64_t nrow = n0 + t * kTileN + r;
@@ -607,8 +611,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float accf = 0.f;
             int32_t acci = 0;
             for (int sl = 0; sl < u.nslots; ++sl) {
-              const size_t off = slot_index(p, wk, u, sl) * slot_elems +
-                                 static_cast<size_t>(t * BM + col) * kTileN + r;
+              const size_t sbase =
+                  u.nslots <= 32
+                      ? static_cast<size_t>(__shfl_sync(0xffffffffu,
+                                                        static_cast<unsigned long long>(lane_slot), sl))
+                      : slot_index(p, wk, u, sl) * slot_elems;
+              const size_t off = sbase + static_cast<size_t>(t * BM + col) * kTileN + r;
               if (MODE == kW4A8) acci += __ldcg(parti + off);
               else accf = sl == 0 ? __ldcg(partf + off) : accf + __ldcg(partf + off);
             }

@@ -43,15 +43,15 @@ def test_static_queries(lib):
 def test_default_heuristic(lib):
     import torch
     name = lambda M, N, K, dt, g: w4.schedule_names()[w4.default_schedule(M, N, K, dt, g)]
-    assert name(1, 8192, 21760, torch.int8, -1) == "dk8_sk"
-    assert name(8, 8192, 21760, torch.int8, 128) == "dk8_sk"
-    assert name(16, 4096, 4096, torch.bfloat16, 128) == "dk16_sk"
+    assert name(1, 8192, 21760, torch.int8, -1) == "ds8_sk"
+    assert name(8, 8192, 21760, torch.int8, 128) == "ds8_sk"
+    assert name(16, 4096, 4096, torch.bfloat16, 128) == "ds16_sk"
     assert name(16, 4096, 4096, torch.bfloat16, 64) == "tc16_sk"   # group 64 splits a K block
     assert name(32, 8192, 21760, torch.int8, -1) == "tc32_sk"
     assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
     assert name(1024, 8192, 21760, torch.int8, -1) == "tc128_sk"  # 512 tiles < 4 waves
     assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"
-    assert name(4, 13, 512, torch.float16, 128) == "dk8_sk"  # any N
+    assert name(4, 13, 512, torch.float16, 128) == "dk8_sk"  # any N (streamed needs N % 8 == 0)
     assert name(20, 13, 512, torch.float16, 128) == "simt"  # N % 8 != 0 beyond 16 rows
     assert w4.default_schedule(0, 8, 64, torch.float16, -1) == -1
 

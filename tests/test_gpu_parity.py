@@ -20,6 +20,7 @@ DEV = "cuda:0"
 ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp",
        "tc128x2_sk", "tc128x2_dp", "tc128x2_kp"]
 DK = ["dk8_sk", "dk16_sk"]
+DS = ["ds8_sk", "ds16_sk"]
 
 
 def sched(w4, name):
@@ -129,19 +130,35 @@ def test_w4a16_ragged(gpu_lib, M, N, K, gs, dt):
     assert_within(got.double().numpy(), ref, absref, fmt(dt), f"ragged {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("name", DK)
+@pytest.mark.parametrize("name", DK + DS)
 @pytest.mark.parametrize("M", [1, 3, 8, 13, 16])
 @pytest.mark.parametrize("dt,zeros,gs", [(torch.bfloat16, True, 128), (torch.float16, False, 128),
                                           (torch.bfloat16, False, -1), (torch.float16, True, 256)])
 def test_dk_w4a16(gpu_lib, name, M, dt, zeros, gs):
     w4 = gpu_lib
-    if M > (8 if name == "dk8_sk" else 16):
+    if M > (8 if name.endswith("8_sk") else 16):
         pytest.skip("more rows than the schedule's tile")
     d = w4synth.gen_w4a16(M, 392, 1280, act_dtype=dt, wtype=w4.UINT4 if zeros else w4.UINT4B8,
                           layout=w4.NK_EXLLAMA, group_size=gs, zeros=zeros, seed=M)
     got = run_w4a16(w4, d, sched(w4, name))
     ref, absref = oracle_w4a16(d)
     assert_within(got.double().numpy(), ref, absref, fmt(dt), f"{name} M={M}")
+
+
+@pytest.mark.parametrize("name", DS)
+@pytest.mark.parametrize("M,N,K,gs,dt", [
+    (5, 200, 576, -1, torch.bfloat16),    # K not a multiple of 128: half-full last block
+    (8, 136, 640, 128, torch.float16),    # ragged N, odd number of K blocks
+    (1, 8, 64, -1, torch.bfloat16),       # one 64-wide K block, one 8-column tile
+    (3, 4096, 4096, 128, torch.float16),  # several tiles per CTA's stream-K range
+])
+def test_ds_ragged(gpu_lib, name, M, N, K, gs, dt):
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=dt, wtype=w4.UINT4, layout=w4.NK_EXLLAMA,
+                          group_size=gs, zeros=True, seed=M + K)
+    got = run_w4a16(w4, d, sched(w4, name))
+    ref, absref = oracle_w4a16(d)
+    assert_within(got.double().numpy(), ref, absref, fmt(dt), f"{name} {M}x{N}x{K}")
 
 
 def test_w4a16_power_of_two_scales_exact(gpu_lib):
@@ -227,11 +244,11 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 
 
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
-                                  "tc128x2_kp", "dk8_sk", "dk16_sk"])
+                                  "tc128x2_kp", "dk8_sk", "dk16_sk", "ds8_sk", "ds16_sk"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
-    M = {"dk8_sk": 8, "dk16_sk": 13}.get(name, 40)
+    M = {"dk8_sk": 8, "dk16_sk": 13, "ds8_sk": 7, "ds16_sk": 16}.get(name, 40)
     e = w4synth.gen_w4a8(M, 384, 2048, group_size=gs, seed=7)
     acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
     ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, e["K"], e["N"])
@@ -253,7 +270,7 @@ def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
     a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(0)).to(torch.int8)
     sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
     e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
-    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk") + (("tc128x2_kp",) if gs == -1 else ())
+    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk", "ds8_sk") + (("tc128x2_kp",) if gs == -1 else ())
     for name in names:
         acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
         ref = oracle.w4a8(a, w, oracle.NK_EXLLAMA, w4.INT4, sg, gs, K, N)
