@@ -76,8 +76,7 @@ bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs
     return M <= sc.bm && (gs == K || gs % 128 == 0);
   if (sc.engine == kEngineDs)  // also bulk copies of 16-byte-multiple scale rows
     return M <= sc.bm && (gs == K || gs % 128 == 0) && N % 8 == 0 &&
-           !(mode == kW4A8 && has_sg && N % 16 != 0) &&
-           (N + kTileN - 1) / kTileN * 4 * 4 <= static_cast<int64_t>(kCounterBytes);
+           !(mode == kW4A8 && has_sg && N % 16 != 0);
   if (N % 8 != 0) return false;                      // 16-byte scale rows
   if (mode == kW4A8 && has_sg && N % 16 != 0) return false;
   // tensor memory must hold the accumulators (and the W4A8 int32 copies)
@@ -233,7 +232,7 @@ DsPlan make_ds_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
   p.kblocks = static_cast<int>((K + 127) / 128);
   // two K blocks (16 KB of nibbles) per stage: each stage costs its producer
   // thread a fixed few hundred nanoseconds, so stages must not be smaller
-  p.sb = 2;
+  p.sb = 2;  // must match the kernel's stage depth
   p.stages = 16;
   while (p.stages > 2 &&
          ds_smem_bytes(p.sb, p.nj, static_cast<int>(M), p.stages) > kDsSmemBudget)

@@ -56,6 +56,7 @@ constexpr int kDsConsumers = kTileN / kDsCols;    // 4
 constexpr int kDsWProd = kDsConsumers;            // weight producer warp
 constexpr int kDsAProd = kDsConsumers + 1;        // activation producer warp
 constexpr int kDsThreads = 32 * (kDsConsumers + 2);
+constexpr int kDsSB = 2;                          // K blocks per pipeline stage
 constexpr int kBlkK = 128;
 constexpr uint32_t kWBlk = 4 * kTileN * 16;       // prepacked bytes of one K block of a tile
 
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
   constexpr bool F16 = MODE == kW4A16_F16;
   using T16 = typename std::conditional<F16, __half, __nv_bfloat16>::type;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int SB = p.sb, S = p.stages;
+  const int SB = kDsSB, S = p.stages;
   const int64_t M = args.M, N = args.N, K = args.K;
   const DsLayout L = ds_layout(SB, NJ, static_cast<int>(M));
   const uint32_t ablk = ds_ablk(NJ, static_cast<int>(M));
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
   }
 
   // ------------------------------------------------------------ consumers
+  asm volatile("griddepcontrol.launch_dependents;");  // ds_reduce may launch and wait
   const int w = warp, g = lane >> 2, t = lane & 3;
   constexpr float kMagic = F16 ? 1024.f : 128.f;
   const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;
@@ -351,8 +353,11 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
   const uint32_t a_chunk = static_cast<uint32_t>(M) * 64;  // fragment bytes per chunk
   constexpr int MR = 8 * NJ;                               // rows of a partial slot
   const size_t slot_elems = static_cast<size_t>(MR) * kTileN;
-  float* pf = static_cast<float*>(args.partials);
-  int32_t* pi = static_cast<int32_t*>(args.partials);
+  // K blocks folded together: one scale group; with one group per column a
+  // run whose fp32 sums stay exact integers below 2^24 (W4A8: 4 blocks of
+  // |a| <= 128 times 128 + q <= 143), or the whole tile segment (W4A16).
+  const int fold_blocks =
+      pc ? (MODE == kW4A8 ? 4 : (1 << 30)) : static_cast<int>(args.group_size / kBlkK);
   auto store = [&](int64_t m, int64_t n, float vf, int32_t vi) {
     if (m >= M || n >= N) return;
     const int64_t o = m * N + n;
@@ -366,11 +371,6 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
     }
   };
 
-  // Tiles shared with other CTAs (at most the first and the last of this
-  // CTA's range): their partial sums are combined after this CTA's stream,
-  // so that no fence or atomic sits between two of its tiles.
-  DsUnit shared_u[2];
-  int nshared = 0;
   uint32_t it = 0;
   bool ok = true;
   DsUnit u;
@@ -378,15 +378,26 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
     const int64_t n0 = static_cast<int64_t>(u.tile) * kTileN;
     float res[kDsRP][NJ][4];
     int32_t ires[kDsRP][NJ][4];
+    float acc[2][kDsRP][NJ][4];  // [MMA parity h][R][j][e]: independent chains
+    float fsum[NJ][2];           // row sums of the blocks since the last fold
+    int isum[NJ][2];
 #pragma unroll
-    for (int R = 0; R < kDsRP; ++R)
+    for (int j = 0; j < NJ; ++j) {
 #pragma unroll
-      for (int j = 0; j < NJ; ++j)
+      for (int e = 0; e < 2; ++e) {
+        fsum[j][e] = 0.f;
+        isum[j][e] = 0;
+      }
+#pragma unroll
+      for (int R = 0; R < kDsRP; ++R)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           res[R][j][e] = 0.f;
           ires[R][j][e] = 0;
+          acc[0][R][j][e] = 0.f;
+          acc[1][R][j][e] = 0.f;
         }
+    }
     // scale / zero-point of row groups q (columns n0 + kDsCols*w + 8q + g)
     float sq[2 * kDsRP], cq[2 * kDsRP];
     int isq[2 * kDsRP];
@@ -406,16 +417,18 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
         }
       }
     }
-    for (int kb = u.kb0; kb < u.kb1; kb += SB, ++it) {
+    for (int kb = u.kb0; kb < u.kb1; kb += kDsSB, ++it) {
       const uint32_t s = it % S;
       if (!mbar_wait(&full[s], (it / S) & 1, abort, args.status)) {
         ok = false;
         break;
       }
-      const int nb = u.kb1 - kb < SB ? u.kb1 - kb : SB;
       const uint32_t st = sbase + s * L.stage;
       const uint8_t* stp = smem + static_cast<size_t>(s) * L.stage;
-      for (int b = 0; b < nb; ++b) {
+#pragma unroll
+      for (int b = 0; b < kDsSB; ++b) {
+        const int kbb = kb + b;
+        if (kbb >= u.kb1) break;
         uint32_t x[2 * kDsRP][4];  // [row group q][chunk c]: word t of row kDsCols*w + 8q + g
 #pragma unroll
         for (int q = 0; q < 2 * kDsRP; ++q)
@@ -427,32 +440,6 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             v[j][c] = live[j] ? lds128(ab + c * a_chunk + aoff[j]) : make_uint4(0, 0, 0, 0);
-        if (!pc) {
-#pragma unroll
-          for (int q = 0; q < 2 * kDsRP; ++q) {
-            const int row = kDsCols * w + 8 * q + g;
-            if (MODE == kW4A8) {
-              isq[q] = args.scales
-                           ? static_cast<int>(reinterpret_cast<const int8_t*>(stp + L.c + b * 256)[row])
-                           : 1;
-            } else {
-              sq[q] = ds_f32(reinterpret_cast<const T16*>(stp + L.c + b * 256)[row]);
-              const float z = args.zeros
-                                  ? ds_f32(reinterpret_cast<const T16*>(stp + L.z + b * 256)[row])
-                                  : 0.f;
-              cq[q] = F16 ? z : fmaf(mb, sq[q], z);
-            }
-          }
-        }
-        float acc[2][kDsRP][NJ][4];  // [MMA parity h][R][j][e]: independent chains
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int R = 0; R < kDsRP; ++R)
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc[h][R][j][e] = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -482,29 +469,60 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
                 mma16816<F16>(acc[h][R][j], a0, a1, a2, a3, b0, b1);
               }
             }
-        // fold the block into the running result
+        // block row sums
         const uint8_t* sums = stp + L.a + b * ablk + M * 256;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           const uint2 S2 = *reinterpret_cast<const uint2*>(sums + (j * 8 + 2 * t) * 4);
+          if (MODE == kW4A8) {
+            isum[j][0] += static_cast<int>(S2.x);
+            isum[j][1] += static_cast<int>(S2.y);
+          } else {
+            fsum[j][0] += __uint_as_float(S2.x);
+            fsum[j][1] += __uint_as_float(S2.y);
+          }
+        }
+        if (!pc) {  // the group's scale (and zero-point) rows
 #pragma unroll
-          for (int R = 0; R < kDsRP; ++R)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int q = 2 * R + (e >> 1);
-              const float a = acc[0][R][j][e] + acc[1][R][j][e];
-              if (MODE == kW4A8) {
-                // integers below 2^22: adding 1.5 * 2^23 leaves them in the
-                // low mantissa bits, read back exactly
-                const int bi = __float_as_int(a + 12582912.0f) - 0x4B400000;
-                const int Si = static_cast<int>((e & 1) ? S2.y : S2.x);
-                const int blk = bi - (128 + args.wbias) * Si;
-                ires[R][j][e] += pc ? blk : isq[q] * blk;
-              } else {
-                const float Sf = __uint_as_float((e & 1) ? S2.y : S2.x);
-                res[R][j][e] = fmaf(sq[q], a, fmaf(-cq[q], Sf, res[R][j][e]));
-              }
+          for (int q = 0; q < 2 * kDsRP; ++q) {
+            const int row = kDsCols * w + 8 * q + g;
+            if (MODE == kW4A8) {
+              isq[q] = args.scales
+                           ? static_cast<int>(reinterpret_cast<const int8_t*>(stp + L.c + b * 256)[row])
+                           : 1;
+            } else {
+              sq[q] = ds_f32(reinterpret_cast<const T16*>(stp + L.c + b * 256)[row]);
+              const float z = args.zeros
+                                  ? ds_f32(reinterpret_cast<const T16*>(stp + L.z + b * 256)[row])
+                                  : 0.f;
+              cq[q] = F16 ? z : fmaf(mb, sq[q], z);
             }
+          }
+        }
+        // fold at the end of a scale group / exact run, and of the segment
+        if (kbb + 1 == u.kb1 || (kbb + 1) % fold_blocks == 0) {
+#pragma unroll
+          for (int j = 0; j < NJ; ++j)
+#pragma unroll
+            for (int R = 0; R < kDsRP; ++R)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int q = 2 * R + (e >> 1);
+                const float a = acc[0][R][j][e] + acc[1][R][j][e];
+                acc[0][R][j][e] = 0.f;
+                acc[1][R][j][e] = 0.f;
+                if (MODE == kW4A8) {
+                  const int blk = __float2int_rn(a) - (128 + args.wbias) * isum[j][e & 1];
+                  ires[R][j][e] += pc ? blk : isq[q] * blk;
+                } else {
+                  res[R][j][e] = fmaf(sq[q], a, fmaf(-cq[q], fsum[j][e & 1], res[R][j][e]));
+                }
+              }
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+            fsum[j][0] = fsum[j][1] = 0.f;
+            isum[j][0] = isum[j][1] = 0;
+          }
         }
       }
       __syncwarp();
@@ -512,7 +530,7 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
     }
     if (!ok) break;
 
-    // ---- this tile's result: the output, or a partial slot
+    // ---- this tile's result: the output, or a partial slot for ds_reduce
     if (u.nslots == 1) {
 #pragma unroll
       for (int R = 0; R < kDsRP; ++R)
@@ -533,84 +551,76 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
         for (int e = 0; e < 4; ++e) {
           const size_t off = mine + static_cast<size_t>(j * 8 + 2 * t + (e & 1)) * kTileN +
                              kDsCols * w + 16 * R + g + 8 * (e >> 1);
-          if (MODE == kW4A8) pi[off] = ires[R][j][e];
-          else pf[off] = res[R][j][e];
+          if (MODE == kW4A8) static_cast<int32_t*>(args.partials)[off] = ires[R][j][e];
+          else static_cast<float*>(args.partials)[off] = res[R][j][e];
         }
-    if (nshared < 2) shared_u[nshared++] = u;
   }
-  if (!ok || nshared == 0) return;
+}
 
-  // ---- shared tiles: the last contributor (per warp sub-tile) adds the
-  // partial slots in K order and writes the output
-  __threadfence();
-  __syncwarp();
-  const int64_t T = static_cast<int64_t>(p.n_tiles) * p.kblocks;
-  for (int k = 0; k < nshared; ++k) {
-    const DsUnit& su = shared_u[k];
-    int prev = 0;
-    int* ctr = args.counters + static_cast<size_t>(su.tile) * kDsConsumers + w;
-    if (lane == 0) prev = atomicAdd(ctr, 1);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev != su.nslots - 1) continue;
-    __threadfence();
-    const int64_t n0 = static_cast<int64_t>(su.tile) * kTileN;
-    // slot of contributor sl (K order); lane sl computes it once
-    auto slot_base = [&](int sl) {
-      const int64_t cpr = su.cfirst + sl;
-      const int64_t seg = su.tile - ds_start(cpr, T, p.grid) / p.kblocks;
-      return (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems;
-    };
-    const unsigned long long lane_base = lane < su.nslots ? slot_base(lane) : 0;
-    float af[kDsRP][NJ][4];
-    int32_t ai[kDsRP][NJ][4];
-    constexpr int kBatch = 4;  // slots whose loads are in flight together
-    for (int s0 = 0; s0 < su.nslots; s0 += kBatch) {
-      uint32_t xs[kBatch][kDsRP][NJ][4];
+// -------------------------------------------------------------- ds_reduce
+// One CTA per 128-column tile: tiles that several CTAs share get the sum of
+// their partial slots, added in K order (deterministic), one thread per
+// output element.  Launched as a programmatic dependent of ds_gemm; waits
+// for it to complete.
+constexpr int kDsRedThreads = 256;
+constexpr int kDsRedMaxSlots = 64;  // slot offsets kept in shared memory
+
+template <int MODE, int NJ>
+__global__ void __launch_bounds__(kDsRedThreads) ds_reduce_kernel(const DsPlan p, const TcArgs args) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  using T16 = typename std::conditional<MODE == kW4A16_F16, __half, __nv_bfloat16>::type;
+  __shared__ unsigned long long sbase[kDsRedMaxSlots];
+  const int64_t T = static_cast<int64_t>(p.n_tiles) * p.kblocks, G = p.grid;
+  const int tile = blockIdx.x;
+  const int64_t cf = ds_owner(static_cast<int64_t>(tile) * p.kblocks, T, G);
+  const int64_t cl = ds_owner((static_cast<int64_t>(tile) + 1) * p.kblocks - 1, T, G);
+  const int nslots = static_cast<int>(cl - cf + 1);
+  if (nslots == 1) return;
+  const size_t slot_elems = static_cast<size_t>(8 * NJ) * kTileN;
+  auto slot_base = [&](int sl) -> unsigned long long {
+    const int64_t cpr = cf + sl;
+    const int64_t seg = tile - ds_start(cpr, T, G) / p.kblocks;
+    return (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems;
+  };
+  for (int sl = threadIdx.x; sl < nslots && sl < kDsRedMaxSlots; sl += kDsRedThreads)
+    sbase[sl] = slot_base(sl);
+  __syncthreads();
+  const uint32_t* part = static_cast<const uint32_t*>(args.partials);
+  const int64_t M = args.M, N = args.N;
+  for (int idx = threadIdx.x; idx < M * kTileN; idx += kDsRedThreads) {
+    const int m = idx / kTileN, col = idx % kTileN;
+    const int64_t n = static_cast<int64_t>(tile) * kTileN + col;
+    if (n >= N) continue;
+    const size_t off = static_cast<size_t>(m) * kTileN + col;
+    float af = 0.f;
+    int32_t ai = 0;
+    constexpr int kBatch = 8;  // slot loads in flight together
+    for (int s0 = 0; s0 < nslots; s0 += kBatch) {
+      uint32_t x[kBatch];
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int sl = s0 + q;
-        if (sl >= su.nslots) break;
-        const size_t base = su.nslots <= 32 ? static_cast<size_t>(__shfl_sync(0xffffffffu, lane_base, sl))
-                                            : slot_base(sl);
-#pragma unroll
-        for (int R = 0; R < kDsRP; ++R)
-#pragma unroll
-          for (int j = 0; j < NJ; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              xs[q][R][j][e] = __ldcg(reinterpret_cast<const uint32_t*>(pi) + base +
-                                      static_cast<size_t>(j * 8 + 2 * t + (e & 1)) * kTileN +
-                                      kDsCols * w + 16 * R + g + 8 * (e >> 1));
+        x[q] = sl < nslots
+                   ? part[(sl < kDsRedMaxSlots ? sbase[sl] : slot_base(sl)) + off]
+                   : 0u;
       }
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int sl = s0 + q;
-        if (sl >= su.nslots) break;
-#pragma unroll
-        for (int R = 0; R < kDsRP; ++R)
-#pragma unroll
-          for (int j = 0; j < NJ; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (MODE == kW4A8) {
-                const int32_t x = static_cast<int32_t>(xs[q][R][j][e]);
-                ai[R][j][e] = sl == 0 ? x : ai[R][j][e] + x;
-              } else {
-                const float x = __uint_as_float(xs[q][R][j][e]);
-                af[R][j][e] = sl == 0 ? x : af[R][j][e] + x;
-              }
-            }
+        if (sl >= nslots) break;
+        if (MODE == kW4A8) ai += static_cast<int32_t>(x[q]);
+        else af = sl == 0 ? __uint_as_float(x[q]) : af + __uint_as_float(x[q]);
       }
     }
-#pragma unroll
-    for (int R = 0; R < kDsRP; ++R)
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          store(j * 8 + 2 * t + (e & 1), n0 + kDsCols * w + 16 * R + g + 8 * (e >> 1),
-                af[R][j][e], ai[R][j][e]);
-    if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
+    const int64_t o = m * N + n;
+    if (MODE == kW4A8) {
+      if (args.out_s32) static_cast<int32_t*>(args.out)[o] = ai;
+      else
+        static_cast<__half*>(args.out)[o] =
+            __float2half_rn(static_cast<float>(ai) * args.s_tok[m] * args.s_ch[n]);
+    } else {
+      static_cast<T16*>(args.out)[o] = ds_t16<T16>(af);
+    }
   }
 }
 
@@ -641,7 +651,12 @@ cudaError_t launch_ds_t(const DsPlan& plan, const void* a, const TcArgs& args, u
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fn, plan, args, static_cast<const uint8_t*>(prep));
+  e = cudaLaunchKernelEx(&cfg, fn, plan, args, static_cast<const uint8_t*>(prep));
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(plan.n_tiles);
+  cfg.blockDim = dim3(kDsRedThreads);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, &ds_reduce_kernel<MODE, NJ>, plan, args);
 }
 }  // namespace
 
