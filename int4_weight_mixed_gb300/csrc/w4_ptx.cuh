@@ -233,6 +233,32 @@ __device__ __forceinline__ void mma_ts_stage16(uint32_t d_tmem, uint32_t a0, uin
       : "memory");
 }
 
+// Eight MMAs from explicit operands (A tensor-memory columns a[i], B
+// descriptors b[i]), all formed before the first one issues.  The issuing
+// thread is held inside each MMA for about its execution time, so the work
+// it does between MMA groups leaves the tensor pipe idle: the more MMAs per
+// group, the less that costs.
+__device__ __forceinline__ void mma_ts_8(uint32_t d_tmem, const uint32_t (&a)[8],
+                                         const uint64_t (&b)[8], uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %17, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %18, %1, t;\n\t}" ::"r"(d_tmem),
+      "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
+      "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]),
+      "l"(b[5]), "l"(b[6]), "l"(b[7])
+      : "memory");
+}
+
 // 3-D tiled tensor copy global -> shared.
 __device__ __forceinline__ void tma_load_3d_a(uint32_t dst, const CUtensorMap* map, int32_t x,
                                               int32_t y, int32_t z, uint32_t bar) {

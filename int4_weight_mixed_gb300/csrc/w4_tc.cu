@@ -378,40 +378,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         bool chunk_start = true;
         const int nkb = u.kb1 - u.kb0;
-        for (int j = 0; j < nkb; ++j) {
-          if (chunk_start && ev > 0) {
-            if (!mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) { ok = false; break; }
-          }
-          // The converter group arrives on tfull only after it observed the
-          // stage's full barrier, so tfull also orders the activation tile.
-          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int k64_0 = (u.kb0 + j) * NS;
-          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
-          for (int t = 0; t < NT; ++t) {
-            const uint32_t dcol = tmem + t * BM;
-            const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
-            const uint64_t dsc = desc0 + s * NS * sub16;
-            if (nv == 4) {
-              mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
-            } else {
-              mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
-              for (int q = 1; q < nv; ++q)
-                mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
-            }
-          }
-          mma_commit(&sm.empty[s]);
-          chunk_start = false;
-          const bool chunk_end =
-              (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
-          if (chunk_end) {
-            mma_commit(sm.dfull);
-            ++ev;
-            chunk_start = true;
-          }
+        auto chunk_end_at = [&](int j) {
+          return (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
+        };
+        auto advance = [&]() {
           if (++s == static_cast<uint32_t>(S)) {
             s = 0;
             ph ^= 1;
@@ -420,6 +390,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ts = 0;
             tph ^= 1;
           }
+        };
+        for (int j = 0; j < nkb;) {
+          if (chunk_start && ev > 0) {
+            if (!mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) { ok = false; break; }
+          }
+          // One-block stages go to the tensor pipe two at a time (eight MMAs
+          // per group) when both belong to the same exact chunk.
+          const bool pair = NS == 1 && NT == 1 && TS >= 2 && !chunk_end_at(j);
+          // The converter group arrives on tfull only after it observed the
+          // stage's full barrier, so tfull also orders the activation tile.
+          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t s1 = s, ts1 = ts;
+          uint32_t s2 = s + 1, ts2 = ts + 1, tph2 = tph;
+          if (s2 == static_cast<uint32_t>(S)) s2 = 0;
+          if (ts2 == static_cast<uint32_t>(TS)) {
+            ts2 = 0;
+            tph2 ^= 1;
+          }
+          if (pair && !mbar_wait(&sm.tfull[ts2], tph2, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool two_blocks = NS == 2 && NT == 1 && p.k64 - (u.kb0 + j) * NS >= 2;
+          if (pair || two_blocks) {
+            // eight MMAs: two stages of one 64-K block, or one stage of two
+            uint32_t a8[8];
+            uint64_t b8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int half = i >> 2, kk = i & 3;
+              if (pair) {
+                a8[i] = tmem + p.acol + (half ? ts2 : ts1) * 32 + 8 * kk;
+                b8[i] = desc0 + (half ? s2 : s1) * sub16 + 2 * kk;
+              } else {
+                a8[i] = tmem + p.acol + ts1 * 64 + 32 * half + 8 * kk;
+                b8[i] = desc0 + s1 * 2 * sub16 + half * sub16 + 2 * kk;
+              }
+            }
+            mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+          } else {
+            const int k64_0 = (u.kb0 + j) * NS;
+            const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+            for (int t = 0; t < NT; ++t) {
+              const uint32_t dcol = tmem + t * BM;
+              const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
+              const uint64_t dsc = desc0 + s * NS * sub16;
+              if (nv == 4) {
+                mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+              } else {
+                mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
+                for (int q = 1; q < nv; ++q)
+                  mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
+              }
+            }
+          }
+          mma_commit(&sm.empty[s1]);
+          advance();
+          if (pair) {
+            mma_commit(&sm.empty[s2]);
+            advance();
+            ++j;
+          }
+          chunk_start = false;
+          if (chunk_end_at(j)) {
+            mma_commit(sm.dfull);
+            ++ev;
+            chunk_start = true;
+          }
+          ++j;
         }
       }
       // All issued MMAs complete before tensor memory is released.
