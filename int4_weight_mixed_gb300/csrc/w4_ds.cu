@@ -193,6 +193,9 @@ __global__ void __launch_bounds__(128 * NJ) ds_prep_kernel(const void* __restric
                                                             uint8_t* __restrict__ prep) {
   // let the dependent GEMM launch now: its weight stream does not need us
   asm volatile("griddepcontrol.launch_dependents;");
+  // the previous kernel of the stream (which may produce the activations, and
+  // the previous call's GEMM, which reads this buffer) is complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr bool F16 = MODE == kW4A16_F16;
   using T16 = typename std::conditional<F16, __half, __nv_bfloat16>::type;
   __shared__ float fpart[4][NJ][32];
@@ -558,16 +561,18 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
 }
 
 // -------------------------------------------------------------- ds_reduce
-// One CTA per 128-column tile: tiles that several CTAs share get the sum of
-// their partial slots, added in K order (deterministic), one thread per
-// output element.  Launched as a programmatic dependent of ds_gemm; waits
-// for it to complete.
-constexpr int kDsRedThreads = 256;
+// Tiles that several CTAs share get the sum of their partial slots, added in
+// K order (deterministic): one thread per output element, a CTA covers two
+// rows of one 128-column tile.  Launched as a programmatic dependent of
+// ds_gemm; waits for it to complete.
+constexpr int kDsRedRows = 2;
+constexpr int kDsRedThreads = kDsRedRows * kTileN;
 constexpr int kDsRedMaxSlots = 64;  // slot offsets kept in shared memory
 
 template <int MODE, int NJ>
 __global__ void __launch_bounds__(kDsRedThreads) ds_reduce_kernel(const DsPlan p, const TcArgs args) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");  // the next call may start its prologue
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // ds_gemm is complete
   using T16 = typename std::conditional<MODE == kW4A16_F16, __half, __nv_bfloat16>::type;
   __shared__ unsigned long long sbase[kDsRedMaxSlots];
   const int64_t T = static_cast<int64_t>(p.n_tiles) * p.kblocks, G = p.grid;
@@ -585,42 +590,38 @@ __global__ void __launch_bounds__(kDsRedThreads) ds_reduce_kernel(const DsPlan p
   for (int sl = threadIdx.x; sl < nslots && sl < kDsRedMaxSlots; sl += kDsRedThreads)
     sbase[sl] = slot_base(sl);
   __syncthreads();
-  const uint32_t* part = static_cast<const uint32_t*>(args.partials);
   const int64_t M = args.M, N = args.N;
-  for (int idx = threadIdx.x; idx < M * kTileN; idx += kDsRedThreads) {
-    const int m = idx / kTileN, col = idx % kTileN;
-    const int64_t n = static_cast<int64_t>(tile) * kTileN + col;
-    if (n >= N) continue;
-    const size_t off = static_cast<size_t>(m) * kTileN + col;
-    float af = 0.f;
-    int32_t ai = 0;
-    constexpr int kBatch = 8;  // slot loads in flight together
-    for (int s0 = 0; s0 < nslots; s0 += kBatch) {
-      uint32_t x[kBatch];
+  const int m = blockIdx.y * kDsRedRows + threadIdx.x / kTileN, col = threadIdx.x % kTileN;
+  const int64_t n = static_cast<int64_t>(tile) * kTileN + col;
+  if (m >= M || n >= N) return;
+  const uint32_t* part = static_cast<const uint32_t*>(args.partials);
+  const size_t off = static_cast<size_t>(m) * kTileN + col;
+  float af = 0.f;
+  int32_t ai = 0;
+  constexpr int kBatch = 8;  // slot loads in flight together
+  for (int s0 = 0; s0 < nslots; s0 += kBatch) {
+    uint32_t x[kBatch];
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int sl = s0 + q;
-        x[q] = sl < nslots
-                   ? part[(sl < kDsRedMaxSlots ? sbase[sl] : slot_base(sl)) + off]
-                   : 0u;
-      }
+    for (int q = 0; q < kBatch; ++q) {
+      const int sl = s0 + q;
+      x[q] = sl < nslots ? part[(sl < kDsRedMaxSlots ? sbase[sl] : slot_base(sl)) + off] : 0u;
+    }
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int sl = s0 + q;
-        if (sl >= nslots) break;
-        if (MODE == kW4A8) ai += static_cast<int32_t>(x[q]);
-        else af = sl == 0 ? __uint_as_float(x[q]) : af + __uint_as_float(x[q]);
-      }
+    for (int q = 0; q < kBatch; ++q) {
+      const int sl = s0 + q;
+      if (sl >= nslots) break;
+      if (MODE == kW4A8) ai += static_cast<int32_t>(x[q]);
+      else af = sl == 0 ? __uint_as_float(x[q]) : af + __uint_as_float(x[q]);
     }
-    const int64_t o = m * N + n;
-    if (MODE == kW4A8) {
-      if (args.out_s32) static_cast<int32_t*>(args.out)[o] = ai;
-      else
-        static_cast<__half*>(args.out)[o] =
-            __float2half_rn(static_cast<float>(ai) * args.s_tok[m] * args.s_ch[n]);
-    } else {
-      static_cast<T16*>(args.out)[o] = ds_t16<T16>(af);
-    }
+  }
+  const int64_t o = m * N + n;
+  if (MODE == kW4A8) {
+    if (args.out_s32) static_cast<int32_t*>(args.out)[o] = ai;
+    else
+      static_cast<__half*>(args.out)[o] =
+          __float2half_rn(static_cast<float>(ai) * args.s_tok[m] * args.s_ch[n]);
+  } else {
+    static_cast<T16*>(args.out)[o] = ds_t16<T16>(af);
   }
 }
 
@@ -628,8 +629,16 @@ namespace {
 template <int MODE, int NJ>
 cudaError_t launch_ds_t(const DsPlan& plan, const void* a, const TcArgs& args, uint8_t* prep,
                         cudaStream_t s) {
-  ds_prep_kernel<MODE, NJ><<<plan.kblocks, 128 * NJ, 0, s>>>(a, args.M, args.K, prep);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3(plan.kblocks);
+  pcfg.blockDim = dim3(128 * NJ);
+  pcfg.stream = s;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&pcfg, &ds_prep_kernel<MODE, NJ>, a, args.M, args.K, prep);
   if (e != cudaSuccess) return e;
   auto fn = &ds_gemm_kernel<MODE, NJ>;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -646,14 +655,11 @@ cudaError_t launch_ds_t(const DsPlan& plan, const void* a, const TcArgs& args, u
   cfg.blockDim = dim3(kDsThreads);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, fn, plan, args, static_cast<const uint8_t*>(prep));
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(plan.n_tiles);
+  cfg.gridDim = dim3(plan.n_tiles, static_cast<unsigned>((args.M + kDsRedRows - 1) / kDsRedRows));
   cfg.blockDim = dim3(kDsRedThreads);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, &ds_reduce_kernel<MODE, NJ>, plan, args);
