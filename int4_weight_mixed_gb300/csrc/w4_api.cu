@@ -222,7 +222,7 @@ DkPlan make_dk_plan(int si, int mode, int64_t M, int64_t N, int64_t K, size_t* w
   return p;
 }
 
-// Plan of the streamed skinny-M schedule: two persistent CTAs per SM over a
+// Plan of the streamed skinny-M schedule: two or three persistent CTAs per SM over a
 // stream-K split of the (128-column tile, 128-K block) iterations.
 DsPlan make_ds_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
   DsPlan p{};
@@ -235,13 +235,13 @@ DsPlan make_ds_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
   p.sb = 2;  // must match the kernel's stage depth
   p.stages = 16;
   while (p.stages > 2 &&
-         ds_smem_bytes(p.sb, p.nj, static_cast<int>(M), p.stages) > kDsSmemBudget)
+         ds_smem_bytes(p.sb, p.nj, static_cast<int>(M), p.stages) > ds_smem_budget(p.nj))
     --p.stages;
   p.smem_bytes = ds_smem_bytes(p.sb, p.nj, static_cast<int>(M), p.stages);
   const int64_t T = static_cast<int64_t>(p.n_tiles) * p.kblocks;
   // every CTA streams at least eight blocks (four stages): a CTA has a fixed
   // start-up cost, and a tile split over many CTAs a long reduction
-  int64_t g = kDsCtasPerSm * static_cast<int64_t>(sm_count());
+  int64_t g = ds_ctas_per_sm(p.nj) * static_cast<int64_t>(sm_count());
   if (g > (T + 7) / 8) g = (T + 7) / 8;
   if (g < 1) g = 1;
   p.grid = static_cast<int>(g);

@@ -47,9 +47,10 @@ namespace w4 {
 namespace {
 
 // A consumer warp owns kDsRP pairs of 8-row groups (16 weight columns per
-// pair, one m16n8k16 A tile).  Two CTAs of six warps share an SM: the
-// register file is split between the four SM sub-partitions, so the twelve
-// warps sit three deep per sub-partition (at most 168 registers a thread).
+// pair, one m16n8k16 A tile).  Two or three CTAs of six warps share an SM;
+// the register file is split between the four SM sub-partitions, so their
+// warps sit three deep (at most 168 registers a thread) or five deep (at
+// most 96) per sub-partition.
 constexpr int kDsRP = 2;                          // 32 weight columns per warp
 constexpr int kDsCols = 16 * kDsRP;
 constexpr int kDsConsumers = kTileN / kDsCols;    // 4
@@ -209,14 +210,17 @@ __global__ void __launch_bounds__(128 * NJ) ds_prep_kernel(const void* __restric
   float fs = 0.f;
   int is = 0;
   if (m < M && k0 < K) {  // K % 64 == 0: the 8 values are all inside or all outside
+    // fp16 fragments (W4A8, f16): the values of odd pairs (positions 2, 3, 6,
+    // 7) are divided by 16, exactly, to match weights read 16x too large
     if (MODE == kW4A8) {
       const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + m * K + k0);
       const int8_t* b8 = reinterpret_cast<const int8_t*>(&raw);
       uint32_t w[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const __nv_bfloat162 p = __floats2bfloat162_rn(static_cast<float>(b8[2 * h]),
-                                                       static_cast<float>(b8[2 * h + 1]));
+        const float f = (h & 1) ? 0.0625f : 1.f;
+        const __half2 p = __floats2half2_rn(static_cast<float>(b8[2 * h]) * f,
+                                            static_cast<float>(b8[2 * h + 1]) * f);
         w[h] = *reinterpret_cast<const uint32_t*>(&p);
         is += static_cast<int>(b8[2 * h]) + static_cast<int>(b8[2 * h + 1]);
       }
@@ -226,6 +230,16 @@ __global__ void __launch_bounds__(128 * NJ) ds_prep_kernel(const void* __restric
       const T16* e = reinterpret_cast<const T16*>(&v);
       fs = ((ds_f32(e[0]) + ds_f32(e[1])) + (ds_f32(e[2]) + ds_f32(e[3]))) +
            ((ds_f32(e[4]) + ds_f32(e[5])) + (ds_f32(e[6]) + ds_f32(e[7])));
+      if (F16) {
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const __half2 q16 = __float2half2_rn(0.0625f);
+#pragma unroll
+        for (int h = 1; h < 4; h += 2) {
+          __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&w[h]), q16);
+          w[h] = *reinterpret_cast<const uint32_t*>(&x);
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
   if (m < M) reinterpret_cast<uint4*>(blk)[(c * M + m) * 4 + (lane & 3)] = v;
@@ -252,7 +266,7 @@ __global__ void __launch_bounds__(128 * NJ) ds_prep_kernel(const void* __restric
 
 // ---------------------------------------------------------------- ds_gemm
 template <int MODE, int NJ>
-__global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
+__global__ void __launch_bounds__(kDsThreads, ds_ctas_per_sm(NJ))
     ds_gemm_kernel(const DsPlan p, const TcArgs args, const uint8_t* __restrict__ prep) {
   constexpr bool F16 = MODE == kW4A16_F16;
   using T16 = typename std::conditional<F16, __half, __nv_bfloat16>::type;
@@ -336,13 +350,22 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
   // ------------------------------------------------------------ consumers
   asm volatile("griddepcontrol.launch_dependents;");  // ds_reduce may launch and wait
   const int w = warp, g = lane >> 2, t = lane & 3;
-  constexpr float kMagic = F16 ? 1024.f : 128.f;
-  const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;
-  const float mb = kMagic + static_cast<float>(args.wbias);
-  uint32_t off2 = 0;
-  if (F16) {
-    const __half2 h = __float2half2_rn(mb);
-    off2 = *reinterpret_cast<const uint32_t*>(&h);
+  // fp16 MMA (W4A8, f16): a word's nibble pairs sit at bits 0-3 / 4-7 (and,
+  // after one shift, 8-11 / 12-15) of each half; OR-ed into the mantissa of
+  // 1024 they read as 1024 + q and 1024 + 16q, exact.  Subtracting
+  // 1024 + bias and 1024 + 16*bias leaves q - bias and 16*(q - bias); the
+  // activations of the second kind of pair were divided by 16 when staged.
+  // bf16 MMA (W4A16 bf16): the 7-bit mantissa holds one nibble, at bits 0-3
+  // (128 + q); the offset 128 + bias is folded out with the block row sums.
+  constexpr bool kFp16Mma = MODE != kW4A16_BF16;
+  const uint32_t magic = kFp16Mma ? 0x64006400u : 0x43004300u;
+  const float mb = 128.f + static_cast<float>(args.wbias);  // bf16 fold offset
+  uint32_t off_lo = 0, off_hi = 0;
+  if (kFp16Mma) {
+    const __half2 lo = __float2half2_rn(1024.f + static_cast<float>(args.wbias));
+    const __half2 hi = __float2half2_rn(1024.f + 16.f * static_cast<float>(args.wbias));
+    off_lo = *reinterpret_cast<const uint32_t*>(&lo);
+    off_hi = *reinterpret_cast<const uint32_t*>(&hi);
   }
   // ldmatrix row address of this lane: matrix (chunk) lane/8, row lane%8
   const uint32_t ldsm_off = (lane >> 3) * 2048 + (kDsCols * w + (lane & 7)) * 16;
@@ -357,10 +380,11 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
   constexpr int MR = 8 * NJ;                               // rows of a partial slot
   const size_t slot_elems = static_cast<size_t>(MR) * kTileN;
   // K blocks folded together: one scale group; with one group per column a
-  // run whose fp32 sums stay exact integers below 2^24 (W4A8: 4 blocks of
-  // |a| <= 128 times 128 + q <= 143), or the whole tile segment (W4A16).
+  // run whose fp32 sums stay exact integers below 2^24 (W4A8: 64 blocks of
+  // 128 products |a * (q - bias)| <= 128 * 8), or the whole tile segment
+  // (W4A16).
   const int fold_blocks =
-      pc ? (MODE == kW4A8 ? 4 : (1 << 30)) : static_cast<int>(args.group_size / kBlkK);
+      pc ? (MODE == kW4A8 ? 64 : (1 << 30)) : static_cast<int>(args.group_size / kBlkK);
   auto store = [&](int64_t m, int64_t n, float vf, int32_t vi) {
     if (m >= M || n >= N) return;
     const int64_t o = m * N + n;
@@ -416,7 +440,7 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
         } else {
           sq[q] = in ? ds_f32(static_cast<const T16*>(args.scales)[n]) : 0.f;
           const float z = (in && args.zeros) ? ds_f32(static_cast<const T16*>(args.zeros)[n]) : 0.f;
-          cq[q] = F16 ? z : fmaf(mb, sq[q], z);
+          cq[q] = kFp16Mma ? z : fmaf(mb, sq[q], z);
         }
       }
     }
@@ -450,26 +474,33 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
 #pragma unroll
             for (int R = 0; R < kDsRP; ++R) {
               const uint32_t xa = x[2 * R][c] >> (8 * h), xb = x[2 * R + 1][c] >> (8 * h);
-              uint32_t a0 = lop_and_or(xa, 0x000F000Fu, magic);
-              uint32_t a1 = lop_and_or(xb, 0x000F000Fu, magic);
-              uint32_t a2 = lop_and_or(xa >> 4, 0x000F000Fu, magic);
-              uint32_t a3 = lop_and_or(xb >> 4, 0x000F000Fu, magic);
-              if constexpr (F16) {  // exact: (1024 + q) - (1024 + bias)
-                const __half2 o = *reinterpret_cast<const __half2*>(&off2);
-                __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&a0), o);
-                __half2 r1 = __hsub2(*reinterpret_cast<__half2*>(&a1), o);
-                __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&a2), o);
-                __half2 r3 = __hsub2(*reinterpret_cast<__half2*>(&a3), o);
+              uint32_t a0, a1, a2, a3;
+              if constexpr (kFp16Mma) {
+                const __half2 lo = *reinterpret_cast<const __half2*>(&off_lo);
+                const __half2 hi = *reinterpret_cast<const __half2*>(&off_hi);
+                uint32_t p0 = lop_and_or(xa, 0x000F000Fu, magic);
+                uint32_t p1 = lop_and_or(xb, 0x000F000Fu, magic);
+                uint32_t p2 = lop_and_or(xa, 0x00F000F0u, magic);
+                uint32_t p3 = lop_and_or(xb, 0x00F000F0u, magic);
+                __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&p0), lo);
+                __half2 r1 = __hsub2(*reinterpret_cast<__half2*>(&p1), lo);
+                __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&p2), hi);
+                __half2 r3 = __hsub2(*reinterpret_cast<__half2*>(&p3), hi);
                 a0 = *reinterpret_cast<uint32_t*>(&r0);
                 a1 = *reinterpret_cast<uint32_t*>(&r1);
                 a2 = *reinterpret_cast<uint32_t*>(&r2);
                 a3 = *reinterpret_cast<uint32_t*>(&r3);
+              } else {
+                a0 = lop_and_or(xa, 0x000F000Fu, magic);
+                a1 = lop_and_or(xb, 0x000F000Fu, magic);
+                a2 = lop_and_or(xa >> 4, 0x000F000Fu, magic);
+                a3 = lop_and_or(xb >> 4, 0x000F000Fu, magic);
               }
 #pragma unroll
               for (int j = 0; j < NJ; ++j) {
                 const uint32_t b0 = h ? v[j][c].z : v[j][c].x;
                 const uint32_t b1 = h ? v[j][c].w : v[j][c].y;
-                mma16816<F16>(acc[h][R][j], a0, a1, a2, a3, b0, b1);
+                mma16816<kFp16Mma>(acc[h][R][j], a0, a1, a2, a3, b0, b1);
               }
             }
         // block row sums
@@ -498,7 +529,7 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
               const float z = args.zeros
                                   ? ds_f32(reinterpret_cast<const T16*>(stp + L.z + b * 256)[row])
                                   : 0.f;
-              cq[q] = F16 ? z : fmaf(mb, sq[q], z);
+              cq[q] = kFp16Mma ? z : fmaf(mb, sq[q], z);
             }
           }
         }
@@ -515,7 +546,7 @@ __global__ void __launch_bounds__(kDsThreads, kDsCtasPerSm)
                 acc[0][R][j][e] = 0.f;
                 acc[1][R][j][e] = 0.f;
                 if (MODE == kW4A8) {
-                  const int blk = __float2int_rn(a) - (128 + args.wbias) * isum[j][e & 1];
+                  const int blk = __float2int_rn(a);  // exact: sum of a * (q - bias)
                   ires[R][j][e] += pc ? blk : isq[q] * blk;
                 } else {
                   res[R][j][e] = fmaf(sq[q], a, fmaf(-cq[q], fsum[j][e & 1], res[R][j][e]));

@@ -100,8 +100,12 @@ struct DkPlan {
 };
 
 // Streamed skinny-M schedule (bulk-copied weight stages, mma.sync, stream-K).
-constexpr int kDsCtasPerSm = 2;
-constexpr size_t kDsSmemBudget = 108 * 1024;  // per CTA: two CTAs share an SM
+// CTAs per SM: three for up to 8 activation rows (about 110 registers a
+// thread), two for up to 16 (about 150)
+__host__ __device__ constexpr int ds_ctas_per_sm(int nj) { return nj == 1 ? 3 : 2; }
+__host__ __device__ constexpr size_t ds_smem_budget(int nj) {
+  return nj == 1 ? 72 * 1024 : 108 * 1024;
+}
 struct DsPlan {
   int mode;
   int nj;          // 8-row activation tiles: M <= 8 * nj
