@@ -166,13 +166,15 @@ def make_inputs(dev):
 
 
 def launches_per_step(w4):
-    """Kernels of this library one step launches: the skinny-M schedule is
-    one launch; the tensor-core W4A8 schedule adds its int8->bf16 staging."""
+    """Kernels of this library one step launches: the streamed skinny-M
+    schedule is three launches (activation staging, GEMM, reduction); the
+    tensor-core W4A8 schedule is two (int8->bf16 staging, GEMM); the
+    register-fed skinny-M and CUDA-core schedules one."""
     names = w4.schedule_names()
     n = 0
     for M in M_SWEEP:
         name = names[w4.default_schedule(M, N, K, torch.int8, -1)]
-        n += 2 if name.startswith("tc") else 1
+        n += 3 if name.startswith("ds") else 2 if name.startswith("tc") else 1
     return n
 
 
