@@ -46,6 +46,7 @@ const Schedule kSchedules[] = {
     {"tc128x2_sk", kEngineTc, 128, kStreamK, 2},      {"tc128x2_dp", kEngineTc, 128, kDataParallel, 2},
     {"tc128x2_kp", kEngineTc, 128, kSplitK, 2},
     {"ds8_sk", kEngineDs, 8, kStreamK, 1},            {"ds16_sk", kEngineDs, 16, kStreamK, 1},
+    {"tc256_kp", kEngineTc, 256, kSplitK, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 constexpr size_t kCounterBytes = 64 * 1024;
@@ -169,7 +170,14 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   bool long_units = p.kb_total > p.chunk_stages;
   if (p.decomp == kSplitK) long_units = (p.kb_total + p.ksplit - 1) / p.ksplit > p.chunk_stages;
   const int dcols = p.nt * p.bm;
-  p.icol = (mode == kW4A8 && long_units) ? dcols : 0;
+  // W4A8 units longer than one exact chunk keep an int32 running sum: in
+  // tensor memory beside the accumulators when that leaves two or more
+  // converted-weight stages, else in a per-CTA global scratch (its owner
+  // thread writes and reads it back, one element per accumulator cell).
+  const bool need_i = mode == kW4A8 && long_units;
+  const bool tmem_i = need_i && 512 - 2 * dcols >= 2 * p.nt * nsub * 32;
+  p.icol = tmem_i ? dcols : 0;
+  p.gicopy = need_i && !tmem_i ? 1 : 0;
   const int used = (p.icol ? 2 * dcols : dcols);
   p.acol = (used + 31) / 32 * 32;
   int ts = p.acol >= 512 ? 0 : (512 - p.acol) / (p.nt * nsub * 32);
@@ -179,7 +187,9 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   p.tstages = ts;
   p.ws_act = align256(p.ws_partials + part);
   size_t act = mode == kW4A8 ? static_cast<size_t>(M) * K * 2 : 0;
-  p.ws_total = align256(p.ws_act + act);
+  p.ws_icopy = align256(p.ws_act + act);
+  const size_t icopy = p.gicopy ? static_cast<size_t>(p.grid) * dcols * kTileN * 4 : 0;
+  p.ws_total = align256(p.ws_icopy + icopy);
   return p;
 }
 
@@ -269,9 +279,10 @@ int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs,
         return si;
   int bm = 16;
   while (bm < M && bm < 256) bm *= 2;
-  if (mode == kW4A8 && bm > 128) bm = 128;
+  // data-parallel for 256-row tiles (whole-tile CTAs beat stream-K's partial
+  // sums there even at under one wave) and for >= 4 waves of 128-row tiles
   const int64_t tiles = ((M + bm - 1) / bm) * ((N + kTileN - 1) / kTileN);
-  const bool dp = tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128;
+  const bool dp = bm >= 256 || (tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128);
   for (int si = 1; si < kNumSchedules; ++si) {
     const Schedule& sc = kSchedules[si];
     if (sc.engine == kEngineTc && sc.bm == bm && (sc.decomp == kDataParallel) == dp &&
@@ -532,6 +543,7 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   TcPlan plan = make_plan(si, pr.mode, M, N, K, pr.gs);
   args.counters = reinterpret_cast<int*>(ws + plan.ws_counters);
   args.partials = ws + plan.ws_partials;
+  args.icopy = reinterpret_cast<int32_t*>(ws + plan.ws_icopy);
   const void* act = a;
   if (pr.mode == kW4A8) {
     cudaError_t e = launch_a8_to_bf16(static_cast<const int8_t*>(a), M * K, ws + plan.ws_act, s);
@@ -598,10 +610,10 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   static const bool debug = getenv("W4_DEBUG") != nullptr;
   if (debug)
     fprintf(stderr,
-            "w4: %s M=%lld N=%lld K=%lld bm=%d nt=%d nsub=%d stages=%d tstages=%d icol=%d "
+            "w4: %s M=%lld N=%lld K=%lld bm=%d nt=%d nsub=%d stages=%d tstages=%d icol=%d gi=%d "
             "acol=%d gps=%d a3d=%d tiles=%d kb=%d grid=%d decomp=%d ksplit=%d segs=%d smem=%zu\n",
             kSchedules[si].name, (long long)M, (long long)N, (long long)K, plan.bm, plan.nt,
-            plan.nsub, plan.stages, plan.tstages, plan.icol, plan.acol, plan.gps, plan.a3d,
+            plan.nsub, plan.stages, plan.tstages, plan.icol, plan.gicopy, plan.acol, plan.gps, plan.a3d,
             plan.tiles, plan.kb_total, plan.grid, plan.decomp, plan.ksplit, plan.max_segs,
             plan.smem_bytes);
   cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);

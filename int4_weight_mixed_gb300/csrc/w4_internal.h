@@ -51,6 +51,7 @@ struct TcPlan {
   int n128;            // ceil(N / 128): prepacked weight tiles that exist
   int ksplit;          // kSplitK: K splits per tile
   int icol;            // W4A8: first tensor-memory column of the int32 copies (0 = none)
+  int gicopy;          // W4A8: int32 copies in global scratch instead (tensor memory full)
   int nsub;            // 64-wide K blocks per pipeline stage (1, 2 or 4)
   int stages;          // shared-memory pipeline stages
   int tstages;         // tensor-memory A stages (nsub * 32 columns each)
@@ -68,6 +69,7 @@ struct TcPlan {
   size_t ws_counters;  // byte offsets into the workspace
   size_t ws_partials;
   size_t ws_act;       // W4A8 bf16 activations
+  size_t ws_icopy;     // W4A8 int32 running sums (gicopy): grid x NT*BM*128 x 4 bytes
   size_t ws_total;
 };
 
@@ -85,6 +87,7 @@ struct TcArgs {
   int* status;
   int* counters;
   void* partials;
+  int32_t* icopy;          // tc W4A8 with gicopy: per-CTA int32 running sums
 };
 
 // Skinny-M schedule (mma.sync, weights dequantized into register fragments).

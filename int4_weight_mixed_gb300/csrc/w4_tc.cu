@@ -583,23 +583,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_wait_ld();
           int32_t iv[8];
           if (MODE == kW4A8) {
-            // int32 running sum of the earlier chunks of this unit
+            // int32 running sum of the earlier chunks of this unit: in tensor
+            // memory, or in this CTA's global scratch (element (column, row))
             const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
+            int32_t* gi = args.icopy +
+                          (static_cast<size_t>(blockIdx.x) * NT * BM + t * BM + cc) * kTileN + r;
             uint32_t prev[8];
             if (!first_chunk) {
-              tmem_ld8(icol, prev);
-              tmem_wait_ld();
+              if (p.gicopy) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) prev[i] = static_cast<uint32_t>(gi[i * kTileN]);
+              } else {
+                tmem_ld8(icol, prev);
+                tmem_wait_ld();
+              }
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               iv[i] = __float2int_rn(__uint_as_float(d[i])) +
                       (first_chunk ? 0 : static_cast<int32_t>(prev[i]));
             if (!final_ev) {
-              uint32_t st[8];
+              if (p.gicopy) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) st[i] = static_cast<uint32_t>(iv[i]);
-              tmem_st8(icol, st);
-              tmem_wait_st();
+                for (int i = 0; i < 8; ++i) gi[i * kTileN] = iv[i];
+              } else {
+                uint32_t st[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st[i] = static_cast<uint32_t>(iv[i]);
+                tmem_st8(icol, st);
+                tmem_wait_st();
+              }
               continue;
             }
           }

@@ -244,7 +244,8 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 
 
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
-                                  "tc128x2_kp", "dk8_sk", "dk16_sk", "ds8_sk", "ds16_sk"])
+                                  "tc128x2_kp", "tc256_kp", "tc256_sk", "tc256_dp", "dk8_sk",
+                                  "dk16_sk", "ds8_sk", "ds16_sk"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
@@ -270,7 +271,8 @@ def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
     a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(0)).to(torch.int8)
     sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
     e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
-    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk", "ds8_sk") + (("tc128x2_kp",) if gs == -1 else ())
+    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk", "ds8_sk", "tc256_sk", "tc256_dp") + (
+        ("tc128x2_kp", "tc256_kp") if gs == -1 else ())
     for name in names:
         acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
         ref = oracle.w4a8(a, w, oracle.NK_EXLLAMA, w4.INT4, sg, gs, K, N)
@@ -291,13 +293,14 @@ def test_w4a8_qqq_per_channel(gpu_lib, M):
     assert_fp16_within_ulp(out[rows, cols], ref, f"qqq per-channel M={M}")
 
 
+@pytest.mark.parametrize("name", ["tc128x2_kp", "tc256_kp"])
 @pytest.mark.parametrize("M", [128, 1024])
-def test_w4a8_qqq_per_channel_split_k(gpu_lib, M):
+def test_w4a8_qqq_per_channel_split_k(gpu_lib, M, name):
     """Two weight tiles per CTA, K split so that no unit passes one exact
     fp32 chunk: bit-exact int32 at the full QQQ shape."""
     w4 = gpu_lib
     e = w4synth.gen_w4a8(M, w4synth.QQQ_N, w4synth.QQQ_K, group_size=-1, seed=1)
-    acc = run_w4a8(w4, e, torch.int32, sched(w4, "tc128x2_kp")).numpy().astype(np.int64)
+    acc = run_w4a8(w4, e, torch.int32, sched(w4, name)).numpy().astype(np.int64)
     rows, cols = samples(M, e["N"], count=256, seed=M + 1)
     ref_acc = oracle.w4a8_elems(e["a"], e["w"], e["layout"], e["wtype"], None, -1, e["K"],
                                 e["N"], rows, cols)
