@@ -279,10 +279,9 @@ int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs,
         return si;
   int bm = 16;
   while (bm < M && bm < 256) bm *= 2;
-  // data-parallel for 256-row tiles (whole-tile CTAs beat stream-K's partial
-  // sums there even at under one wave) and for >= 4 waves of 128-row tiles
+  // stream-K balances fewer than four waves of wide tiles; data-parallel beyond
   const int64_t tiles = ((M + bm - 1) / bm) * ((N + kTileN - 1) / kTileN);
-  const bool dp = bm >= 256 || (tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128);
+  const bool dp = tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128;
   for (int si = 1; si < kNumSchedules; ++si) {
     const Schedule& sc = kSchedules[si];
     if (sc.engine == kEngineTc && sc.bm == bm && (sc.decomp == kDataParallel) == dp &&

@@ -659,33 +659,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // by shuffle) when there are at most 32 contributors
         const size_t lane_slot =
             lane < u.nslots ? slot_index(p, wk, u, lane) * slot_elems : 0;
+        // one 8-column block at a time; the loads of two slots x eight
+        // columns are in flight together, and the slots are added in K order
+        const uint32_t* part = reinterpret_cast<const uint32_t*>(args.partials);
         for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
           const int t = bb / nblk, cc = (bb - t * nblk) * 8;
           const int64_t nrow = n0 + t * kTileN + r;
-          for (int i = 0; i < 8; ++i) {
-            const int col = cc + i;
-            float accf = 0.f;
-            int32_t acci = 0;
-            for (int sl = 0; sl < u.nslots; ++sl) {
+          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r;
+          float accf[8];
+          int32_t acci[8];
+          constexpr int kBatch = 2;
+          for (int s0 = 0; s0 < u.nslots; s0 += kBatch) {
+            uint32_t x[kBatch][8];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+              const int sl = s0 + q;
+              if (sl >= u.nslots) break;
               const size_t sbase =
                   u.nslots <= 32
                       ? static_cast<size_t>(__shfl_sync(0xffffffffu,
                                                         static_cast<unsigned long long>(lane_slot), sl))
                       : slot_index(p, wk, u, sl) * slot_elems;
-              const size_t off = sbase + static_cast<size_t>(t * BM + col) * kTileN + r;
-              if (MODE == kW4A8) acci += __ldcg(parti + off);
-              else accf = sl == 0 ? __ldcg(partf + off) : accf + __ldcg(partf + off);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[q][i] = __ldcg(part + sbase + coff + i * kTileN);
             }
-            const int64_t m = m0 + col;
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+              const int sl = s0 + q;
+              if (sl >= u.nslots) break;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (MODE == kW4A8) {
+                  acci[i] = sl == 0 ? static_cast<int32_t>(x[q][i])
+                                    : acci[i] + static_cast<int32_t>(x[q][i]);
+                } else {
+                  accf[i] = sl == 0 ? __uint_as_float(x[q][i]) : accf[i] + __uint_as_float(x[q][i]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int64_t m = m0 + cc + i;
             if (nrow < N && m < M) {
               const int64_t o = m * N + nrow;
               if (MODE == kW4A8) {
-                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci;
+                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci[i];
                 else
                   static_cast<__half*>(args.out)[o] = __float2half_rn(
-                      static_cast<float>(acci) * args.s_tok[m] * args.s_ch[nrow]);
+                      static_cast<float>(acci[i]) * args.s_tok[m] * args.s_ch[nrow]);
               } else {
-                static_cast<T16*>(args.out)[o] = to_t16<T16>(accf);
+                static_cast<T16*>(args.out)[o] = to_t16<T16>(accf[i]);
               }
             }
           }
