@@ -47,6 +47,7 @@ const Schedule kSchedules[] = {
     {"tc128x2_kp", kEngineTc, 128, kSplitK, 2},
     {"ds8_sk", kEngineDs, 8, kStreamK, 1},            {"ds16_sk", kEngineDs, 16, kStreamK, 1},
     {"tc256_kp", kEngineTc, 256, kSplitK, 1},
+    {"ds32_sk", kEngineDs, 32, kStreamK, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 constexpr size_t kCounterBytes = 64 * 1024;
@@ -271,8 +272,9 @@ DsPlan make_ds_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
 }
 
 int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
-  // skinny M: warp-level MMAs on dequantized weights; the streamed schedule
-  // first, the register-fed one where it cannot run (N not a multiple of 8)
+  // skinny M (up to 32 rows with the streamed schedule, 16 with the
+  // register-fed one where the streamed one cannot run: N not a multiple of
+  // 8): warp-level MMAs on dequantized weights
   for (int eng : {kEngineDs, kEngineDk})
     for (int si = 1; si < kNumSchedules; ++si)
       if (kSchedules[si].engine == eng && schedule_fits(si, mode, M, N, K, gs, has_sg))

@@ -51,12 +51,18 @@ namespace {
 // the register file is split between the four SM sub-partitions, so their
 // warps sit three deep (at most 168 registers a thread) or five deep (at
 // most 96) per sub-partition.
-constexpr int kDsRP = 2;                          // 32 weight columns per warp
-constexpr int kDsCols = 16 * kDsRP;
-constexpr int kDsConsumers = kTileN / kDsCols;    // 4
-constexpr int kDsWProd = kDsConsumers;            // weight producer warp
-constexpr int kDsAProd = kDsConsumers + 1;        // activation producer warp
-constexpr int kDsThreads = 32 * (kDsConsumers + 2);
+// Up to 16 rows: 32 weight columns per warp (four consumer warps); 32 rows:
+// 16 columns per warp (eight consumer warps), so that the accumulators of
+// four activation tiles fit in registers.
+template <int NJ>
+struct DsShape {
+  static constexpr int RP = NJ >= 4 ? 1 : 2;
+  static constexpr int Cols = 16 * RP;
+  static constexpr int Consumers = kTileN / Cols;
+  static constexpr int WProd = Consumers;      // weight producer warp
+  static constexpr int AProd = Consumers + 1;  // activation producer warp
+  static constexpr int Threads = 32 * (Consumers + 2);
+};
 constexpr int kDsSB = 2;                          // K blocks per pipeline stage
 constexpr int kBlkK = 128;
 constexpr uint32_t kWBlk = 4 * kTileN * 16;       // prepacked bytes of one K block of a tile
@@ -266,8 +272,11 @@ __global__ void __launch_bounds__(128 * NJ) ds_prep_kernel(const void* __restric
 
 // ---------------------------------------------------------------- ds_gemm
 template <int MODE, int NJ>
-__global__ void __launch_bounds__(kDsThreads, ds_ctas_per_sm(NJ))
+__global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
     ds_gemm_kernel(const DsPlan p, const TcArgs args, const uint8_t* __restrict__ prep) {
+  constexpr int kDsRP = DsShape<NJ>::RP, kDsCols = DsShape<NJ>::Cols;
+  constexpr int kDsConsumers = DsShape<NJ>::Consumers;
+  constexpr int kDsWProd = DsShape<NJ>::WProd, kDsAProd = DsShape<NJ>::AProd;
   constexpr bool F16 = MODE == kW4A16_F16;
   using T16 = typename std::conditional<F16, __half, __nv_bfloat16>::type;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -461,14 +470,12 @@ __global__ void __launch_bounds__(kDsThreads, ds_ctas_per_sm(NJ))
         for (int q = 0; q < 2 * kDsRP; ++q)
           ldsm_x4(st + L.w + b * kWBlk + ldsm_off + q * 128, x[q]);
         const uint32_t ab = st + L.a + b * ablk;
-        uint4 v[NJ][4];
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
+        for (int c = 0; c < 4; ++c) {
+          uint4 v[NJ];  // this chunk's activation fragments
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            v[j][c] = live[j] ? lds128(ab + c * a_chunk + aoff[j]) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int j = 0; j < NJ; ++j)
+            v[j] = live[j] ? lds128(ab + c * a_chunk + aoff[j]) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -498,11 +505,12 @@ __global__ void __launch_bounds__(kDsThreads, ds_ctas_per_sm(NJ))
               }
 #pragma unroll
               for (int j = 0; j < NJ; ++j) {
-                const uint32_t b0 = h ? v[j][c].z : v[j][c].x;
-                const uint32_t b1 = h ? v[j][c].w : v[j][c].y;
+                const uint32_t b0 = h ? v[j].z : v[j].x;
+                const uint32_t b1 = h ? v[j].w : v[j].y;
                 mma16816<kFp16Mma>(acc[h][R][j], a0, a1, a2, a3, b0, b1);
               }
             }
+        }
         // block row sums
         const uint8_t* sums = stp + L.a + b * ablk + M * 256;
 #pragma unroll
@@ -678,12 +686,13 @@ cudaError_t launch_ds_t(const DsPlan& plan, const void* a, const TcArgs& args, u
   static const bool debug = getenv("W4_DEBUG") != nullptr;
   if (debug) {
     int blocks = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kDsThreads, plan.smem_bytes);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, DsShape<NJ>::Threads,
+                                                  plan.smem_bytes);
     fprintf(stderr, "w4: ds resident CTAs per SM: %d (smem %zu)\n", blocks, plan.smem_bytes);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
-  cfg.blockDim = dim3(kDsThreads);
+  cfg.blockDim = dim3(DsShape<NJ>::Threads);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -704,9 +713,14 @@ cudaError_t launch_ds(const DsPlan& plan, const void* a, const TcArgs& args, uin
     if (plan.mode == kW4A16_BF16) return launch_ds_t<kW4A16_BF16, 1>(plan, a, args, prep, s);
     return launch_ds_t<kW4A8, 1>(plan, a, args, prep, s);
   }
-  if (plan.mode == kW4A16_F16) return launch_ds_t<kW4A16_F16, 2>(plan, a, args, prep, s);
-  if (plan.mode == kW4A16_BF16) return launch_ds_t<kW4A16_BF16, 2>(plan, a, args, prep, s);
-  return launch_ds_t<kW4A8, 2>(plan, a, args, prep, s);
+  if (plan.nj == 2) {
+    if (plan.mode == kW4A16_F16) return launch_ds_t<kW4A16_F16, 2>(plan, a, args, prep, s);
+    if (plan.mode == kW4A16_BF16) return launch_ds_t<kW4A16_BF16, 2>(plan, a, args, prep, s);
+    return launch_ds_t<kW4A8, 2>(plan, a, args, prep, s);
+  }
+  if (plan.mode == kW4A16_F16) return launch_ds_t<kW4A16_F16, 4>(plan, a, args, prep, s);
+  if (plan.mode == kW4A16_BF16) return launch_ds_t<kW4A16_BF16, 4>(plan, a, args, prep, s);
+  return launch_ds_t<kW4A8, 4>(plan, a, args, prep, s);
 }
 
 }  // namespace w4

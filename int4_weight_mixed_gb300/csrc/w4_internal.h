@@ -104,10 +104,10 @@ struct DkPlan {
 
 // Streamed skinny-M schedule (bulk-copied weight stages, mma.sync, stream-K).
 // CTAs per SM: three for up to 8 activation rows (about 110 registers a
-// thread), two for up to 16 (about 150)
-__host__ __device__ constexpr int ds_ctas_per_sm(int nj) { return nj == 1 ? 3 : 2; }
+// thread), two for up to 16 (about 150), one of ten warps for up to 32
+__host__ __device__ constexpr int ds_ctas_per_sm(int nj) { return nj == 1 ? 3 : nj == 2 ? 2 : 1; }
 __host__ __device__ constexpr size_t ds_smem_budget(int nj) {
-  return nj == 1 ? 72 * 1024 : 108 * 1024;
+  return nj == 1 ? 72 * 1024 : nj == 2 ? 108 * 1024 : 216 * 1024;
 }
 struct DsPlan {
   int mode;

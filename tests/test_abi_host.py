@@ -47,7 +47,7 @@ def test_default_heuristic(lib):
     assert name(8, 8192, 21760, torch.int8, 128) == "ds8_sk"
     assert name(16, 4096, 4096, torch.bfloat16, 128) == "ds16_sk"
     assert name(16, 4096, 4096, torch.bfloat16, 64) == "tc16_sk"   # group 64 splits a K block
-    assert name(32, 8192, 21760, torch.int8, -1) == "tc32_sk"
+    assert name(32, 8192, 21760, torch.int8, -1) == "ds32_sk"
     assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
     assert name(1024, 8192, 21760, torch.int8, -1) == "tc256_sk"  # 256 tiles < 4 waves
     assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"

@@ -20,7 +20,8 @@ DEV = "cuda:0"
 ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp",
        "tc128x2_sk", "tc128x2_dp", "tc128x2_kp"]
 DK = ["dk8_sk", "dk16_sk"]
-DS = ["ds8_sk", "ds16_sk"]
+DS = ["ds8_sk", "ds16_sk", "ds32_sk"]
+ROWS = {"dk8_sk": 8, "dk16_sk": 16, "ds8_sk": 8, "ds16_sk": 16, "ds32_sk": 32}
 
 
 def sched(w4, name):
@@ -131,12 +132,12 @@ def test_w4a16_ragged(gpu_lib, M, N, K, gs, dt):
 
 
 @pytest.mark.parametrize("name", DK + DS)
-@pytest.mark.parametrize("M", [1, 3, 8, 13, 16])
+@pytest.mark.parametrize("M", [1, 3, 8, 13, 16, 27, 32])
 @pytest.mark.parametrize("dt,zeros,gs", [(torch.bfloat16, True, 128), (torch.float16, False, 128),
                                           (torch.bfloat16, False, -1), (torch.float16, True, 256)])
 def test_dk_w4a16(gpu_lib, name, M, dt, zeros, gs):
     w4 = gpu_lib
-    if M > (8 if name.endswith("8_sk") else 16):
+    if M > ROWS[name]:
         pytest.skip("more rows than the schedule's tile")
     d = w4synth.gen_w4a16(M, 392, 1280, act_dtype=dt, wtype=w4.UINT4 if zeros else w4.UINT4B8,
                           layout=w4.NK_EXLLAMA, group_size=gs, zeros=zeros, seed=M)
@@ -245,11 +246,11 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
                                   "tc128x2_kp", "tc256_kp", "tc256_sk", "tc256_dp", "dk8_sk",
-                                  "dk16_sk", "ds8_sk", "ds16_sk"])
+                                  "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
-    M = {"dk8_sk": 8, "dk16_sk": 13, "ds8_sk": 7, "ds16_sk": 16}.get(name, 40)
+    M = {"dk8_sk": 8, "dk16_sk": 13, "ds8_sk": 7, "ds16_sk": 16, "ds32_sk": 29}.get(name, 40)
     e = w4synth.gen_w4a8(M, 384, 2048, group_size=gs, seed=7)
     acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
     ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, e["K"], e["N"])
