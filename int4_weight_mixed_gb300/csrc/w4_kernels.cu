@@ -82,6 +82,9 @@ __global__ void unprepack_kernel(const uint32_t* __restrict__ packed, int wtype,
 
 __global__ void a8_to_bf16_kernel(const int8_t* __restrict__ a, int64_t count8,
                                   uint4* __restrict__ out) {
+  // the W4A8 tensor-core GEMM that follows may launch now: it streams weights
+  // until this grid is complete
+  asm volatile("griddepcontrol.launch_dependents;");
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count8;
        i += (int64_t)gridDim.x * blockDim.x) {
     uint2 v = reinterpret_cast<const uint2*>(a)[i];

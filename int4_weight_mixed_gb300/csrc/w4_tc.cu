@@ -306,6 +306,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // activation tile(s).
     if (lane == 0) {
       const bool wprod = warp == 0;
+      // W4A8: the activations come from the staging grid this one may have
+      // been launched beside (programmatic dependent launch); wait for it
+      if (!wprod) asm volatile("griddepcontrol.wait;" ::: "memory");
       uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       Unit u;
@@ -738,16 +741,30 @@ cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtenso
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem_bytes));
   if (e != cudaSuccess) return e;
-  if (plan.mode == kW4A16_F16)
+  if (plan.mode == kW4A16_F16) {
     tc_gemm_kernel<kW4A16_F16>
         <<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
-  else if (plan.mode == kW4A16_BF16)
+    return cudaGetLastError();
+  }
+  if (plan.mode == kW4A16_BF16) {
     tc_gemm_kernel<kW4A16_BF16>
         <<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
-  else
-    tc_gemm_kernel<kW4A8><<<plan.grid, kTcThreads, plan.smem_bytes, s>>>(amap, smap, zmap, plan,
-                                                                          args);
-  return cudaGetLastError();
+    return cudaGetLastError();
+  }
+  // W4A8: a programmatic dependent of its int8 -> bf16 staging launch; only
+  // the activation producer waits for that grid (weights and scales are not
+  // written by it), so the weight stream starts at once
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = plan.smem_bytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, &tc_gemm_kernel<kW4A8>, amap, smap, zmap, plan, args);
 }
 
 }  // namespace w4

@@ -363,3 +363,38 @@ def test_invalid_on_device_pointers(gpu_lib):
         w4.gemm(d["a"].to(DEV), b, d["wtype"], d["N"], scales=d["s"].to(DEV).bfloat16(),
                 group_size=128)
     assert ei.value.status == w4.ERR_INVALID_ARGUMENT
+
+
+def test_back_to_back_calls(gpu_lib):
+    """Calls of several schedules enqueued back to back on one stream, sharing
+    the cached workspace, with no synchronization between them: the launches
+    that overlap a previous call's tail (activation staging, programmatic
+    dependents) must leave every result equal to its oracle."""
+    w4 = gpu_lib
+    N, K = 1024, 2048
+    e1 = w4synth.gen_w4a8(1, N, K, group_size=-1, seed=21)
+    e2 = w4synth.gen_w4a8(8, N, K, group_size=-1, seed=22)
+    e3 = w4synth.gen_w4a8(300, N, K, group_size=-1, seed=23)
+    e4 = w4synth.gen_w4a8(24, N, K, group_size=128, seed=24)
+    d5 = w4synth.gen_w4a16(5, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4, group_size=128,
+                           zeros=True, seed=25)
+    jobs = []
+    for e in (e1, e2, e3, e4, e1, e3):
+        b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], e["K"], e["N"])
+        sg = None if e["sg"] is None else e["sg"].to(DEV)
+        jobs.append((e, b, e["a"].to(DEV), sg))
+    b5 = w4.prepack_B(d5["w"].to(DEV), d5["wtype"], d5["layout"], K, N)
+    a5, s5, z5 = d5["a"].to(DEV), d5["s"].to(DEV), d5["z"].to(DEV)
+    torch.cuda.synchronize()
+    outs = []
+    for i, (e, b, a, sg) in enumerate(jobs):
+        outs.append(w4.gemm(a, b, e["wtype"], N, scales=sg, group_size=e["group_size"],
+                            out_dtype=torch.int32))
+        if i == 2:
+            out5 = w4.gemm(a5, b5, d5["wtype"], N, scales=s5, zeros=z5, group_size=128)
+    torch.cuda.synchronize()
+    for (e, _, _, _), got in zip(jobs, outs):
+        ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], e["group_size"], K, N)
+        assert np.array_equal(got.cpu().numpy().astype(np.int64), ref)
+    ref, absref = oracle_w4a16(d5)
+    assert_within(out5.cpu().double().numpy(), ref, absref, "bf16", "back to back W4A16")
