@@ -381,9 +381,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         bool chunk_start = true;
         const int nkb = u.kb1 - u.kb0;
-        auto chunk_end_at = [&](int j) {
-          return (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
-        };
+        // stages of the current exact chunk (W4A8) or of the unit still to go
+        const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
+        int left = 0;
         auto advance = [&]() {
           if (++s == static_cast<uint32_t>(S)) {
             s = 0;
@@ -395,12 +395,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         };
         for (int j = 0; j < nkb;) {
-          if (chunk_start && ev > 0) {
-            if (!mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) { ok = false; break; }
+          if (chunk_start) {
+            if (ev > 0 && !mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) {
+              ok = false;
+              break;
+            }
+            left = chunk_len < nkb - j ? chunk_len : nkb - j;
           }
           // One-block stages go to the tensor pipe two at a time (eight MMAs
           // per group) when both belong to the same exact chunk.
-          const bool pair = NS == 1 && NT == 1 && TS >= 2 && !chunk_end_at(j);
+          const bool pair = NS == 1 && NT == 1 && TS >= 2 && left >= 2;
           // The converter group arrives on tfull only after it observed the
           // stage's full barrier, so tfull also orders the activation tile.
           if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
@@ -457,15 +461,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (pair) {
             mma_commit(&sm.empty[s2]);
             advance();
-            ++j;
           }
+          const int used = pair ? 2 : 1;
+          j += used;
+          left -= used;
           chunk_start = false;
-          if (chunk_end_at(j)) {
+          if (left == 0) {
             mma_commit(sm.dfull);
             ++ev;
             chunk_start = true;
           }
-          ++j;
         }
       }
       // All issued MMAs complete before tensor memory is released.
@@ -482,6 +487,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int nblk = BM / 8;           // 8-column blocks of the accumulator
     uint32_t it = 0, ev = 0;
+    // stage counters kept incrementally (no division in the loop): it % S and
+    // its phase, it % TS, and (it - TS) % S and its phase once it >= TS
+    uint32_t cs = 0, cph = 0, cts = 0, ps = 0, pph = 0;
+    auto adv = [&]() {
+      if (++cs == static_cast<uint32_t>(S)) {
+        cs = 0;
+        cph ^= 1;
+      }
+      if (++cts == static_cast<uint32_t>(TS)) cts = 0;
+      if (it > static_cast<uint32_t>(TS) && ++ps == static_cast<uint32_t>(S)) {
+        ps = 0;
+        pph ^= 1;
+      }
+    };
     bool ok = true;
     Unit u;
     for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
@@ -490,19 +509,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int64_t n0 = static_cast<int64_t>(nt) * NT * kTileN;  // first weight column
       const int64_t m0 = static_cast<int64_t>(mt) * BM;
       const int nkb = u.kb1 - u.kb0;
+      const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
+      int cleft = 0;  // stages left in the current exact chunk
       bool first_chunk = true;
-      for (int j = 0; j < nkb; ++j, ++it) {
+      for (int j = 0; j < nkb; ++j, ++it, adv()) {
+        if (cleft == 0) cleft = chunk_len < nkb - j ? chunk_len : nkb - j;
         if (static_cast<int>(it % kConvGroups) == grp) {
-          const uint32_t s = it % S, ts = it % TS;
-          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], (it / S) & 1, abort, args.status))) {
+          const uint32_t s = cs, ts = cts;
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], cph, abort, args.status))) {
             ok = false;
             break;
           }
           if (it >= static_cast<uint32_t>(TS)) {
             // the tensor-memory slot is free once the MMA of stage it-TS retired
-            const uint32_t pit = it - TS;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(&sm.empty[pit % S], (pit / S) & 1, abort, args.status))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.empty[ps], pph, abort, args.status))) {
               ok = false;
               break;
             }
@@ -560,8 +580,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(&sm.empty[s]);
           }
         }
-        const bool chunk_end =
-            (j == nkb - 1) || (MODE == kW4A8 && ((j + 1) % p.chunk_stages) == 0);
+        const bool chunk_end = --cleft == 0;
         if (!chunk_end) continue;
         // ------------------------------------------------ drain an event
         if (!__all_sync(0xffffffffu, mbar_wait(sm.dfull, ev & 1, abort, args.status))) {
