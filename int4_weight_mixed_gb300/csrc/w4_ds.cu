@@ -309,18 +309,21 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
     if (lane == 0) {
       const bool wprod = warp == kDsWProd;
       if (!wprod) asm volatile("griddepcontrol.wait;" ::: "memory");  // ds_prep is complete
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;  // stage count, it % S, (it / S) & 1
       bool ok = true;
       DsUnit u;
+      // K blocks per scale group (one division per unit below, none per block)
+      const int bpg = pc ? 1 : static_cast<int>(args.group_size / kBlkK);
       for (int ui = 0; ok && ds_unit(p, ui, u); ++ui) {
         const int64_t n0 = static_cast<int64_t>(u.tile) * kTileN;
         const uint32_t ncol = static_cast<uint32_t>(N - n0 < kTileN ? N - n0 : kTileN);
         const uint32_t scb = (!pc && args.scales) ? ncol * esz : 0;
         const uint32_t zpb = (!pc && args.zeros) ? ncol * esz : 0;
         const uint8_t* wtile = args.b_packed + static_cast<int64_t>(u.tile) * chunks * (kTileN * 16);
+        int64_t gcur = u.kb0 / bpg;          // scale group of the next block
+        int gleft = bpg - u.kb0 % bpg;       // blocks left in it
         for (int kb = u.kb0; kb < u.kb1; kb += SB, ++it) {
-          const uint32_t s = it % S;
-          if (!mbar_wait(&empty[s], ((it / S) & 1) ^ 1, abort, args.status)) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort, args.status)) {
             ok = false;
             break;
           }
@@ -333,7 +336,11 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
             mbar_arrive_expect_tx(&full[s], wb + nb * (scb + zpb));
             bulk_g2s_a(st + L.w, wtile + static_cast<int64_t>(kb) * kWBlk, wb, bar);
             for (int b = 0; b < nb && (scb || zpb); ++b) {
-              const int64_t g = (static_cast<int64_t>(kb + b) * kBlkK) / args.group_size;
+              const int64_t g = gcur;
+              if (--gleft == 0) {
+                ++gcur;
+                gleft = bpg;
+              }
               if (scb)
                 bulk_g2s_a(st + L.c + b * 256,
                            static_cast<const uint8_t*>(args.scales) + (g * N + n0) * esz, scb, bar);
@@ -344,6 +351,10 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
           } else {
             mbar_arrive_expect_tx(&full[s], nb * ablk);
             bulk_g2s_a(st + L.a, prep + static_cast<int64_t>(kb) * ablk, nb * ablk, bar);
+          }
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1;
           }
         }
       }
@@ -407,7 +418,7 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
     }
   };
 
-  uint32_t it = 0;
+  uint32_t it = 0, cs = 0, cph = 0;  // stage count, it % S, (it / S) & 1
   bool ok = true;
   DsUnit u;
   for (int ui = 0; ok && ds_unit(p, ui, u); ++ui) {
@@ -453,11 +464,17 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
         }
       }
     }
+    // blocks to go before the next fold (scale groups are aligned to K = 0)
+    int fleft = pc ? fold_blocks : fold_blocks - u.kb0 % fold_blocks;
     for (int kb = u.kb0; kb < u.kb1; kb += kDsSB, ++it) {
-      const uint32_t s = it % S;
-      if (!mbar_wait(&full[s], (it / S) & 1, abort, args.status)) {
+      const uint32_t s = cs;
+      if (!mbar_wait(&full[s], cph, abort, args.status)) {
         ok = false;
         break;
+      }
+      if (++cs == static_cast<uint32_t>(S)) {
+        cs = 0;
+        cph ^= 1;
       }
       const uint32_t st = sbase + s * L.stage;
       const uint8_t* stp = smem + static_cast<size_t>(s) * L.stage;
@@ -542,7 +559,8 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
           }
         }
         // fold at the end of a scale group / exact run, and of the segment
-        if (kbb + 1 == u.kb1 || (kbb + 1) % fold_blocks == 0) {
+        if (--fleft == 0) fleft = fold_blocks;
+        if (kbb + 1 == u.kb1 || fleft == fold_blocks) {
 #pragma unroll
           for (int j = 0; j < NJ; ++j)
 #pragma unroll
