@@ -296,6 +296,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int64_t M = args.M, N = args.N, K = args.K;
   const int gsz = static_cast<int>(args.group_size);
   const int sub_per_group = gsz / kStageK;  // 64-K blocks per scale group
+  // A stage lies inside one scale group (sub_per_group >= NS) or covers whole
+  // groups of 1 or 2 blocks (the plan guarantees one or the other): the group
+  // of block qq of a stage is the stage's first group + (qq >> grow_shift).
+  const bool stage_in_group = sub_per_group >= NS;
+  const int grow_shift = sub_per_group >= 2 ? 1 : 0;
   const int esz = MODE == kW4A8 ? 1 : 2;
 
   if (warp == 0 || warp == kActWarp) {
@@ -329,6 +334,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ((static_cast<int64_t>(nt) * NT * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * 2) *
              kTileN) * 16;
         const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
+        // scale group of the stage, kept without division per stage
+        int gcur = u.kb0 * NS / sub_per_group;
+        int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           if (!mbar_wait(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
           const int k64_0 = kb * NS;
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int t = 0; t < ntv; ++t)
               bulk_g2s_a(w0 + (s * NT + t) * NS * 4096, wsrc + t * tile_stride, nv * 4096, fb);
             if (sc_bytes || zp_bytes) {
-              const int g0 = k64_0 / sub_per_group;
+              const int g0 = gcur;
               for (int t = 0; t < NT; ++t) {
                 if (sc_bytes)
                   tma_load_2d_a(s0 + (s * NT + t) * NS * 256, &smap, n0 + t * kTileN, g0, fb);
@@ -355,6 +363,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive_expect_tx_a(fb, nv * a_sub);
             for (int j = 0; j < nv; ++j)
               tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * kStageK, y, fb);
+          }
+          if (stage_in_group) {
+            gleft -= NS;
+            if (gleft == 0) {
+              ++gcur;
+              gleft = sub_per_group;
+            }
+          } else {
+            gcur += p.gps;
           }
           if (++s == static_cast<uint32_t>(S)) {
             s = 0;
@@ -512,7 +529,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
       int cleft = 0;  // stages left in the current exact chunk
       bool first_chunk = true;
-      for (int j = 0; j < nkb; ++j, ++it, adv()) {
+      int gcur = u.kb0 * NS / sub_per_group;  // scale group of stage j
+      int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
+      auto gadv = [&]() {
+        if (stage_in_group) {
+          gleft -= NS;
+          if (gleft == 0) {
+            ++gcur;
+            gleft = sub_per_group;
+          }
+        } else {
+          gcur += p.gps;
+        }
+      };
+      for (int j = 0; j < nkb; ++j, ++it, adv(), gadv()) {
         if (cleft == 0) cleft = chunk_len < nkb - j ? chunk_len : nkb - j;
         if (static_cast<int>(it % kConvGroups) == grp) {
           const uint32_t s = cs, ts = cts;
@@ -530,7 +560,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           const int k64_0 = (u.kb0 + j) * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
-          const int g0 = k64_0 / sub_per_group;
           for (int t = 0; t < NT; ++t) {
             const size_t st_idx = static_cast<size_t>(s) * NT + t;
             const uint8_t* wst = sm.w + st_idx * NS * 4096;
@@ -541,7 +570,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int qq = 0; qq < nv; ++qq) {
               const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
               const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
-              const int grow = (k64_0 + qq) / sub_per_group - g0;
+              const int grow = stage_in_group ? 0 : qq >> grow_shift;
               uint32_t s2 = 0, nz2 = 0;
               bool has_s = true;
               if (MODE == kW4A8) {
