@@ -128,7 +128,8 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
  *          multiplied left to right in fp32, with a_token_scales = s_tok [M]
  *          and ch_scales = s_ch [N] (fp32, device).
  *          out_type W4_S32: out = acc, both scale pointers NULL.
- *   workspace  device buffer of at least w4_gemm_workspace_size(...) bytes.
+ *   workspace  device buffer of at least w4_gemm_workspace_size(...) bytes,
+ *             16-byte aligned (W4_ERR_WORKSPACE otherwise).
  *
  * M == 0 is a no-op; K == 0 writes zeros.  Errors: INVALID_ARGUMENT
  * (null required pointer, dtype mismatch, K % 8 != 0, group_size not

@@ -489,6 +489,7 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
     si = 0;
   }
   if (!workspace) return fail(W4_ERR_WORKSPACE, "workspace is null");
+  if (!aligned16(workspace)) return fail(W4_ERR_WORKSPACE, "workspace is not 16-byte aligned");
   const size_t need = ws_needed(si, pr);
   if (workspace_bytes < need)
     return fail(W4_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, need);

@@ -84,6 +84,48 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait until the high half of a global counter (bits 16..31) reaches
+// `target`, reading it with acquire semantics at device scope; bounded like
+// mbar_wait.
+__device__ __forceinline__ bool wait_count_hi(const int* ctr, int target, volatile int* abort,
+                                              int* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if ((v >> 16) >= target) return true;
+    if (it == 0) {
+      t0 = global_timer_ns();
+    } else if ((it & 15u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > W4_WAIT_TIMEOUT_NS) {
+        *abort = 1;
+        if (status) atomicExch(status, 5 /* W4_ERR_TIMEOUT */);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
+// ------------------------------------------------------- global accesses
+// 32 contiguous bytes (16-byte aligned) loaded at L2 (bypassing L1, which
+// does not see other SMs' writes) or stored.
+__device__ __forceinline__ void ld_cg_v8(const void* p, uint32_t (&v)[8]) {
+  const uint4* q = static_cast<const uint4*>(p);
+  const uint4 a = __ldcg(q), b = __ldcg(q + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
+  uint4* q = static_cast<uint4*>(p);
+  q[0] = make_uint4(v[0], v[1], v[2], v[3]);
+  q[1] = make_uint4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------- bulk copies
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes must be
 // a multiple of 16, both addresses 16-byte aligned).

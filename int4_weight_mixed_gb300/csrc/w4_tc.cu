@@ -612,81 +612,151 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool chunk_end = --cleft == 0;
         if (!chunk_end) continue;
         // ------------------------------------------------ drain an event
+        const bool final_ev = (j == nkb - 1);
+        const bool split = final_ev && u.nslots > 1;
+        const size_t slot_elems = static_cast<size_t>(NT) * kTileN * BM;
+        const uint32_t* part = reinterpret_cast<const uint32_t*>(args.partials);
+        // Split tile: each warp takes its place in the arrival order of the
+        // tile's contributors for its sub-tile (low half of the counter).
+        // The last to arrive adds the others' partial sums to its own
+        // accumulator; the others write theirs and then count themselves as
+        // written (high half), which the last one waits for.
+        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + cw;
+        bool reducer = false;
+        if (split) {
+          int prev_count = 0;
+          if (lane == 0) prev_count = atomicAdd(ctr, 1);
+          prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
+          reducer = (prev_count & 0xffff) == u.nslots - 1;
+        }
+        // position of this unit among the tile's contributors (K order), and
+        // the slot of contributor sl held by lane sl (<= 32 contributors)
+        const int my_sl = p.decomp == kSplitK ? u.split : static_cast<int>(blockIdx.x) - u.cfirst;
+        const size_t lane_slot =
+            reducer && lane < u.nslots ? slot_index(p, wk, u, lane) * slot_elems : 0;
+        // Pull what this drain will read toward L2 while the last MMAs run:
+        // the other contributors' partial sums (reducer) and the int32
+        // running sum of the earlier chunks (W4A8 with the global copy).
+        int32_t* gi_base = args.icopy + static_cast<size_t>(blockIdx.x) * NT * BM * kTileN;
+        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+          if (MODE == kW4A8 && p.gicopy && !first_chunk) prefetch_l2(gi_base + coff);
+          if (reducer) {
+            for (int sl = 0; sl < u.nslots; ++sl) {
+              if (sl == my_sl) continue;
+              const size_t sbase =
+                  u.nslots <= 32
+                      ? static_cast<size_t>(__shfl_sync(
+                            0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
+                      : slot_index(p, wk, u, sl) * slot_elems;
+              prefetch_l2(part + sbase + coff);
+            }
+          }
+        }
         if (!__all_sync(0xffffffffu, mbar_wait(sm.dfull, ev & 1, abort, args.status))) {
           ok = false;
           break;
         }
         ++ev;
         tc_fence_after();
-        const bool final_ev = (j == nkb - 1);
-        float* partf = static_cast<float*>(args.partials);
-        int32_t* parti = static_cast<int32_t*>(args.partials);
-        const size_t slot_elems = static_cast<size_t>(NT) * kTileN * BM;
-        const size_t my_slot = own_slot(p, u) * slot_elems;
-        // blocks of 8 accumulator columns over all weight tiles, round-robin
-        // over the converter groups
+        if (reducer) {
+          // every other contributor has written its partial sums
+          bool done = true;
+          if (lane == 0) done = wait_count_hi(ctr, u.nslots - 1, abort, args.status);
+          if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, done, 0))) {
+            ok = false;
+            break;
+          }
+          __threadfence();
+        }
+        const size_t my_slot = split && !reducer ? own_slot(p, u) * slot_elems : 0;
+        // Blocks of 8 accumulator columns over all weight tiles, round-robin
+        // over the converter groups.  Global layout of partial sums and of
+        // the int32 running sum: block (t, cc) is 128 rows x 8 columns, row r
+        // holding its 8 columns contiguously.
         for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
           const int t = bb / nblk, cc = (bb - t * nblk) * 8;
           const uint32_t dcol = tmem + lane_base + t * BM + cc;
           const int64_t nrow = n0 + t * kTileN + r;  // output column
+          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
           uint32_t d[8];
           tmem_ld8(dcol, d);
-          tmem_wait_ld();
-          int32_t iv[8];
           if (MODE == kW4A8) {
-            // int32 running sum of the earlier chunks of this unit: in tensor
-            // memory, or in this CTA's global scratch (element (column, row))
+            // add the int32 running sum of the earlier chunks of this unit:
+            // in tensor memory, or in this CTA's global scratch
             const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
-            int32_t* gi = args.icopy +
-                          (static_cast<size_t>(blockIdx.x) * NT * BM + t * BM + cc) * kTileN + r;
+            int32_t* gi = gi_base + coff;
             uint32_t prev[8];
             if (!first_chunk) {
-              if (p.gicopy) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) prev[i] = static_cast<uint32_t>(gi[i * kTileN]);
-              } else {
-                tmem_ld8(icol, prev);
-                tmem_wait_ld();
-              }
+              if (p.gicopy) ld_cg_v8(gi, prev);
+              else tmem_ld8(icol, prev);
             }
+            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              iv[i] = __float2int_rn(__uint_as_float(d[i])) +
-                      (first_chunk ? 0 : static_cast<int32_t>(prev[i]));
+              d[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(d[i])) +
+                                           (first_chunk ? 0 : static_cast<int32_t>(prev[i])));
             if (!final_ev) {
               if (p.gicopy) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) gi[i * kTileN] = iv[i];
+                st_v8(gi, d);
               } else {
-                uint32_t st[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) st[i] = static_cast<uint32_t>(iv[i]);
-                tmem_st8(icol, st);
+                tmem_st8(icol, d);
                 tmem_wait_st();
               }
               continue;
             }
+          } else {
+            tmem_wait_ld();
           }
-          // final event: outputs or partials
+          // d: this unit's sums of the block (int32 or fp32 bits)
+          if (split && !reducer) {
+            st_v8(static_cast<uint32_t*>(args.partials) + my_slot + coff, d);
+            continue;
+          }
+          if (reducer) {
+            // add the contributors in K order, this unit's own sums at its place
+            uint32_t acc[8];
+            for (int sl = 0; sl < u.nslots; ++sl) {
+              uint32_t x[8];
+              if (sl == my_sl) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = d[i];
+              } else {
+                const size_t sbase =
+                    u.nslots <= 32
+                        ? static_cast<size_t>(__shfl_sync(
+                              0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
+                        : slot_index(p, wk, u, sl) * slot_elems;
+                ld_cg_v8(part + sbase + coff, x);
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (sl == 0) acc[i] = x[i];
+                else if (MODE == kW4A8)
+                  acc[i] = static_cast<uint32_t>(static_cast<int32_t>(acc[i]) +
+                                                 static_cast<int32_t>(x[i]));
+                else
+                  acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __uint_as_float(x[i]));
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = acc[i];
+          }
+          // outputs
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int col = cc + i;
-            if (u.nslots > 1) {
-              const size_t off = my_slot + static_cast<size_t>(t * BM + col) * kTileN + r;
-              if (MODE == kW4A8) parti[off] = iv[i];
-              else partf[off] = __uint_as_float(d[i]);
-            } else {
-              const int64_t m = m0 + col;
-              if (nrow < N && m < M) {
-                const int64_t o = m * N + nrow;
-                if (MODE == kW4A8) {
-                  if (args.out_s32) static_cast<int32_t*>(args.out)[o] = iv[i];
-                  else
-                    static_cast<__half*>(args.out)[o] = __float2half_rn(
-                        static_cast<float>(iv[i]) * args.s_tok[m] * args.s_ch[nrow]);
-                } else {
-                  static_cast<T16*>(args.out)[o] = to_t16<T16>(__uint_as_float(d[i]));
-                }
+            const int64_t m = m0 + cc + i;
+            if (nrow < N && m < M) {
+              const int64_t o = m * N + nrow;
+              if (MODE == kW4A8) {
+                const int32_t acc = static_cast<int32_t>(d[i]);
+                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acc;
+                else
+                  static_cast<__half*>(args.out)[o] = __float2half_rn(
+                      static_cast<float>(acc) * args.s_tok[m] * args.s_ch[nrow]);
+              } else {
+                static_cast<T16*>(args.out)[o] = to_t16<T16>(__uint_as_float(d[i]));
               }
             }
           }
@@ -695,77 +765,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.dempty);
         first_chunk = false;
-        if (!final_ev || u.nslots == 1) continue;
-
-        // ------------------- split-K fix-up, per (lane quadrant, group) sub-tile
-        __threadfence();
-        __syncwarp();
-        int prev_count = 0;
-        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + cw;
-        if (lane == 0) prev_count = atomicAdd(ctr, 1);
-        prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
-        if (prev_count != u.nslots - 1) continue;
-        __threadfence();
-        // slot of contributor sl, computed once: lane sl holds it (broadcast
-        // by shuffle) when there are at most 32 contributors
-        const size_t lane_slot =
-            lane < u.nslots ? slot_index(p, wk, u, lane) * slot_elems : 0;
-        // one 8-column block at a time; the loads of two slots x eight
-        // columns are in flight together, and the slots are added in K order
-        const uint32_t* part = reinterpret_cast<const uint32_t*>(args.partials);
-        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
-          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
-          const int64_t nrow = n0 + t * kTileN + r;
-          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r;
-          float accf[8];
-          int32_t acci[8];
-          constexpr int kBatch = 2;
-          for (int s0 = 0; s0 < u.nslots; s0 += kBatch) {
-            uint32_t x[kBatch][8];
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-              const int sl = s0 + q;
-              if (sl >= u.nslots) break;
-              const size_t sbase =
-                  u.nslots <= 32
-                      ? static_cast<size_t>(__shfl_sync(0xffffffffu,
-                                                        static_cast<unsigned long long>(lane_slot), sl))
-                      : slot_index(p, wk, u, sl) * slot_elems;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) x[q][i] = __ldcg(part + sbase + coff + i * kTileN);
-            }
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-              const int sl = s0 + q;
-              if (sl >= u.nslots) break;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (MODE == kW4A8) {
-                  acci[i] = sl == 0 ? static_cast<int32_t>(x[q][i])
-                                    : acci[i] + static_cast<int32_t>(x[q][i]);
-                } else {
-                  accf[i] = sl == 0 ? __uint_as_float(x[q][i]) : accf[i] + __uint_as_float(x[q][i]);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int64_t m = m0 + cc + i;
-            if (nrow < N && m < M) {
-              const int64_t o = m * N + nrow;
-              if (MODE == kW4A8) {
-                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acci[i];
-                else
-                  static_cast<__half*>(args.out)[o] = __float2half_rn(
-                      static_cast<float>(acci[i]) * args.s_tok[m] * args.s_ch[nrow]);
-              } else {
-                static_cast<T16*>(args.out)[o] = to_t16<T16>(accf[i]);
-              }
-            }
-          }
+        if (split && !reducer) {
+          // partial sums visible device-wide, then counted as written
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(ctr, 0x10000);
+        } else if (reducer) {
+          if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
         }
-        if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
       }
     }
   }

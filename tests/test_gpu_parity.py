@@ -347,6 +347,38 @@ def test_deterministic_stream_k(gpu_lib):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name", ["tc16_sk", "tc32_sk"])
+def test_stream_k_many_contributors(gpu_lib, name):
+    """One weight tile over a long K: stream-K spreads its stages over more
+    than 32 CTAs, so the tile's last arriving warp adds over 32 other partial
+    sums (the slot of each computed in turn rather than held by a lane)."""
+    w4 = gpu_lib
+    N, K = 128, 32768
+    e = w4synth.gen_w4a8(8, N, K, group_size=-1, seed=31)
+    got = run_w4a8(w4, e, torch.int32, schedule=sched(w4, name))
+    ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], e["group_size"], K, N)
+    assert np.array_equal(got.numpy().astype(np.int64), ref)
+    d = w4synth.gen_w4a16(8, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4, group_size=128,
+                          zeros=True, seed=32)
+    o1 = run_w4a16(w4, d, schedule=sched(w4, name))
+    o2 = run_w4a16(w4, d, schedule=sched(w4, name))
+    assert torch.equal(o1, o2)  # partial sums are added in K order
+    ref, absref = oracle_w4a16(d)
+    assert_within(o1.double().numpy(), ref, absref, "bf16", f"{name} many contributors")
+
+
+def test_misaligned_workspace_rejected(gpu_lib):
+    w4 = gpu_lib
+    d = w4synth.tiny_w4a16(seed=2)
+    b = w4.prepack_B(d["w"].to(DEV), d["wtype"], d["layout"], d["K"], d["N"])
+    nbytes = w4.workspace_size(d["M"], d["N"], d["K"], d["a"].dtype, d["group_size"])
+    ws = torch.zeros(nbytes + 16, dtype=torch.uint8, device=DEV)[8:]
+    with pytest.raises(w4.W4Error) as ei:
+        w4.gemm(d["a"].to(DEV), b, d["wtype"], d["N"], scales=d["s"].to(DEV),
+                group_size=d["group_size"], ws=ws)
+    assert ei.value.status == w4.ERR_WORKSPACE
+
+
 def test_check_status_clean(gpu_lib):
     w4 = gpu_lib
     d = w4synth.tiny_w4a16(seed=1)
