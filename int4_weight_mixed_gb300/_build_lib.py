@@ -1,6 +1,6 @@
 """Build libw4.so in-tree with nvcc for sm_103a (no cmake, no torch extension).
 
-The three translation units compile in parallel; the shared library lands in
+The translation units compile in parallel; the shared library lands in
 int4_weight_mixed_gb300/_build/libw4.so.
 """
 from __future__ import annotations
@@ -13,8 +13,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libw4.so")
-SOURCES = ["w4_api.cu", "w4_kernels.cu", "w4_tc.cu", "w4_dk.cu", "w4_noalloc.cu", "w4_ds.cu"]
-HEADERS = ["w4_internal.h", "w4_ptx.cuh", os.path.join("..", "..", "include", "w4.h")]
+SOURCES = ["w4_api.cu", "w4_kernels.cu", "w4_tc.cu", "w4_tc2.cu", "w4_dk.cu", "w4_noalloc.cu",
+           "w4_ds.cu"]
+HEADERS = ["w4_internal.h", "w4_ptx.cuh", "w4_tc_kernel.cuh", os.path.join("..", "..", "include", "w4.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

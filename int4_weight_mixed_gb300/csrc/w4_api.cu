@@ -613,11 +613,12 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   if (debug)
     fprintf(stderr,
             "w4: %s M=%lld N=%lld K=%lld bm=%d nt=%d nsub=%d stages=%d tstages=%d icol=%d gi=%d "
-            "acol=%d gps=%d a3d=%d tiles=%d kb=%d grid=%d decomp=%d ksplit=%d segs=%d smem=%zu\n",
+            "acol=%d gps=%d a3d=%d mma2=%d tiles=%d kb=%d grid=%d decomp=%d ksplit=%d segs=%d "
+            "smem=%zu\n",
             kSchedules[si].name, (long long)M, (long long)N, (long long)K, plan.bm, plan.nt,
             plan.nsub, plan.stages, plan.tstages, plan.icol, plan.gicopy, plan.acol, plan.gps, plan.a3d,
-            plan.tiles, plan.kb_total, plan.grid, plan.decomp, plan.ksplit, plan.max_segs,
-            plan.smem_bytes);
+            tc_mma2(plan) ? 1 : 0, plan.tiles, plan.kb_total, plan.grid, plan.decomp, plan.ksplit,
+            plan.max_segs, plan.smem_bytes);
   cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
 }

@@ -25,9 +25,12 @@ constexpr int kMaxTmemStages = 8;
 constexpr int kConvGroups = 4;
 constexpr int kConvWarps = 4 * kConvGroups;
 // warp 0: weight producer + tensor-memory allocation; warp 1: MMA issue;
-// warps 2..kConvWarps+1: converters / epilogue; last warp: activation producer
-constexpr int kTcThreads = 64 + 32 * kConvWarps + 32;
-constexpr int kActWarp = kTcThreads / 32 - 1;
+// warps 2..kConvWarps+1: converters / epilogue; then the activation producer
+// and the second MMA-issuing warp (the two issuers alternate by MMA group)
+constexpr int kTcThreads = 64 + 32 * kConvWarps + 64;  // with the second MMA warp
+// (a kernel without it launches kTcThreads - 32 threads)
+constexpr int kActWarp = kTcThreads / 32 - 2;
+constexpr int kMma2Warp = kTcThreads / 32 - 1;
 constexpr size_t kWsHeader = 256;                // status word + spare
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
@@ -72,6 +75,10 @@ struct TcPlan {
   size_t ws_icopy;     // W4A8 int32 running sums (gicopy): grid x NT*BM*128 x 4 bytes
   size_t ws_total;
 };
+
+// MMA groups issued by two alternating threads (else one): where a group's
+// MMAs are short (N <= 128 activation rows)
+inline bool tc_mma2(const TcPlan& p) { return p.bm <= 128; }
 
 struct TcArgs {
   const uint8_t* b_packed;

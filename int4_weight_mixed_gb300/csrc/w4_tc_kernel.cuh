@@ -1,0 +1,960 @@
+#pragma once
+// w4_tc_kernel.cuh — the tensor-core schedule of the 4-bit-weight GEMM for
+// sm_103a: kernel template and its launcher, included by w4_tc.cu (one MMA
+// issuer) and w4_tc2.cu (two alternating issuers), so that each kernel
+// variant is compiled in a translation unit of its own.
+//
+// Orientation: the weight tile is the 128-row UMMA "A" operand and the
+// activations are the UMMA "B" operand, so each CTA computes
+//   D[n, m] = sum_k w_hat[k, n] * a[m, k]      (n: 128 weight columns,
+//                                               m: BM activation rows)
+// which is the transposed statement of out = a x w_hat (the Machete Readme,
+// "Overview", writes the weight on the left of "@ a").
+//
+// Data flow per pipeline stage (nsub = 1, 2 or 4 blocks of 64 K; the
+// stage is sized so that every stage moves >= 8 KB of nibbles for skinny
+// tiles, because each stage costs the single producer thread a few hundred
+// cycles whatever its size):
+//   producer warp : nsub TMA tiles of the activations (128B-swizzled,
+//                   K-major) + one bulk copy of the stage's prepacked nibbles
+//                   + one TMA box each of scale / zero-point rows
+//   8 converter warps : nibbles -> 16-bit weights in registers, one fused
+//                   multiply-add per pair with the scale and pre-scaled
+//                   zero-point (Machete Readme "Overview" NOTE), stored
+//                   straight into tensor memory (tcgen05.st): dequantized
+//                   weights never touch shared memory
+//   MMA thread    : 4 * nsub tcgen05.mma (K = 16) with A from tensor memory
+//                   and B from shared memory, fp32 accumulator in tensor
+//                   memory; one commit per stage releases the stage
+//   epilogue      : converter warps drain the accumulator (tcgen05.ld),
+//                   convert / scale and store, or write split-K partials and
+//                   let the last arriving warp of each sub-tile reduce them.
+//
+// W4A8 (pytorch/ao PR #1113 "support W4A8 Marlin kernel") runs on the same
+// bf16 tensor cores: int8 activations and int4 (x int8 group scale)
+// weights are exact in bf16, their products are exact in fp32, and the
+// accumulator is drained into an int32 copy in tensor memory before any
+// partial sum can exceed 2^24, so the int32 result is exact.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "w4_internal.h"
+#include "w4_ptx.cuh"
+
+namespace w4 {
+
+namespace {
+
+struct Unit {
+  int tile;
+  int kb0, kb1;
+  int nslots;   // units contributing to this tile
+  int cfirst;   // first contributing CTA (stream-K)
+  int seg;      // index of this tile among the CTA's segments (stream-K)
+  int split;    // K split of this unit (split-K)
+};
+
+struct Work {
+  int64_t T, G, kb;
+  int64_t begin, end;  // stream-K range of this CTA
+  int64_t first_tile;
+};
+
+__device__ __forceinline__ int64_t sk_start(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+
+// Stream-K: the CTA that owns linear iteration i.
+__device__ __forceinline__ int64_t sk_owner(int64_t i, int64_t T, int64_t G) {
+  return ((i + 1) * G - 1) / T;
+}
+
+// u-th unit of this CTA; false when there is none.
+__device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
+  if (p.decomp == kSplitK) {
+    // units (tile, split), c, c+G, ...: split j covers stages
+    // [j*kb/ks, (j+1)*kb/ks) of its tile
+    const int64_t v = blockIdx.x + static_cast<int64_t>(u) * p.grid;
+    if (v >= static_cast<int64_t>(p.tiles) * p.ksplit) return false;
+    const int t = static_cast<int>(v / p.ksplit), j = static_cast<int>(v % p.ksplit);
+    out.tile = t;
+    out.split = j;
+    out.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kb_total / p.ksplit);
+    out.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kb_total / p.ksplit);
+    out.nslots = p.ksplit;
+    out.cfirst = 0;
+    out.seg = 0;
+    return true;
+  }
+  if (p.decomp == kDataParallel) {
+    int64_t t = blockIdx.x + static_cast<int64_t>(u) * p.grid;
+    if (t >= p.tiles) return false;
+    out.tile = static_cast<int>(t);
+    out.kb0 = 0;
+    out.kb1 = p.kb_total;
+    out.nslots = 1;
+    out.cfirst = blockIdx.x;
+    out.seg = 0;
+    out.split = 0;
+    return true;
+  }
+  int64_t t = w.first_tile + u;
+  int64_t lo = t * w.kb, hi = lo + w.kb;
+  if (lo < w.begin) lo = w.begin;
+  if (hi > w.end) hi = w.end;
+  if (lo >= hi) return false;
+  out.tile = static_cast<int>(t);
+  out.kb0 = static_cast<int>(lo - t * w.kb);
+  out.kb1 = static_cast<int>(hi - t * w.kb);
+  int64_t cf = sk_owner(t * w.kb, w.T, w.G);
+  int64_t cl = sk_owner((t + 1) * w.kb - 1, w.T, w.G);
+  out.cfirst = static_cast<int>(cf);
+  out.nslots = static_cast<int>(cl - cf + 1);
+  out.seg = u;
+  out.split = 0;
+  return true;
+}
+
+// Partial-sum slot of contributor sl (0-based, in K order) of the unit's tile.
+__device__ __forceinline__ size_t slot_index(const TcPlan& p, const Work& w, const Unit& u,
+                                             int sl) {
+  if (p.decomp == kSplitK) return static_cast<size_t>(u.tile) * p.ksplit + sl;
+  const int64_t cpr = u.cfirst + sl;
+  const int64_t seg = u.tile - sk_start(cpr, w.T, w.G) / w.kb;
+  return static_cast<size_t>(cpr) * p.max_segs + seg;
+}
+__device__ __forceinline__ size_t own_slot(const TcPlan& p, const Unit& u) {
+  if (p.decomp == kSplitK) return static_cast<size_t>(u.tile) * p.ksplit + u.split;
+  return static_cast<size_t>(blockIdx.x) * p.max_segs + u.seg;
+}
+
+// Tile -> (m_tile, n_tile), grouped raster: runs of up to 8 m-tiles share
+// each weight tile while it is in L2.
+__device__ __forceinline__ void tile_coords(const TcPlan& p, int t, int& mt, int& nt) {
+  int gm_full = p.m_tiles < 8 ? p.m_tiles : 8;
+  int group = t / (gm_full * p.n_tiles);
+  int local = t - group * gm_full * p.n_tiles;
+  int gm = p.m_tiles - group * gm_full;
+  if (gm > gm_full) gm = gm_full;
+  mt = group * gm_full + local % gm;
+  nt = local / gm;
+}
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+template <typename T2>
+__device__ __forceinline__ T2 as_t2(uint32_t x) {
+  return *reinterpret_cast<T2*>(&x);
+}
+template <typename T2>
+__device__ __forceinline__ uint32_t as_u32(T2 x) {
+  return *reinterpret_cast<uint32_t*>(&x);
+}
+
+// Dequantize the 32 K-values of one 16-byte chunk (4 words, ExLlama order)
+// into 16 packed pairs.  Pair p of word x holds (k0+2p, k0+2p+1) at bits
+// (4p, 16+4p).  OR-ing a nibble into the mantissa of the "magic" constant
+// gives magic+q exactly; subtracting magic+bias is exact; the FMA with the
+// scale and negated zero-point rounds once.
+template <int MODE>
+__device__ __forceinline__ void convert_chunk(const uint4& wv, uint32_t s2u, uint32_t nz2u,
+                                              bool has_z, bool has_s, int wbias,
+                                              uint32_t (&v)[16]) {
+  const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+  if constexpr (MODE == kW4A16_F16) {
+    const __half2 off = __half2half2(__int2half_rn(1024 + wbias));
+    const __half2 s2 = as_t2<__half2>(s2u), nz2 = as_t2<__half2>(nz2u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        __half2 h = as_t2<__half2>(lop_and_or(wd[i] >> (4 * p), 0x000F000Fu, 0x64006400u));
+        __half2 q = __hsub2(h, off);
+        v[4 * i + p] = as_u32(has_z ? __hfma2(q, s2, nz2) : __hmul2(q, s2));
+      }
+  } else {
+    const __nv_bfloat162 off = __bfloat162bfloat162(__int2bfloat16_rn(128 + wbias));
+    const __nv_bfloat162 s2 = as_t2<__nv_bfloat162>(s2u), nz2 = as_t2<__nv_bfloat162>(nz2u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        __nv_bfloat162 h =
+            as_t2<__nv_bfloat162>(lop_and_or(wd[i] >> (4 * p), 0x000F000Fu, 0x43004300u));
+        __nv_bfloat162 q = __hsub2(h, off);
+        if constexpr (MODE == kW4A8) {
+          v[4 * i + p] = as_u32(has_s ? __hmul2(q, s2) : q);
+        } else {
+          v[4 * i + p] = as_u32(has_z ? __hfma2(q, s2, nz2) : __hmul2(q, s2));
+        }
+      }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T to_t16(float x);
+template <>
+__device__ __forceinline__ __half to_t16<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_t16<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+struct Smem {
+  uint8_t* a;       // stages x nsub x BM x 128 B  (128B-swizzled activation tiles)
+  uint8_t* w;       // stages x nsub x 4096 B      (prepacked nibbles)
+  uint8_t* s;       // stages x nsub x 256 B       (scale rows, up to nsub groups)
+  uint8_t* z;       // stages x nsub x 256 B       (zero-point rows)
+  uint64_t* full;   // [kMaxStages]  TMA bytes landed
+  uint64_t* empty;  // [kMaxStages]  stage consumed (converter group + MMA commit)
+  uint64_t* tfull;  // [kMaxTmemStages] converted weights stored in tensor memory
+  uint64_t* dfull;  // accumulator ready for the epilogue
+  uint64_t* dempty; // accumulator drained
+  uint64_t* fin;    // all MMAs retired (before tensor memory is freed)
+  uint64_t* tok;    // [2] MMA issuing turn of thread 0 / 1
+  uint32_t* tmem_slot;
+  int* abort;
+};
+
+}  // namespace
+
+// MMA2: two alternating MMA-issuing threads (one more warp); a separate
+// instantiation, so that the one-issuer kernel keeps its register budget.
+template <int MODE, bool MMA2>
+__global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                   const __grid_constant__ CUtensorMap smap,
+                   const __grid_constant__ CUtensorMap zmap, const TcPlan p, const TcArgs args) {
+  using T16 = typename std::conditional<MODE == kW4A16_F16, __half, __nv_bfloat16>::type;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages, NT = p.nt;
+  const uint32_t a_sub = static_cast<uint32_t>(BM) * 128;  // bytes of one 64-K activation tile
+  Smem sm;
+  sm.a = base;
+  sm.w = sm.a + static_cast<size_t>(S) * NS * a_sub;             // [S][NT][NS][4096]
+  sm.s = sm.w + static_cast<size_t>(S) * NT * NS * 4096;          // [S][NT][NS * 256]
+  sm.z = sm.s + static_cast<size_t>(S) * NT * NS * 256;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * NT * NS * 256);
+  sm.full = bars;
+  sm.empty = bars + kMaxStages;
+  sm.tfull = bars + 2 * kMaxStages;
+  sm.dfull = sm.tfull + kMaxTmemStages;
+  sm.dempty = sm.dfull + 1;
+  sm.fin = sm.dempty + 1;
+  sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.fin + 1);
+  sm.abort = reinterpret_cast<int*>(sm.tmem_slot + 1);
+  sm.tok = sm.fin + 2;  // after the slot and abort words (8-byte aligned)
+  volatile int* abort = sm.abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&sm.full[i], 2);  // weight producer + activation producer
+      mbar_init(&sm.empty[i], 4 + 1);  // one converter group + the MMA commit
+    }
+    for (int i = 0; i < TS; ++i) mbar_init(&sm.tfull[i], 4);
+    mbar_init(sm.dfull, 1);
+    mbar_init(sm.dempty, kConvWarps);
+    mbar_init(sm.fin, MMA2 ? 2 : 1);  // one commit per MMA issuing thread
+    if constexpr (MMA2) {
+      mbar_init(&sm.tok[0], 1);
+      mbar_init(&sm.tok[1], 1);
+    }
+    *sm.abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&amap);
+    if (args.scales) prefetch_tensormap(&smap);
+    if (args.zeros) prefetch_tensormap(&zmap);
+  }
+  if (warp == 0) {
+    tmem_alloc(sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_slot;
+
+  Work wk;
+  wk.kb = p.kb_total;
+  wk.T = static_cast<int64_t>(p.tiles) * p.kb_total;
+  wk.G = p.grid;
+  wk.begin = sk_start(blockIdx.x, wk.T, wk.G);
+  wk.end = sk_start(blockIdx.x + 1, wk.T, wk.G);
+  wk.first_tile = wk.begin / wk.kb;
+
+  const int64_t M = args.M, N = args.N, K = args.K;
+  const int gsz = static_cast<int>(args.group_size);
+  const int sub_per_group = gsz / kStageK;  // 64-K blocks per scale group
+  // A stage lies inside one scale group (sub_per_group >= NS) or covers whole
+  // groups of 1 or 2 blocks (the plan guarantees one or the other): the group
+  // of block qq of a stage is the stage's first group + (qq >> grow_shift).
+  const bool stage_in_group = sub_per_group >= NS;
+  const int grow_shift = sub_per_group >= 2 ? 1 : 0;
+  const int esz = MODE == kW4A8 ? 1 : 2;
+
+  if (warp == 0 || warp == kActWarp) {
+    // ----------------------------------------------------------- producers
+    // Two single-thread producers fill each stage in parallel, each with its
+    // own expect-tx on the stage's full barrier: warp 0 the bulk copy of the
+    // stage's nibbles and the scale / zero-point boxes, the last warp the
+    // activation tile(s).
+    if (lane == 0) {
+      const bool wprod = warp == 0;
+      // W4A8: the activations come from the staging grid this one may have
+      // been launched beside (programmatic dependent launch); wait for it
+      if (!wprod) asm volatile("griddepcontrol.wait;" ::: "memory");
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = true;
+      Unit u;
+      const uint32_t a0 = smem_addr(sm.a), w0 = smem_addr(sm.w);
+      const uint32_t s0 = smem_addr(sm.s), z0 = smem_addr(sm.z);
+      const uint32_t full0 = smem_addr(sm.full);
+      const uint32_t sc_bytes = args.scales ? static_cast<uint32_t>(128 * p.gps * esz) : 0;
+      const uint32_t zp_bytes = args.zeros ? static_cast<uint32_t>(128 * p.gps * 2) : 0;
+      for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+        int mt, nt;
+        tile_coords(p, u.tile, mt, nt);
+        const int32_t n0 = nt * NT * kTileN;       // first weight column of the CTA tile
+        const int32_t y = mt * BM;
+        int ntv = p.n128 - nt * NT;                 // weight tiles that exist (ragged N)
+        if (ntv > NT) ntv = NT;
+        const uint8_t* wsrc =
+            args.b_packed +
+            ((static_cast<int64_t>(nt) * NT * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * 2) *
+             kTileN) * 16;
+        const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
+        // scale group of the stage, kept without division per stage
+        int gcur = u.kb0 * NS / sub_per_group;
+        int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+          if (!mbar_wait(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
+          const int k64_0 = kb * NS;
+          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
+          const uint32_t fb = full0 + s * 8;
+          if (wprod) {
+            mbar_arrive_expect_tx_a(fb, ntv * nv * 4096 + NT * (sc_bytes + zp_bytes));
+            for (int t = 0; t < ntv; ++t)
+              bulk_g2s_a(w0 + (s * NT + t) * NS * 4096, wsrc + t * tile_stride, nv * 4096, fb);
+            if (sc_bytes || zp_bytes) {
+              const int g0 = gcur;
+              for (int t = 0; t < NT; ++t) {
+                if (sc_bytes)
+                  tma_load_2d_a(s0 + (s * NT + t) * NS * 256, &smap, n0 + t * kTileN, g0, fb);
+                if (zp_bytes)
+                  tma_load_2d_a(z0 + (s * NT + t) * NS * 256, &zmap, n0 + t * kTileN, g0, fb);
+              }
+            }
+            wsrc += NS * 4096;
+          } else if (p.a3d) {
+            mbar_arrive_expect_tx_a(fb, NS * a_sub);
+            tma_load_3d_a(a0 + s * NS * a_sub, &amap, 0, y, k64_0, fb);
+          } else {
+            mbar_arrive_expect_tx_a(fb, nv * a_sub);
+            for (int j = 0; j < nv; ++j)
+              tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * kStageK, y, fb);
+          }
+          if (stage_in_group) {
+            gleft -= NS;
+            if (gleft == 0) {
+              ++gcur;
+              gleft = sub_per_group;
+            }
+          } else {
+            gcur += p.gps;
+          }
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // Let every copy issued land before the CTA can exit.
+      const uint32_t issued = it;
+      for (uint32_t j = (issued > static_cast<uint32_t>(S) ? issued - S : 0); j < issued; ++j) {
+        volatile int no_abort = 0;
+        mbar_wait(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
+      }
+    }
+  } else if (warp == 1 || warp == kMma2Warp) {
+    // ----------------------------------------------------------------- MMA
+    // With MMA2, two issuing threads take turns by MMA group (one stage, or
+    // two one-block stages): the issuing thread is held inside each
+    // tcgen05.mma for about its execution time, so one thread's barrier waits
+    // and bookkeeping run while the other's MMAs keep the tensor pipe busy.  A
+    // group is issued only after the previous one (token barrier between
+    // tcgen05 fences), so the pipe receives the groups in K order, and the
+    // issuer of a chunk's last group alone signals the accumulator ready: its
+    // MMAs accumulate after all earlier ones.  Without MMA2, warp 1 alone
+    // issues every group (the loop right below).
+    if constexpr (!MMA2) {
+    if (lane == 0 && warp == 1) {
+      const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
+      const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
+      const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
+      uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0;
+      bool ok = true;
+      Unit u;
+      for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+        bool chunk_start = true;
+        const int nkb = u.kb1 - u.kb0;
+        // stages of the current exact chunk (W4A8) or of the unit still to go
+        const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
+        int left = 0;
+        auto advance = [&]() {
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1;
+          }
+          if (++ts == static_cast<uint32_t>(TS)) {
+            ts = 0;
+            tph ^= 1;
+          }
+        };
+        for (int j = 0; j < nkb;) {
+          if (chunk_start) {
+            if (ev > 0 && !mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) {
+              ok = false;
+              break;
+            }
+            left = chunk_len < nkb - j ? chunk_len : nkb - j;
+          }
+          // One-block stages go to the tensor pipe two at a time (eight MMAs
+          // per group) when both belong to the same exact chunk.
+          const bool pair = NS == 1 && NT == 1 && TS >= 2 && left >= 2;
+          // The converter group arrives on tfull only after it observed the
+          // stage's full barrier, so tfull also orders the activation tile.
+          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t s1 = s, ts1 = ts;
+          uint32_t s2 = s + 1, ts2 = ts + 1, tph2 = tph;
+          if (s2 == static_cast<uint32_t>(S)) s2 = 0;
+          if (ts2 == static_cast<uint32_t>(TS)) {
+            ts2 = 0;
+            tph2 ^= 1;
+          }
+          if (pair && !mbar_wait(&sm.tfull[ts2], tph2, abort, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool two_blocks = NS == 2 && NT == 1 && p.k64 - (u.kb0 + j) * NS >= 2;
+          if (pair || two_blocks) {
+            // eight MMAs: two stages of one 64-K block, or one stage of two
+            uint32_t a8[8];
+            uint64_t b8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int half = i >> 2, kk = i & 3;
+              if (pair) {
+                a8[i] = tmem + p.acol + (half ? ts2 : ts1) * 32 + 8 * kk;
+                b8[i] = desc0 + (half ? s2 : s1) * sub16 + 2 * kk;
+              } else {
+                a8[i] = tmem + p.acol + ts1 * 64 + 32 * half + 8 * kk;
+                b8[i] = desc0 + s1 * 2 * sub16 + half * sub16 + 2 * kk;
+              }
+            }
+            mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+          } else {
+            const int k64_0 = (u.kb0 + j) * NS;
+            const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+            for (int t = 0; t < NT; ++t) {
+              const uint32_t dcol = tmem + t * BM;
+              const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
+              const uint64_t dsc = desc0 + s * NS * sub16;
+              if (nv == 4) {
+                mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+              } else {
+                mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
+                for (int q = 1; q < nv; ++q)
+                  mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
+              }
+            }
+          }
+          mma_commit(&sm.empty[s1]);
+          advance();
+          if (pair) {
+            mma_commit(&sm.empty[s2]);
+            advance();
+          }
+          const int used = pair ? 2 : 1;
+          j += used;
+          left -= used;
+          chunk_start = false;
+          if (left == 0) {
+            mma_commit(sm.dfull);
+            ++ev;
+            chunk_start = true;
+          }
+        }
+      }
+      // All issued MMAs complete before tensor memory is released.
+      mma_commit(sm.fin);
+      volatile int no_abort = 0;
+      mbar_wait(sm.fin, 0, &no_abort, args.status);
+    }
+    } else {
+    if (lane == 0) {
+      const uint32_t me = warp == 1 ? 0u : 1u;  // issues the groups g with g % 2 == me
+      const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
+      const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
+      const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
+      uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0, g = 0, tok_ph = 0;
+      bool ok = true, issued = false;
+      Unit u;
+      for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+        bool chunk_start = true;
+        const int nkb = u.kb1 - u.kb0;
+        // stages of the current exact chunk (W4A8) or of the unit still to go
+        const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
+        int left = 0;
+        auto advance = [&]() {
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1;
+          }
+          if (++ts == static_cast<uint32_t>(TS)) {
+            ts = 0;
+            tph ^= 1;
+          }
+        };
+        for (int j = 0; j < nkb; ++g) {
+          if (chunk_start) left = chunk_len < nkb - j ? chunk_len : nkb - j;
+          // One-block stages go to the tensor pipe two at a time (eight MMAs
+          // per group) when both belong to the same exact chunk.
+          const bool pair = NS == 1 && NT == 1 && TS >= 2 && left >= 2;
+          const int used = pair ? 2 : 1;
+          const bool chunk_end = left == used;
+          if ((g & 1u) == me) {
+            if (chunk_start && ev > 0 && !mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) {
+              ok = false;
+              break;
+            }
+            // The converter group arrives on tfull only after it observed the
+            // stage's full barrier, so tfull also orders the activation tile.
+            if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t s1 = s, ts1 = ts;
+            uint32_t s2 = s + 1, ts2 = ts + 1, tph2 = tph;
+            if (s2 == static_cast<uint32_t>(S)) s2 = 0;
+            if (ts2 == static_cast<uint32_t>(TS)) {
+              ts2 = 0;
+              tph2 ^= 1;
+            }
+            if (pair && !mbar_wait(&sm.tfull[ts2], tph2, abort, args.status)) {
+              ok = false;
+              break;
+            }
+            // the other thread has issued the previous group (waited last,
+            // so that the pipe changes hands with the least delay)
+            if (g > 0) {
+              if (!mbar_wait(&sm.tok[me], tok_ph, abort, args.status)) {
+                ok = false;
+                break;
+              }
+              tok_ph ^= 1;
+            }
+            tc_fence_after();
+            const bool two_blocks = NS == 2 && NT == 1 && p.k64 - (u.kb0 + j) * NS >= 2;
+            if (pair || two_blocks) {
+              // eight MMAs: two stages of one 64-K block, or one stage of two
+              uint32_t a8[8];
+              uint64_t b8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int half = i >> 2, kk = i & 3;
+                if (pair) {
+                  a8[i] = tmem + p.acol + (half ? ts2 : ts1) * 32 + 8 * kk;
+                  b8[i] = desc0 + (half ? s2 : s1) * sub16 + 2 * kk;
+                } else {
+                  a8[i] = tmem + p.acol + ts1 * 64 + 32 * half + 8 * kk;
+                  b8[i] = desc0 + s1 * 2 * sub16 + half * sub16 + 2 * kk;
+                }
+              }
+              mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+            } else {
+              const int k64_0 = (u.kb0 + j) * NS;
+              const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+              for (int t = 0; t < NT; ++t) {
+                const uint32_t dcol = tmem + t * BM;
+                const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
+                const uint64_t dsc = desc0 + s * NS * sub16;
+                if (nv == 4) {
+                  mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+                } else {
+                  mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
+                  for (int q = 1; q < nv; ++q)
+                    mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
+                }
+              }
+            }
+            // hand the pipe over, then release the stages (a commit tracks
+            // this thread's own MMAs)
+            tc_fence_before();
+            mbar_arrive(&sm.tok[me ^ 1u]);
+            mma_commit(&sm.empty[s1]);
+            if (pair) mma_commit(&sm.empty[s2]);
+            if (chunk_end) mma_commit(sm.dfull);
+            issued = true;
+          }
+          advance();
+          if (pair) advance();
+          j += used;
+          left -= used;
+          chunk_start = false;
+          if (left == 0) {
+            ++ev;
+            chunk_start = true;
+          }
+        }
+      }
+      // All issued MMAs complete before tensor memory is released (a thread
+      // that issued none arrives directly).
+      if (issued) mma_commit(sm.fin);
+      else mbar_arrive(sm.fin);
+      volatile int no_abort = 0;
+      mbar_wait(sm.fin, 0, &no_abort, args.status);
+    }
+    }
+  } else {
+    // ----------------------------------------------- converters + epilogue
+    const int cw = warp - 2;           // converter warp index 0..kConvWarps-1
+    const int grp = cw >> 2;           // group: converts stages it % kConvGroups == grp
+    const int q = warp & 3;            // tensor-memory lane quadrant of this warp
+    const int r = q * 32 + lane;       // weight row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int nblk = BM / 8;           // 8-column blocks of the accumulator
+    uint32_t it = 0, ev = 0;
+    // stage counters kept incrementally (no division in the loop): it % S and
+    // its phase, it % TS, and (it - TS) % S and its phase once it >= TS
+    uint32_t cs = 0, cph = 0, cts = 0, ps = 0, pph = 0;
+    auto adv = [&]() {
+      if (++cs == static_cast<uint32_t>(S)) {
+        cs = 0;
+        cph ^= 1;
+      }
+      if (++cts == static_cast<uint32_t>(TS)) cts = 0;
+      if (it > static_cast<uint32_t>(TS) && ++ps == static_cast<uint32_t>(S)) {
+        ps = 0;
+        pph ^= 1;
+      }
+    };
+    bool ok = true;
+    Unit u;
+    for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
+      int mt, nt;
+      tile_coords(p, u.tile, mt, nt);
+      const int64_t n0 = static_cast<int64_t>(nt) * NT * kTileN;  // first weight column
+      const int64_t m0 = static_cast<int64_t>(mt) * BM;
+      const int nkb = u.kb1 - u.kb0;
+      const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
+      int cleft = 0;  // stages left in the current exact chunk
+      bool first_chunk = true;
+      int gcur = u.kb0 * NS / sub_per_group;  // scale group of stage j
+      int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
+      auto gadv = [&]() {
+        if (stage_in_group) {
+          gleft -= NS;
+          if (gleft == 0) {
+            ++gcur;
+            gleft = sub_per_group;
+          }
+        } else {
+          gcur += p.gps;
+        }
+      };
+      for (int j = 0; j < nkb; ++j, ++it, adv(), gadv()) {
+        if (cleft == 0) cleft = chunk_len < nkb - j ? chunk_len : nkb - j;
+        if (static_cast<int>(it % kConvGroups) == grp) {
+          const uint32_t s = cs, ts = cts;
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], cph, abort, args.status))) {
+            ok = false;
+            break;
+          }
+          if (it >= static_cast<uint32_t>(TS)) {
+            // the tensor-memory slot is free once the MMA of stage it-TS retired
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.empty[ps], pph, abort, args.status))) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after();
+          const int k64_0 = (u.kb0 + j) * NS;
+          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+          for (int t = 0; t < NT; ++t) {
+            const size_t st_idx = static_cast<size_t>(s) * NT + t;
+            const uint8_t* wst = sm.w + st_idx * NS * 4096;
+            const uint8_t* sst = sm.s + st_idx * NS * 256;
+            const uint8_t* zst = sm.z + st_idx * NS * 256;
+            const uint32_t tcol = tmem + lane_base + p.acol + (ts * NT + t) * NS * 32;
+            const bool row_ok = n0 + t * kTileN + r < N;
+            for (int qq = 0; qq < nv; ++qq) {
+              const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
+              const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
+              const int grow = stage_in_group ? 0 : qq >> grow_shift;
+              uint32_t s2 = 0, nz2 = 0;
+              bool has_s = true;
+              if (MODE == kW4A8) {
+                has_s = args.scales != nullptr;
+                if (has_s) {
+                  const float sg = static_cast<float>(
+                      reinterpret_cast<const int8_t*>(sst + grow * 128)[r]);
+                  s2 = as_u32(__float2bfloat162_rn(sg));
+                }
+              } else {
+                const uint16_t sv = reinterpret_cast<const uint16_t*>(sst + grow * 256)[r];
+                s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
+                if (args.zeros) {
+                  const uint16_t zv =
+                      reinterpret_cast<const uint16_t*>(zst + grow * 256)[r] ^ 0x8000u;
+                  nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
+                }
+              }
+              uint32_t v[32];
+              uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+              uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
+              convert_chunk<MODE>(w0, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v0);
+              convert_chunk<MODE>(w1, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v1);
+              if (!row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0;
+              }
+              tmem_st32(tcol + qq * 32, v);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sm.tfull[ts]);
+            mbar_arrive(&sm.empty[s]);
+          }
+        }
+        const bool chunk_end = --cleft == 0;
+        if (!chunk_end) continue;
+        // ------------------------------------------------ drain an event
+        const bool final_ev = (j == nkb - 1);
+        const bool split = final_ev && u.nslots > 1;
+        const size_t slot_elems = static_cast<size_t>(NT) * kTileN * BM;
+        const uint32_t* part = reinterpret_cast<const uint32_t*>(args.partials);
+        // Split tile: each warp takes its place in the arrival order of the
+        // tile's contributors for its sub-tile (low half of the counter).
+        // The last to arrive adds the others' partial sums to its own
+        // accumulator; the others write theirs and then count themselves as
+        // written (high half), which the last one waits for.
+        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + cw;
+        bool reducer = false;
+        if (split) {
+          int prev_count = 0;
+          if (lane == 0) prev_count = atomicAdd(ctr, 1);
+          prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
+          reducer = (prev_count & 0xffff) == u.nslots - 1;
+        }
+        // position of this unit among the tile's contributors (K order), and
+        // the slot of contributor sl held by lane sl (<= 32 contributors)
+        const int my_sl = p.decomp == kSplitK ? u.split : static_cast<int>(blockIdx.x) - u.cfirst;
+        const size_t lane_slot =
+            reducer && lane < u.nslots ? slot_index(p, wk, u, lane) * slot_elems : 0;
+        // Pull what this drain will read toward L2 while the last MMAs run:
+        // the other contributors' partial sums (reducer) and the int32
+        // running sum of the earlier chunks (W4A8 with the global copy).
+        int32_t* gi_base = args.icopy + static_cast<size_t>(blockIdx.x) * NT * BM * kTileN;
+        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+          if (MODE == kW4A8 && p.gicopy && !first_chunk) prefetch_l2(gi_base + coff);
+          if (reducer) {
+            for (int sl = 0; sl < u.nslots; ++sl) {
+              if (sl == my_sl) continue;
+              const size_t sbase =
+                  u.nslots <= 32
+                      ? static_cast<size_t>(__shfl_sync(
+                            0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
+                      : slot_index(p, wk, u, sl) * slot_elems;
+              prefetch_l2(part + sbase + coff);
+            }
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(sm.dfull, ev & 1, abort, args.status))) {
+          ok = false;
+          break;
+        }
+        ++ev;
+        tc_fence_after();
+        if (reducer) {
+          // every other contributor has written its partial sums
+          bool done = true;
+          if (lane == 0) done = wait_count_hi(ctr, u.nslots - 1, abort, args.status);
+          if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, done, 0))) {
+            ok = false;
+            break;
+          }
+          __threadfence();
+        }
+        const size_t my_slot = split && !reducer ? own_slot(p, u) * slot_elems : 0;
+        // Blocks of 8 accumulator columns over all weight tiles, round-robin
+        // over the converter groups.  Global layout of partial sums and of
+        // the int32 running sum: block (t, cc) is 128 rows x 8 columns, row r
+        // holding its 8 columns contiguously.
+        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+          const uint32_t dcol = tmem + lane_base + t * BM + cc;
+          const int64_t nrow = n0 + t * kTileN + r;  // output column
+          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+          uint32_t d[8];
+          tmem_ld8(dcol, d);
+          if (MODE == kW4A8) {
+            // add the int32 running sum of the earlier chunks of this unit:
+            // in tensor memory, or in this CTA's global scratch
+            const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
+            int32_t* gi = gi_base + coff;
+            uint32_t prev[8];
+            if (!first_chunk) {
+              if (p.gicopy) ld_cg_v8(gi, prev);
+              else tmem_ld8(icol, prev);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(d[i])) +
+                                           (first_chunk ? 0 : static_cast<int32_t>(prev[i])));
+            if (!final_ev) {
+              if (p.gicopy) {
+                st_v8(gi, d);
+              } else {
+                tmem_st8(icol, d);
+                tmem_wait_st();
+              }
+              continue;
+            }
+          } else {
+            tmem_wait_ld();
+          }
+          // d: this unit's sums of the block (int32 or fp32 bits)
+          if (split && !reducer) {
+            st_v8(static_cast<uint32_t*>(args.partials) + my_slot + coff, d);
+            continue;
+          }
+          if (reducer) {
+            // add the contributors in K order, this unit's own sums at its place
+            uint32_t acc[8];
+            for (int sl = 0; sl < u.nslots; ++sl) {
+              uint32_t x[8];
+              if (sl == my_sl) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = d[i];
+              } else {
+                const size_t sbase =
+                    u.nslots <= 32
+                        ? static_cast<size_t>(__shfl_sync(
+                              0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
+                        : slot_index(p, wk, u, sl) * slot_elems;
+                ld_cg_v8(part + sbase + coff, x);
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (sl == 0) acc[i] = x[i];
+                else if (MODE == kW4A8)
+                  acc[i] = static_cast<uint32_t>(static_cast<int32_t>(acc[i]) +
+                                                 static_cast<int32_t>(x[i]));
+                else
+                  acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __uint_as_float(x[i]));
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = acc[i];
+          }
+          // outputs
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int64_t m = m0 + cc + i;
+            if (nrow < N && m < M) {
+              const int64_t o = m * N + nrow;
+              if (MODE == kW4A8) {
+                const int32_t acc = static_cast<int32_t>(d[i]);
+                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acc;
+                else
+                  static_cast<__half*>(args.out)[o] = __float2half_rn(
+                      static_cast<float>(acc) * args.s_tok[m] * args.s_ch[nrow]);
+              } else {
+                static_cast<T16*>(args.out)[o] = to_t16<T16>(__uint_as_float(d[i]));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.dempty);
+        first_chunk = false;
+        if (split && !reducer) {
+          // partial sums visible device-wide, then counted as written
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(ctr, 0x10000);
+        } else if (reducer) {
+          if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+
+namespace {
+template <bool MMA2>
+cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                        const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  const void* fn;
+  if (plan.mode == kW4A16_F16)
+    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_F16, MMA2>);
+  else if (plan.mode == kW4A16_BF16)
+    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_BF16, MMA2>);
+  else fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A8, MMA2>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(plan.smem_bytes));
+  if (e != cudaSuccess) return e;
+  const int threads = MMA2 ? kTcThreads : kTcThreads - 32;
+  if (plan.mode == kW4A16_F16) {
+    tc_gemm_kernel<kW4A16_F16, MMA2>
+        <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
+    return cudaGetLastError();
+  }
+  if (plan.mode == kW4A16_BF16) {
+    tc_gemm_kernel<kW4A16_BF16, MMA2>
+        <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
+    return cudaGetLastError();
+  }
+  // W4A8: a programmatic dependent of its int8 -> bf16 staging launch; only
+  // the activation producer waits for that grid (weights and scales are not
+  // written by it), so the weight stream starts at once
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = plan.smem_bytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, &tc_gemm_kernel<kW4A8, MMA2>, amap, smap, zmap, plan, args);
+}
+}  // namespace
+
+}  // namespace w4
