@@ -75,9 +75,9 @@ struct DsUnit {
   int seg;        // index of this tile among the CTA's tiles
 };
 
-__device__ __forceinline__ int64_t ds_start(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+__device__ __forceinline__ int64_t ds_start(int64_t c, int64_t T, int64_t G) { return div_nn(c * T, G); }
 __device__ __forceinline__ int64_t ds_owner(int64_t i, int64_t T, int64_t G) {
-  return ((i + 1) * G - 1) / T;
+  return div_nn((i + 1) * G - 1, T);
 }
 
 // u-th tile segment of this CTA's stream-K range; false when there is none.
@@ -85,7 +85,7 @@ __device__ __forceinline__ bool ds_unit(const DsPlan& p, int u, DsUnit& o) {
   const int64_t T = static_cast<int64_t>(p.n_tiles) * p.kblocks, G = p.grid;
   const int64_t b = ds_start(blockIdx.x, T, G), e = ds_start(blockIdx.x + 1, T, G);
   if (b >= e) return false;
-  const int64_t t = b / p.kblocks + u;
+  const int64_t t = div_nn(b, p.kblocks) + u;
   int64_t lo = t * p.kblocks, hi = lo + p.kblocks;
   if (lo < b) lo = b;
   if (hi > e) hi = e;
@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kDsRedThreads) ds_reduce_kernel(const DsPlan p
   const size_t slot_elems = static_cast<size_t>(8 * NJ) * kTileN;
   auto slot_base = [&](int sl) -> unsigned long long {
     const int64_t cpr = cf + sl;
-    const int64_t seg = tile - ds_start(cpr, T, G) / p.kblocks;
+    const int64_t seg = tile - div_nn(ds_start(cpr, T, G), p.kblocks);
     return (static_cast<size_t>(cpr) * p.max_segs + seg) * slot_elems;
   };
   for (int sl = threadIdx.x; sl < nslots && sl < kDsRedMaxSlots; sl += kDsRedThreads)

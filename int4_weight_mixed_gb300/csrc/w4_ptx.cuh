@@ -23,6 +23,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// a / b for non-negative 64-bit values, in 32-bit arithmetic when both fit:
+// division by a runtime value is a long dependent instruction sequence, and
+// the 64-bit one several times longer (it delays a CTA's first copy).
+__device__ __forceinline__ int64_t div_nn(int64_t a, int64_t b) {
+  if (((a | b) >> 32) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)

@@ -60,11 +60,11 @@ struct Work {
   int64_t first_tile;
 };
 
-__device__ __forceinline__ int64_t sk_start(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+__device__ __forceinline__ int64_t sk_start(int64_t c, int64_t T, int64_t G) { return div_nn(c * T, G); }
 
 // Stream-K: the CTA that owns linear iteration i.
 __device__ __forceinline__ int64_t sk_owner(int64_t i, int64_t T, int64_t G) {
-  return ((i + 1) * G - 1) / T;
+  return div_nn((i + 1) * G - 1, T);
 }
 
 // u-th unit of this CTA; false when there is none.
@@ -74,11 +74,11 @@ __device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
     // [j*kb/ks, (j+1)*kb/ks) of its tile
     const int64_t v = blockIdx.x + static_cast<int64_t>(u) * p.grid;
     if (v >= static_cast<int64_t>(p.tiles) * p.ksplit) return false;
-    const int t = static_cast<int>(v / p.ksplit), j = static_cast<int>(v % p.ksplit);
+    const int t = static_cast<int>(div_nn(v, p.ksplit)), j = static_cast<int>(v - static_cast<int64_t>(t) * p.ksplit);
     out.tile = t;
     out.split = j;
-    out.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kb_total / p.ksplit);
-    out.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kb_total / p.ksplit);
+    out.kb0 = static_cast<int>(div_nn(static_cast<int64_t>(j) * p.kb_total, p.ksplit));
+    out.kb1 = static_cast<int>(div_nn(static_cast<int64_t>(j + 1) * p.kb_total, p.ksplit));
     out.nslots = p.ksplit;
     out.cfirst = 0;
     out.seg = 0;
@@ -118,7 +118,7 @@ __device__ __forceinline__ size_t slot_index(const TcPlan& p, const Work& w, con
                                              int sl) {
   if (p.decomp == kSplitK) return static_cast<size_t>(u.tile) * p.ksplit + sl;
   const int64_t cpr = u.cfirst + sl;
-  const int64_t seg = u.tile - sk_start(cpr, w.T, w.G) / w.kb;
+  const int64_t seg = u.tile - div_nn(sk_start(cpr, w.T, w.G), w.kb);
   return static_cast<size_t>(cpr) * p.max_segs + seg;
 }
 __device__ __forceinline__ size_t own_slot(const TcPlan& p, const Unit& u) {
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
   wk.G = p.grid;
   wk.begin = sk_start(blockIdx.x, wk.T, wk.G);
   wk.end = sk_start(blockIdx.x + 1, wk.T, wk.G);
-  wk.first_tile = wk.begin / wk.kb;
+  wk.first_tile = div_nn(wk.begin, wk.kb);
 
   const int64_t M = args.M, N = args.N, K = args.K;
   const int gsz = static_cast<int>(args.group_size);
