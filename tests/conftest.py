@@ -37,3 +37,16 @@ def gpu_lib():
     import int4_weight_mixed_gb300 as w4
     w4.load()
     return w4
+
+
+@pytest.fixture(autouse=True)
+def no_device_timeouts(request):
+    """After every GPU test: no kernel recorded a device-side wait timeout in
+    any workspace the binding handed out (a timed-out wait can still leave
+    correct outputs, so results alone would not show it)."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import int4_weight_mixed_gb300 as w4
+    for ws in list(w4._ws_cache.values()):
+        assert w4.check_status(ws) == w4.OK, "a device-side wait timed out"
