@@ -24,13 +24,24 @@ constexpr int kMaxTmemStages = 8;
 // it % kConvGroups == g, so kConvGroups stages are in conversion at once.
 constexpr int kConvGroups = 4;
 constexpr int kConvWarps = 4 * kConvGroups;
-// warp 0: weight producer + tensor-memory allocation; warp 1: MMA issue;
-// warps 2..kConvWarps+1: converters / epilogue; then the activation producer
-// and the second MMA-issuing warp (the two issuers alternate by MMA group)
-constexpr int kTcThreads = 64 + 32 * kConvWarps + 64;  // with the second MMA warp
-// (a kernel without it launches kTcThreads - 32 threads)
-constexpr int kActWarp = kTcThreads / 32 - 2;
-constexpr int kMma2Warp = kTcThreads / 32 - 1;
+// warps 0..kConvWarps-1: converters / epilogue (four warpgroups); then the
+// weight producer (also allocates tensor memory), the MMA issuer, the
+// activation producer and the second MMA-issuing warp (the two issuers
+// alternate by MMA group; idle in the one-issuer kernel) — the fifth warpgroup
+constexpr int kTcThreads = 32 * kConvWarps + 128;
+constexpr int kProdWarp = kConvWarps;
+constexpr int kMmaWarp = kConvWarps + 1;
+constexpr int kActWarp = kConvWarps + 2;
+constexpr int kMma2Warp = kConvWarps + 3;
+// Registers a thread after the split at kernel start (setmaxnreg): the
+// launch gives every thread 96 (640 threads, five warps on a sub-partition);
+// the converter warpgroups take 104, the fifth warpgroup keeps 64:
+// 512 * 104 + 128 * 64 = 61440 <= 640 * 96 = 61440.
+constexpr int kTcLaunchRegs = 96;
+constexpr int kTcConvRegs = 104;
+constexpr int kTcOtherRegs = 64;
+static_assert(32 * kConvWarps * kTcConvRegs + 128 * kTcOtherRegs <= kTcThreads * kTcLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr size_t kWsHeader = 256;                // status word + spare
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };

@@ -220,10 +220,9 @@ struct Smem {
 
 }  // namespace
 
-// MMA2: two alternating MMA-issuing threads (one more warp); a separate
-// instantiation, so that the one-issuer kernel keeps its register budget.
+// MMA2: two alternating MMA-issuing threads; a separate instantiation.
 template <int MODE, bool MMA2>
-__global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap amap,
                    const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ CUtensorMap zmap, const TcPlan p, const TcArgs args) {
@@ -271,7 +270,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
     if (args.scales) prefetch_tensormap(&smap);
     if (args.zeros) prefetch_tensormap(&zmap);
   }
-  if (warp == 0) {
+  if (warp == kProdWarp) {
     tmem_alloc(sm.tmem_slot, 512);
     tmem_relinquish();
   }
@@ -279,6 +278,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
+
 
   Work wk;
   wk.kb = p.kb_total;
@@ -298,14 +298,20 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
   const int grow_shift = sub_per_group >= 2 ? 1 : 0;
   const int esz = MODE == kW4A8 ? 1 : 2;
 
-  if (warp == 0 || warp == kActWarp) {
+  if (warp >= kConvWarps) {
+  // W4A16 with one MMA issuer: the fifth warpgroup (producers, MMA) gives
+  // registers to the converters, whose scale / zero-point FMAs otherwise
+  // spill (the other kernels keep the even split: measured faster)
+  if constexpr (MODE != kW4A8 && !MMA2)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcOtherRegs));
+  if (warp == kProdWarp || warp == kActWarp) {
     // ----------------------------------------------------------- producers
     // Two single-thread producers fill each stage in parallel, each with its
     // own expect-tx on the stage's full barrier: warp 0 the bulk copy of the
     // stage's nibbles and the scale / zero-point boxes, the last warp the
     // activation tile(s).
     if (lane == 0) {
-      const bool wprod = warp == 0;
+      const bool wprod = warp == kProdWarp;
       // W4A8: the activations come from the staging grid this one may have
       // been launched beside (programmatic dependent launch); wait for it
       if (!wprod) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -381,7 +387,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
         mbar_wait(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
       }
     }
-  } else if (warp == 1 || warp == kMma2Warp) {
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
     // ----------------------------------------------------------------- MMA
     // With MMA2, two issuing threads take turns by MMA group (one stage, or
     // two one-block stages): the issuing thread is held inside each
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
     // MMAs accumulate after all earlier ones.  Without MMA2, warp 1 alone
     // issues every group (the loop right below).
     if constexpr (!MMA2) {
-    if (lane == 0 && warp == 1) {
+    if (lane == 0 && warp == kMmaWarp) {
       const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
       const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
       const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
@@ -502,7 +508,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
     }
     } else {
     if (lane == 0) {
-      const uint32_t me = warp == 1 ? 0u : 1u;  // issues the groups g with g % 2 == me
+      const uint32_t me = warp == kMmaWarp ? 0u : 1u;  // issues the groups g with g % 2 == me
       const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
       const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
       const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
@@ -625,9 +631,12 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
       mbar_wait(sm.fin, 0, &no_abort, args.status);
     }
     }
+  }
   } else {
+    if constexpr (MODE != kW4A8 && !MMA2)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcConvRegs));
     // ----------------------------------------------- converters + epilogue
-    const int cw = warp - 2;           // converter warp index 0..kConvWarps-1
+    const int cw = warp;               // converter warp index 0..kConvWarps-1
     const int grp = cw >> 2;           // group: converts stages it % kConvGroups == grp
     const int q = warp & 3;            // tensor-memory lane quadrant of this warp
     const int r = q * 32 + lane;       // weight row within the tile
@@ -909,7 +918,7 @@ __global__ void __launch_bounds__(MMA2 ? kTcThreads : kTcThreads - 32, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kProdWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -929,7 +938,7 @@ cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUten
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem_bytes));
   if (e != cudaSuccess) return e;
-  const int threads = MMA2 ? kTcThreads : kTcThreads - 32;
+  const int threads = kTcThreads;
   if (plan.mode == kW4A16_F16) {
     tc_gemm_kernel<kW4A16_F16, MMA2>
         <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
