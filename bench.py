@@ -299,46 +299,56 @@ def run_gpu(args):
         h2d = sum(host_a[M].numel() + 4 * host_s[M].numel() for M in M_SWEEP)
         d2h = sum(2 * M * N for M in M_SWEEP)
         e2e_steps = max(3, min(args.steps, 50))
-        # Copies on a second stream overlap the GEMMs: the inputs of the next M
-        # go in while the current GEMM runs, and each result comes back while
-        # the next GEMM runs (device buffers allocated once, outside the timing).
-        copy_stream = torch.cuda.Stream(device=dev)
-        dev_a = {M: torch.empty_like(host_a[M], device=dev) for M in M_SWEEP}
-        dev_s = {M: torch.empty_like(host_s[M], device=dev) for M in M_SWEEP}
-        dev_o = {M: torch.empty((M, N), dtype=torch.float16, device=dev) for M in M_SWEEP}
+        # Copies on two more streams (one per direction, so that both copy
+        # engines run) overlap the GEMMs: the inputs of the next M go in while
+        # the current GEMM runs, and each result comes back while the next GEMM
+        # runs. Two sets of device buffers, used by alternate steps, let a
+        # step's GEMMs start while the previous step's last result is still
+        # being copied back (allocated once, outside the timing).
+        h2d_stream = torch.cuda.Stream(device=dev)
+        d2h_stream = torch.cuda.Stream(device=dev)
+        bufs = [dict(a={M: torch.empty_like(host_a[M], device=dev) for M in M_SWEEP},
+                     s={M: torch.empty_like(host_s[M], device=dev) for M in M_SWEEP},
+                     o={M: torch.empty((M, N), dtype=torch.float16, device=dev) for M in M_SWEEP},
+                     free=None)
+                for _ in range(2)]
         ev_in = {M: torch.cuda.Event() for M in M_SWEEP}
         ev_out = {M: torch.cuda.Event() for M in M_SWEEP}
+        step_no = [0]
 
         def e2e_step():
-            with torch.cuda.stream(copy_stream):
+            b = bufs[step_no[0] % 2]
+            step_no[0] += 1
+            with torch.cuda.stream(h2d_stream):
+                if b["free"] is not None:  # this set's previous GEMMs and copies are done
+                    h2d_stream.wait_event(b["free"])
                 for M in M_SWEEP:
-                    dev_a[M].copy_(host_a[M], non_blocking=True)
-                    dev_s[M].copy_(host_s[M], non_blocking=True)
-                    ev_in[M].record(copy_stream)
+                    b["a"][M].copy_(host_a[M], non_blocking=True)
+                    b["s"][M].copy_(host_s[M], non_blocking=True)
+                    ev_in[M].record(h2d_stream)
             for M in M_SWEEP:
                 stream.wait_event(ev_in[M])
-                w4.gemm(dev_a[M], sets[0]["b"], sets[0]["wtype"], N, scales=None, group_size=-1,
-                        token_scales=dev_s[M], channel_scales=sets[0]["s_ch"], out=dev_o[M],
-                        ws=ws)
+                w4.gemm(b["a"][M], sets[0]["b"], sets[0]["wtype"], N, scales=None,
+                        group_size=-1, token_scales=b["s"][M], channel_scales=sets[0]["s_ch"],
+                        out=b["o"][M], ws=ws)
                 ev_out[M].record(stream)
-            with torch.cuda.stream(copy_stream):
+            with torch.cuda.stream(d2h_stream):
                 for M in M_SWEEP:
-                    copy_stream.wait_event(ev_out[M])
-                    host_o[M].copy_(dev_o[M], non_blocking=True)
-            # the next step's inputs overwrite device buffers the GEMMs read,
-            # and its GEMMs the outputs being copied back: both streams join
-            done = torch.cuda.Event()
-            done.record(copy_stream)
-            stream.wait_event(done)
+                    d2h_stream.wait_event(ev_out[M])
+                    host_o[M].copy_(b["o"][M], non_blocking=True)
+                b["free"] = torch.cuda.Event()
+                b["free"].record(d2h_stream)
 
         for _ in range(3):
             e2e_step()
         barrier()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         x0.record(stream)
-        copy_stream.wait_stream(stream)
+        h2d_stream.wait_stream(stream)
+        d2h_stream.wait_stream(stream)
         for _ in range(e2e_steps):
             e2e_step()
+        stream.wait_stream(d2h_stream)  # the last results are back on the host
         x1.record(stream)
         barrier()
         e2e_ms = x0.elapsed_time(x1) / e2e_steps
