@@ -83,6 +83,21 @@ def measured_traffic(kernel, M):
         return None
 
 
+def slowest_rank_ms(local_ms, world, device):
+    """The job's time: the slowest rank's (ms), returned on every rank."""
+    if world <= 1:
+        return local_ms
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops, world, ms_per_step):
+    """Whole-job throughput: every rank's flops over the slowest rank's time."""
+    return step_flops * world / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -284,11 +299,7 @@ def run_gpu(args):
     if w4.check_status(ws) != w4.OK:
         raise RuntimeError("a device-side wait timed out during the benchmark")
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(total_ms, world, dev)
 
     # end-to-end through the public API from pinned host buffers
     e2e = None
@@ -351,8 +362,8 @@ def run_gpu(args):
         stream.wait_stream(d2h_stream)  # the last results are back on the host
         x1.record(stream)
         barrier()
-        e2e_ms = x0.elapsed_time(x1) / e2e_steps
-        e2e = {"value": sum(flops(M) for M in M_SWEEP) * world / (e2e_ms * 1e-3) / 1e12,
+        e2e_ms = slowest_rank_ms(x0.elapsed_time(x1) / e2e_steps, world, dev)
+        e2e = {"value": job_tflops(sum(flops(M) for M in M_SWEEP), world, e2e_ms),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms}
 
@@ -365,7 +376,7 @@ def run_gpu(args):
     pk = peaks()
     step_flops = sum(flops(M) for M in M_SWEEP)
     ms_per_step = total_ms / args.steps
-    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(step_flops, world, ms_per_step)
     sweep = []
     for M in M_SWEEP:
         if M not in per_m:
