@@ -13,22 +13,28 @@
 //
 // Data flow per pipeline stage (nsub = 1, 2 or 4 blocks of 64 K; the
 // stage is sized so that every stage moves >= 8 KB of nibbles for skinny
-// tiles, because each stage costs the single producer thread a few hundred
-// cycles whatever its size):
-//   producer warp : nsub TMA tiles of the activations (128B-swizzled,
-//                   K-major) + one bulk copy of the stage's prepacked nibbles
-//                   + one TMA box each of scale / zero-point rows
-//   8 converter warps : nibbles -> 16-bit weights in registers, one fused
+// tiles, because each stage costs a producer thread a few hundred cycles
+// whatever its size):
+//   weight producer : one bulk copy of the stage's prepacked nibbles + one
+//                   TMA box each of scale / zero-point rows
+//   activation producer : one 3-D TMA box of the stage's activations
+//                   (128B-swizzled, K-major)
+//   16 converter warps (four groups, each converting every fourth stage) :
+//                   nibbles -> 16-bit weights in registers, one fused
 //                   multiply-add per pair with the scale and pre-scaled
 //                   zero-point (Machete Readme "Overview" NOTE), stored
 //                   straight into tensor memory (tcgen05.st): dequantized
 //                   weights never touch shared memory
-//   MMA thread    : 4 * nsub tcgen05.mma (K = 16) with A from tensor memory
+//   MMA thread(s) : 4 * nsub tcgen05.mma (K = 16) with A from tensor memory
 //                   and B from shared memory, fp32 accumulator in tensor
-//                   memory; one commit per stage releases the stage
+//                   memory; one commit per stage releases the stage (two
+//                   threads alternate by MMA group in the MMA2 variant)
 //   epilogue      : converter warps drain the accumulator (tcgen05.ld),
 //                   convert / scale and store, or write split-K partials and
-//                   let the last arriving warp of each sub-tile reduce them.
+//                   let the last arriving warp of each sub-tile add them.
+// Warps 0-15 are the converters (warpgroups 0-3); the weight producer, the
+// MMA thread, the activation producer and the second MMA thread are warps
+// 16-19 (warpgroup 4).
 //
 // W4A8 (pytorch/ao PR #1113 "support W4A8 Marlin kernel") runs on the same
 // bf16 tensor cores: int8 activations and int4 (x int8 group scale)
