@@ -313,9 +313,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kProdWarp || warp == kActWarp) {
     // ----------------------------------------------------------- producers
     // Two single-thread producers fill each stage in parallel, each with its
-    // own expect-tx on the stage's full barrier: warp 0 the bulk copy of the
-    // stage's nibbles and the scale / zero-point boxes, the last warp the
-    // activation tile(s).
+    // own expect-tx on the stage's full barrier: the weight producer the bulk
+    // copy of the stage's nibbles and the scale / zero-point boxes, the
+    // activation producer the activation tile(s).
     if (lane == 0) {
       const bool wprod = warp == kProdWarp;
       // W4A8: the activations come from the staging grid this one may have
@@ -402,8 +402,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // group is issued only after the previous one (token barrier between
     // tcgen05 fences), so the pipe receives the groups in K order, and the
     // issuer of a chunk's last group alone signals the accumulator ready: its
-    // MMAs accumulate after all earlier ones.  Without MMA2, warp 1 alone
-    // issues every group (the loop right below).
+    // MMAs accumulate after all earlier ones.  Without MMA2, the MMA warp
+    // alone issues every group (the loop right below).
     if constexpr (!MMA2) {
     if (lane == 0 && warp == kMmaWarp) {
       const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
