@@ -289,6 +289,23 @@ __device__ __forceinline__ void mma_ts_stage16(uint32_t d_tmem, uint32_t a0, uin
 // thread is held inside each MMA for about its execution time, so the work
 // it does between MMA groups leaves the tensor pipe idle: the more MMAs per
 // group, the less that costs.
+// Four MMAs into one accumulator (a, b: four operand addresses each); the
+// first accumulates only when `accumulate` is non-zero.
+__device__ __forceinline__ void mma_ts_4(uint32_t d_tmem, const uint32_t* a, const uint64_t* b,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "setp.eq.b32 t, %2, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %9, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %10, %1, t;\n\t}" ::"r"(d_tmem),
+      "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]),
+      "l"(b[1]), "l"(b[2]), "l"(b[3])
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_8(uint32_t d_tmem, const uint32_t (&a)[8],
                                          const uint64_t (&b)[8], uint32_t idesc,
                                          uint32_t accumulate) {

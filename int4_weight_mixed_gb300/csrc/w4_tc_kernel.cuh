@@ -473,7 +473,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 b8[i] = desc0 + s1 * 2 * sub16 + half * sub16 + 2 * kk;
               }
             }
-            mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+            if (MODE == kW4A8 && pair) {
+              // W4A8: the first stage's shared-memory slot is released as soon
+              // as its own four MMAs retire (measured 3% faster at 256-row
+              // tiles; W4A16 measured slower with the extra commit)
+              mma_ts_4(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              mma_commit(&sm.empty[s1]);
+              mma_ts_4(tmem, a8 + 4, b8 + 4, idesc, 1u);
+            } else {
+              mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+            }
           } else {
             const int k64_0 = (u.kb0 + j) * NS;
             const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
@@ -490,7 +499,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
           }
-          mma_commit(&sm.empty[s1]);
+          if (!(MODE == kW4A8 && pair)) mma_commit(&sm.empty[s1]);
           advance();
           if (pair) {
             mma_commit(&sm.empty[s2]);
