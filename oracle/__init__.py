@@ -23,6 +23,11 @@ What each function computes, and the page it follows:
   "support W4A8 Marlin kernel": int8 x int4 (per-channel) or int8 x
   (int4 * group scale) (per-group), exact integer accumulator, then
   acc * s_tok[m] * s_ch[n].
+* ``quant_per_token`` — vLLM PR #6547 "Enable Dynamic Per Token fp8" (one
+  activation scale per token, computed from that token at run time) with
+  the symmetric int8 activations of pytorch/ao PR #1113: s = amax/127 and
+  q = round-half-even(a/s) in fp32 (the formula is a reading; the pages
+  print none).
 
 Every function is pinned by ``tests/test_oracle_pins.py``; none is "parity
 unpinned".
@@ -78,6 +83,7 @@ def _load():
             lib.or_w4a8.argtypes = [i64, i64, i64, p, p, i32, i32, p, i64, p]
             lib.or_w4a8_elems.argtypes = [i64, i64, i64, p, p, i32, i32, p, i64, i64, p, p, p]
             lib.or_w4a8_scale.argtypes = [i64, p, p, p, p, p, p]
+            lib.or_quant_per_token.argtypes = [i64, i64, p, p, p]
             lib.or_num_threads.restype = i32
             _lib = lib
     return _lib
@@ -201,3 +207,21 @@ def w4a8_scale(acc, rows, cols, s_tok, s_ch):
     _load().or_w4a8_scale(acc.shape[0], _ptr(acc), _ptr(rows), _ptr(cols), _ptr(s_tok),
                           _ptr(s_ch), _ptr(ref))
     return ref
+
+
+def quant_per_token(a):
+    """Per-token int8 codes [M, K] and fp32 scales [M] of fp16/bf16/fp32
+    activations a [M, K] (converted to fp32 exactly)."""
+    try:
+        import torch
+
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().to(torch.float32).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    M, K = a.shape
+    q = np.empty((M, K), np.int8)
+    s = np.empty(M, np.float32)
+    _load().or_quant_per_token(M, K, _ptr(a), _ptr(q), _ptr(s))
+    return q, s

@@ -34,9 +34,12 @@
  *  - W4A8 per-group: an int8 group scale sg[g][n] multiplies the int4 value
  *    to give the int8 weight v*sg that enters the integer product;
  *  - W4A8 epilogue: out = acc * s_tok[m] * s_ch[n] (exact here, in fp64).
+ *  - dynamic per-token activation quantization: s = amax/127 and
+ *    q = round-half-even(a/s), in fp32 (or_quant_per_token).
  *
  * Arithmetic: floating-point results in fp64 with k ascending; integer
- * results in int64.  Every function is pinned by tests under tests/ against
+ * results in int64; the per-token quantizer in fp32, the precision its codes
+ * are decided in.  Every function is pinned by tests under tests/ against
  * values the pages print, closed forms, invariants and library routines.
  */
 #include <stdint.h>
@@ -204,6 +207,45 @@ void or_w4a8_scale(int64_t count, const int64_t* acc, const int64_t* rows,
                    double* ref) {
   for (int64_t i = 0; i < count; ++i)
     ref[i] = (double)acc[i] * s_tok[rows[i]] * s_ch[cols[i]];
+}
+
+/* Dynamic per-token int8 quantization of the activations that feed W4A8.
+ * vLLM PR #6547 "Enable Dynamic Per Token fp8" (summary): one activation
+ * scale per token, computed at run time from that token's own values;
+ * pytorch/ao PR #1113 "support W4A8 Marlin kernel": the W4A8 activations
+ * are symmetric int8.  The pages print no formula; the reading taken is the
+ * plain symmetric one, every step in fp32 (the precision the quantized code
+ * is decided in):
+ *   amax      = max_k |a[m][k]|            (exact: inputs are fp16/bf16)
+ *   s_tok[m]  = amax / 127                 (one correctly rounded division)
+ *   q[m][k]   = nearest integer to a[m][k] / s_tok[m] (the quotient rounded
+ *               once to fp32, then to an integer, ties to even), within
+ *               [-127, 127]
+ * A row with amax == 0 gets s_tok = 0 and codes 0.  a is fp32 [M][K]
+ * (exact copies of the fp16/bf16 inputs), q int8 [M][K], s_tok fp32 [M]. */
+void or_quant_per_token(int64_t M, int64_t K, const float* a, int8_t* q, float* s_tok) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    const float* row = a + m * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = fabsf(row[k]);
+      if (v > amax) amax = v;
+    }
+    const float s = amax / 127.0f;
+    s_tok[m] = s;
+    for (int64_t k = 0; k < K; ++k) {
+      if (amax == 0.0f) {
+        q[m * K + k] = 0;
+        continue;
+      }
+      const float x = row[k] / s;
+      float r = rintf(x); /* default rounding mode: to nearest, ties to even */
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      q[m * K + k] = (int8_t)r;
+    }
+  }
 }
 
 /* Threads the oracle's parallel loops use (1 when built without OpenMP). */

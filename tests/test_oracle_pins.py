@@ -261,3 +261,125 @@ def test_w4a8_scale_closed_form():
     s_tok = np.array([0.5, 0.25]); s_ch = np.array([2.0, 0.125])
     ref = oracle.w4a8_scale(acc, rows, cols, s_tok, s_ch)
     assert list(ref) == [3 * 0.5 * 0.125, -7 * 0.25 * 2.0, (1 << 20) * 0.25 * 0.125]
+
+
+# --------------------------------------------- per-token int8 quantization ---
+# Reading of vLLM PR #6547 "Enable Dynamic Per Token fp8" (one scale per
+# token, from that token's values) with the symmetric int8 activations of
+# pytorch/ao PR #1113: s = amax / 127, q = round-half-even(a / s), in fp32.
+
+def test_quant_worked_example():
+    # amax 254 -> s = 2 exactly; 127/2 = 63.5 and 65/2 = 32.5 are ties (to
+    # even: 64 and 32), 63.5/2 = 31.75 -> 32, 0.5/2 = 0.25 -> 0
+    a = torch.tensor([[-254.0, 127.0, 63.5, 0.5, 0.0, 65.0, -65.0, 5.0],
+                      [0.0] * 8,
+                      [3.0, -3.0, 1.5, 0.0, 0.0, 0.0, 0.0, 0.0]], dtype=torch.float16)
+    q, s = oracle.quant_per_token(a)
+    assert s.dtype == np.float32 and list(s[:2]) == [2.0, 0.0]
+    assert q[0].tolist() == [-127, 64, 32, 0, 0, 32, -32, 2]
+    assert q[1].tolist() == [0] * 8
+    # amax 3: s = fl32(3/127); 3/s and -3/s round to +-127, 1.5/s = 63.5(1+d) -> 63 or 64
+    assert q[2, 0] == 127 and q[2, 1] == -127 and q[2, 2] in (63, 64)
+
+
+def test_quant_error_bound_and_extremes():
+    g = torch.Generator().manual_seed(3)
+    for dt in (torch.float16, torch.bfloat16):
+        a = torch.randn(24, 1000, generator=g).to(dt)
+        a[5, 17] = 40.0  # an outlier channel
+        q, s = oracle.quant_per_token(a)
+        x = a.double().numpy()
+        amax = np.abs(x).max(axis=1)
+        s64 = s.astype(np.float64)
+        # 127 steps of s reach amax (to the rounding of one fp32 division)
+        assert np.all(np.abs(s64 * 127 - amax) <= amax * 2.0**-23)
+        # every code within half a step of the value, |q| <= 127
+        err = np.abs(q.astype(np.float64) * s64[:, None] - x)
+        assert np.all(err <= s64[:, None] * (0.5 + 1e-5))
+        assert np.abs(q.astype(np.int32)).max() <= 127
+        # the largest |a| of a row maps to +-127 with its sign
+        am = np.abs(x).argmax(axis=1)
+        r = np.arange(x.shape[0])
+        assert np.array_equal(q[r, am].astype(np.int32), 127 * np.sign(x[r, am]).astype(np.int32))
+
+
+def test_quant_symmetry_scaling_rows_independent():
+    g = torch.Generator().manual_seed(4)
+    a = torch.randn(9, 300, generator=g).to(torch.bfloat16)
+    q, s = oracle.quant_per_token(a)
+    qn, sn = oracle.quant_per_token(-a)
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+    for e in (-3, 5):  # powers of two scale s and leave the codes
+        qe, se = oracle.quant_per_token(a.float() * 2.0**e)
+        assert np.array_equal(qe, q) and np.array_equal(se, s * np.float32(2.0**e))
+    for m in (0, 4, 8):  # each row on its own (M = 1) gives the same result
+        q1, s1 = oracle.quant_per_token(a[m:m + 1])
+        assert np.array_equal(q1[0], q[m]) and s1[0] == s[m]
+    qz, sz = oracle.quant_per_token(np.zeros((3, 0), np.float32))
+    assert qz.shape == (3, 0) and list(sz) == [0.0, 0.0, 0.0]
+
+
+def test_quant_brute_force_exact_rationals():
+    """Codes against exact rational arithmetic: the nearest integer to a/s
+    (ties to even) for the returned fp32 s, except where a/s lies so close
+    to a half-integer that rounding the quotient to fp32 may decide it."""
+    from fractions import Fraction
+
+    g = torch.Generator().manual_seed(5)
+    a = (torch.rand(6, 64, generator=g) * 20 - 10).to(torch.float16)
+    a[2, :8] = torch.tensor([2.5, -2.5, 10.0, 0.125, -7.75, 3.0, 1.0, 0.0])
+    q, s = oracle.quant_per_token(a)
+    x = a.float().numpy()
+    checked = 0
+    for m in range(x.shape[0]):
+        sm = Fraction(float(s[m]))
+        for k in range(x.shape[1]):
+            t = Fraction(float(x[m, k])) / sm
+            fl = t.numerator // t.denominator
+            frac = t - fl
+            exact = fl + (1 if frac > Fraction(1, 2) or (frac == Fraction(1, 2) and fl % 2) else 0)
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 1 << 16) * (abs(t) + 1):
+                assert q[m, k] in (fl, fl + 1)
+                continue
+            assert q[m, k] == exact, (m, k, t)
+            checked += 1
+    assert checked > 370
+
+
+def test_quant_feeds_w4a8_within_quantization_error():
+    """Dynamic quantization then W4A8 approximates the fp64 product a x v
+    to within the codes' error: |acc*s_tok - a.v| <= sum_k (s/2)|v_k|."""
+    M, N, K = 5, 48, 256
+    g = torch.Generator().manual_seed(6)
+    a = torch.randn(M, K, generator=g).to(torch.float16)
+    w = w4synth.random_words(w4synth.packed_shape(oracle.NK_EXLLAMA, K, N), g)
+    q, s = oracle.quant_per_token(a)
+    acc = oracle.w4a8(q, w, oracle.NK_EXLLAMA, oracle.INT4, None, -1, K, N)
+    rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    approx = oracle.w4a8_scale(acc.reshape(-1), rows.reshape(-1), cols.reshape(-1),
+                               s.astype(np.float64), np.ones(N)).reshape(M, N)
+    v = np.vectorize(lambda t: oracle.value(int(t), oracle.INT4))(
+        oracle.unpack(w, oracle.NK_EXLLAMA, K, N)).astype(np.float64)
+    exact = a.double().numpy() @ v
+    bound = (s.astype(np.float64)[:, None] / 2) * np.abs(v).sum(axis=0)[None, :] * (1 + 1e-4)
+    assert np.all(np.abs(approx - exact) <= bound)
+    assert np.abs(approx - exact).max() > 0  # the codes are not exact here
+
+
+def test_quant_quotient_rounded_once_in_fp32():
+    """Codes decided by one correctly rounded fp32 division a / s (worked
+    with exact rationals):
+      amax 0.80615234375: s = amax/127 = 0.00634765625 exactly, and
+        0.041259765625 / s = 6.5, 0.092041015625 / s = 14.5 exactly
+        (ties, to even: 6 and 14);
+      amax 3110: s = fl32(3110/127) = 24.488189697265625; 1555 / s is
+        63.5 - 1.87e-6, which rounds to the fp32 value 63.5 (a tie: 64);
+      amax 12.0078125: 6.00390625 / s is 63.5 - 2.25e-6, whose fp32 value
+        63.499996... gives 63.
+    Multiplying by a rounded reciprocal 1/s instead gives 7, 15, 63, 64."""
+    a = torch.tensor([[0.80615234375, 0.041259765625, 0.092041015625],
+                      [3110.0, 1555.0, 0.0],
+                      [12.0078125, 6.00390625, 0.0]], dtype=torch.float16)
+    q, s = oracle.quant_per_token(a)
+    assert s[0] == np.float32(0.00634765625) and s[1] == np.float32(24.488189697265625)
+    assert q.tolist() == [[127, 6, 14], [127, 64, 0], [127, 63, 0]]
