@@ -234,6 +234,24 @@ def run_gpu(args):
     prepack_us = e0.elapsed_time(e1) * 1e3 / 10
     del wq, pre_b
 
+    # per-token int8 quantization of fp16 activations at the largest sweep M
+    # (the step before a W4A8 GEMM; timed beside the step, not inside it):
+    # ROTATE input copies > L2, 2 bytes read + 1 written per element
+    qm = max(M_SWEEP)
+    qa = [w4synth.gen_act16(qm, K, torch.float16, seed=50 + r).to(dev) for r in range(ROTATE)]
+    qo = [(torch.empty(qm, K, dtype=torch.int8, device=dev),
+           torch.empty(qm, dtype=torch.float32, device=dev)) for _ in range(ROTATE)]
+    for r in range(3):
+        w4.quantize_per_token(qa[r % ROTATE], out=qo[r % ROTATE][0], scales=qo[r % ROTATE][1])
+    e0.record(stream)
+    for r in range(20):
+        w4.quantize_per_token(qa[r % ROTATE], out=qo[r % ROTATE][0], scales=qo[r % ROTATE][1])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    quant_us = e0.elapsed_time(e1) * 1e3 / 20
+    quant_gbs = (3 * qm * K + 4 * qm) / (quant_us * 1e-6) / 1e9
+    del qa, qo
+
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -409,6 +427,9 @@ def run_gpu(args):
         "sweep": sweep, "roofline": roofline, "e2e": e2e,
         "prepack": {"us": round(prepack_us, 1),
                     "gbs": round(2 * K * N // 2 / (prepack_us * 1e-6) / 1e9, 1)},
+        "quantize": {"kernel": "quant_per_token_kernel<fp16>", "M": qm, "K": K,
+                     "us": round(quant_us, 2), "gbs": round(quant_gbs, 1), "bound": "hbm",
+                     "frac": round(quant_gbs / pk["hbm"], 3)},
         "gpu_launches": launches_per_step(w4) * args.steps,
         "clocks": clk,
     }
@@ -440,6 +461,22 @@ def run_single(args):
     print(json.dumps({"single_M": M, "launches": args.warmup + args.steps, "status": st}))
     if st != w4.OK:
         sys.exit(1)
+
+
+def run_quant_single(args):
+    """Per-token int8 quantization of fp16 activations [M = args.quant_single,
+    K], eager launches: the small case for ncu captures (one input copy)."""
+    import int4_weight_mixed_gb300 as w4
+
+    dev = torch.device("cuda", 0)
+    M = args.quant_single
+    a = w4synth.gen_act16(M, K, torch.float16, seed=50).to(dev)
+    q = torch.empty(M, K, dtype=torch.int8, device=dev)
+    s = torch.empty(M, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        w4.quantize_per_token(a, out=q, scales=s)
+    torch.cuda.synchronize()
+    print(json.dumps({"quant_M": M, "K": K, "launches": args.warmup + args.steps}))
 
 
 def oracle_sample(rows_per_m, cols, seed=0):
@@ -519,6 +556,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--single", type=int, default=0, help="run only the GEMM with this M")
     ap.add_argument("--schedule", type=int, default=-1)
+    ap.add_argument("--quant-single", type=int, default=0,
+                    help="run only the per-token quantization of this many rows")
     ap.add_argument("--eager", action="store_true",
                     help="launch the step without CUDA graphs (profiler launch lists)")
     args = ap.parse_args()
@@ -528,6 +567,8 @@ def main():
         run_reference(args)
     elif args.single:
         run_single(args)
+    elif args.quant_single:
+        run_quant_single(args)
     else:
         run_gpu(args)
 

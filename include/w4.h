@@ -193,6 +193,27 @@ w4_status w4_gemm_noalloc(const void* a, int a_type, int64_t M, int64_t K, const
                           const void* b_zeros, int64_t group_size, const float* a_token_scales,
                           const float* ch_scales, void* out, int out_type, void* stream);
 
+/* Dynamic per-token int8 quantization of activations for W4A8: the step
+ * that makes the `a` (W4_S8) and `a_token_scales` arguments of w4_gemm
+ * from fp16/bf16 activations ([PT]: one activation scale per token,
+ * computed at run time from that token's values; [QQQ]: symmetric int8
+ * activations).  For every row m of a [M,K] (a_type W4_F16 or W4_BF16):
+ *   s_tok[m]  = max_k |a[m][k]| / 127, in fp32 (one rounding);
+ *   a_q[m][k] = a[m][k] / s_tok[m] rounded once to fp32, then to the
+ *               nearest integer, ties to even (always within [-127,127]).
+ * A row of zeros gets s_tok 0 and codes 0, so the W4A8 product of that row
+ * is 0.  Values must be finite (a row holding Inf or NaN gets unspecified
+ * codes and scale).
+ *   a      [M,K] device, contiguous rows; 16-byte aligned with K % 8 == 0
+ *          for the vectorised path (any other K or alignment runs a
+ *          slower element-wise path with the same results).
+ *   a_q    [M,K] int8 device output; s_tok [M] fp32 device output.
+ * M == 0 is a no-op; K == 0 sets every s_tok to 0.  Errors:
+ * INVALID_ARGUMENT (negative size, bad a_type, a null pointer that the
+ * sizes need), UNSUPPORTED (M > 2^31 - 1), CUDA. */
+w4_status w4_quantize_per_token(const void* a, int a_type, int64_t M, int64_t K, int8_t* a_q,
+                                float* s_tok, void* stream);
+
 /* Static text for a status code; message of the last failed call on this
  * host thread ("" when none). */
 const char* w4_status_string(int status);

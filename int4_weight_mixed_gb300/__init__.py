@@ -82,6 +82,8 @@ def load():
         lib.w4_schedule_name.restype = ctypes.c_char_p
         lib.w4_default_schedule.argtypes = [i64, i64, i64, i32, i64]
         lib.w4_default_schedule.restype = i32
+        lib.w4_quantize_per_token.argtypes = [p, i32, i64, i64, p, p, p]
+        lib.w4_quantize_per_token.restype = i32
         lib.w4_check_status.argtypes = [p, sz, p]
         lib.w4_check_status.restype = i32
         lib.w4_status_string.argtypes = [i32]
@@ -199,6 +201,25 @@ def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
                         ws.numel(), _stream(a.device), schedule)
     _check(st, "w4_gemm")
     return out
+
+
+def quantize_per_token(a: torch.Tensor, out: torch.Tensor | None = None,
+                       scales: torch.Tensor | None = None):
+    """w4_quantize_per_token: fp16/bf16 activations [M, K] -> (int8 codes
+    [M, K], fp32 per-token scales [M]), the `a` and `token_scales` of a
+    W4A8 gemm."""
+    lib = load()
+    assert a.dim() == 2 and a.is_cuda and a.is_contiguous()
+    M, K = a.shape
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.int8, device=a.device)
+    if scales is None:
+        scales = torch.empty(M, dtype=torch.float32, device=a.device)
+    assert out.dtype == torch.int8 and out.is_contiguous() and out.shape == (M, K)
+    assert scales.dtype == torch.float32 and scales.is_contiguous() and scales.numel() == M
+    _check(lib.w4_quantize_per_token(_ptr(a), _DTYPE_CODE[a.dtype], M, K, _ptr(out), _ptr(scales),
+                                     _stream(a.device)), "w4_quantize_per_token")
+    return out, scales
 
 
 def check_status(ws: torch.Tensor) -> int:

@@ -633,6 +633,19 @@ w4_status w4_gemm(const void* a, int a_type, int64_t M, int64_t K, const void* b
                     workspace_bytes, stream, -1);
 }
 
+w4_status w4_quantize_per_token(const void* a, int a_type, int64_t M, int64_t K, int8_t* a_q,
+                                float* s_tok, void* stream) {
+  if (M < 0 || K < 0) return fail(W4_ERR_INVALID_ARGUMENT, "negative size");
+  if (a_type != W4_F16 && a_type != W4_BF16)
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16 or W4_BF16");
+  if (M == 0) return W4_OK;
+  if (!s_tok || (K > 0 && (!a || !a_q))) return fail(W4_ERR_INVALID_ARGUMENT, "null pointer");
+  if (M > 0x7fffffff) return fail(W4_ERR_UNSUPPORTED, "M above 2^31 - 1");
+  cudaError_t e = launch_quant_per_token(a_type == W4_BF16, a, M, K, a_q, s_tok,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4_OK : cuda_fail(e, "quantize launch");
+}
+
 w4_status w4_check_status(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < kWsHeader)
     return fail(W4_ERR_WORKSPACE, "workspace is null or smaller than its header");

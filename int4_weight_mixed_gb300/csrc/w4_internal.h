@@ -147,6 +147,8 @@ cudaError_t launch_unprepack(const uint8_t* packed, int wtype, int layout, int64
                              int64_t N, int32_t* w_q, cudaStream_t s);
 cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_t s);
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s);
+cudaError_t launch_quant_per_token(bool bf16, const void* a, int64_t M, int64_t K, int8_t* q,
+                                   float* s_tok, cudaStream_t s);
 cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                       const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
 cudaError_t launch_dk(const DkPlan& plan, const void* a, const TcArgs& args, cudaStream_t s);

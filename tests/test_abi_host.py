@@ -122,3 +122,17 @@ def test_prepack_argument_errors(lib):
     assert lib.w4_prepack_B(1, 0, 0, 60, 8, 1, None) == E
     assert lib.w4_prepack_B(1, 0, 0, 96, 8, 1, None) == w4.ERR_UNSUPPORTED
     assert lib.w4_unprepack_B(1, 0, 0, 64, 0, 1, None) == E
+
+
+def test_quantize_argument_errors(lib):
+    E = w4.ERR_INVALID_ARGUMENT
+    q = lib.w4_quantize_per_token
+    assert q(1, 0, -1, 64, 1, 1, None) == E            # negative M
+    assert q(1, 0, 4, -8, 1, 1, None) == E             # negative K
+    assert q(1, 2, 4, 64, 1, 1, None) == E             # int8 input
+    assert q(1, 3, 4, 64, 1, 1, None) == E             # int32 input
+    assert q(None, 0, 4, 64, 1, 1, None) == E          # activations needed
+    assert q(1, 1, 4, 64, None, 1, None) == E          # codes needed
+    assert q(1, 1, 4, 0, None, None, None) == E        # scales needed even at K == 0
+    assert q(None, 0, 0, 64, None, None, None) == w4.OK  # M == 0: nothing launched
+    assert q(1, 0, 1 << 31, 64, 1, 1, None) == w4.ERR_UNSUPPORTED

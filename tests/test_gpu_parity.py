@@ -430,3 +430,92 @@ def test_back_to_back_calls(gpu_lib):
         assert np.array_equal(got.cpu().numpy().astype(np.int64), ref)
     ref, absref = oracle_w4a16(d5)
     assert_within(out5.cpu().double().numpy(), ref, absref, "bf16", "back to back W4A16")
+
+
+# ------------------------------------------- per-token int8 quantization ---
+# Codes and scales are decided in fp32 on both sides: bit-exact.
+
+def _quant_gpu(w4, a_dev):
+    q, s = w4.quantize_per_token(a_dev)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+def _assert_quant_equal(q, s, rq, rs, what):
+    assert np.array_equal(s.view(np.int32), rs.view(np.int32)), f"{what}: scales differ"
+    bad = np.argwhere(q != rq)
+    assert bad.size == 0, f"{what}: {len(bad)} codes differ, first {bad[:3].tolist()}"
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,K", [(1, 21760), (16, 21760), (37, 4096), (5, 72), (3, 13), (2, 8),
+                                 (0, 64), (4, 0), (1024, 21760)])
+def test_quantize_per_token_bit_exact(gpu_lib, M, K, dt):
+    w4 = gpu_lib
+    a = w4synth.gen_act16(M, K, dt, seed=M + K)
+    q, s = _quant_gpu(w4, a.to(DEV))
+    rq, rs = oracle.quant_per_token(a)
+    _assert_quant_equal(q, s, rq, rs, f"M={M} K={K} {fmt(dt)}")
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_quantize_special_rows(gpu_lib, dt, aligned):
+    """Zero rows, one outlier, equal values, exact ties and near-ties,
+    the largest and the smallest magnitudes of the type, on the vectorised
+    path and (a view one element off 16-byte alignment) the element-wise
+    one."""
+    w4 = gpu_lib
+    K = 264
+    a = w4synth.gen_act16(12, K, dt, seed=21).float()
+    a[0] = 0.0
+    a[1] = 0.0
+    a[1, 100] = -3.0
+    a[2] = 1.5
+    a[3, :3] = torch.tensor([0.80615234375, 0.041259765625, 0.092041015625])
+    a[4, :2] = torch.tensor([3110.0, 1555.0])
+    a[5, :2] = torch.tensor([12.0078125, 6.00390625])
+    a[6, :8] = torch.tensor([-254.0, 127.0, 63.5, 0.5, 0.0, 65.0, -65.0, 5.0])
+    big = 65504.0 if dt == torch.float16 else 3.0e38
+    a[7] *= big / a[7].abs().max()
+    small = 6.0e-5 if dt == torch.float16 else 1.0e-38
+    a[8] *= small / a[8].abs().max()
+    a[9, ::2] = -a[9, ::2].abs()
+    a[10] = torch.arange(K, dtype=torch.float32) - K / 2
+    a = a.to(dt)
+    if aligned:
+        a_dev = a.to(DEV)
+    else:
+        buf = torch.zeros(a.numel() + 1, dtype=dt, device=DEV)
+        buf[1:] = a.reshape(-1).to(DEV)
+        a_dev = buf[1:].view(a.shape)
+        assert a_dev.data_ptr() % 16 != 0
+    q, s = _quant_gpu(w4, a_dev)
+    rq, rs = oracle.quant_per_token(a)
+    _assert_quant_equal(q, s, rq, rs, f"special rows {fmt(dt)} aligned={aligned}")
+    assert s[0] == 0 and not q[0].any()
+
+
+@pytest.mark.parametrize("M", [5, 300])
+def test_quantize_feeds_w4a8(gpu_lib, M):
+    """fp16 activations -> GPU per-token codes -> GPU W4A8 GEMM, against the
+    oracle's codes through the oracle's W4A8: int32 bit-exact, fp16 within
+    one ulp."""
+    w4 = gpu_lib
+    N, K = 384, 2048
+    e = w4synth.gen_w4a8(M, N, K, group_size=-1, seed=11)
+    a16 = w4synth.gen_act16(M, K, torch.float16, seed=12)
+    q, s = w4.quantize_per_token(a16.to(DEV))
+    rq, rs = oracle.quant_per_token(a16)
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], K, N)
+    acc = w4.gemm(q, b, e["wtype"], N, group_size=-1, out_dtype=torch.int32)
+    out = w4.gemm(q, b, e["wtype"], N, group_size=-1, token_scales=s,
+                  channel_scales=e["s_ch"].to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), rq)
+    ref = oracle.w4a8(rq, e["w"], e["layout"], e["wtype"], None, -1, K, N)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref)
+    rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    refo = oracle.w4a8_scale(ref.reshape(-1), rows.reshape(-1), cols.reshape(-1),
+                             rs.astype(np.float64), e["s_ch"])
+    assert_fp16_within_ulp(out.cpu().double().numpy().reshape(-1), refo, f"quantized W4A8 M={M}")

@@ -101,6 +101,12 @@ def gen_w4a8(M: int, N: int, K: int, group_size: int = -1, layout: int = NK_EXLL
                 wtype=INT4, group_size=group_size)
 
 
+def gen_act16(M: int, K: int, dtype=torch.float16, seed: int = 0) -> torch.Tensor:
+    """Activations [M, K] ~ N(0, 1) in fp16 / bf16 (the W4A16 activation
+    distribution): the input of the per-token int8 quantization."""
+    return torch.randn(M, K, generator=_gen(seed)).to(dtype)
+
+
 def tiny_w4a16(seed: int = 0) -> dict:
     """The tiny W4A16 case: fp16 [16,512] x uint4b8 [512,256], g128."""
     return gen_w4a16(16, 256, 512, act_dtype=torch.float16, wtype=UINT4B8,
