@@ -23,6 +23,12 @@ What each function computes, and the page it follows:
   "support W4A8 Marlin kernel": int8 x int4 (per-channel) or int8 x
   (int4 * group scale) (per-group), exact integer accumulator, then
   acc * s_tok[m] * s_ch[n].
+* ``e4m3_decode`` / ``e4m3_encode`` / ``quant_per_token_fp8`` / ``w4a8_fp8``
+  — the fp8 activations of vLLM PR #9855 ("including fp8 activations"),
+  read as OCP E4M3 (bias 7, largest value 448, no infinity): decoding,
+  round-to-nearest-even encoding saturated at 448, per-token scales
+  amax/448, and the exact fp64 product of decoded activations with int4
+  weights.
 * ``quant_per_token`` — vLLM PR #6547 "Enable Dynamic Per Token fp8" (one
   activation scale per token, computed from that token at run time) with
   the symmetric int8 activations of pytorch/ao PR #1113: s = amax/127 and
@@ -84,6 +90,10 @@ def _load():
             lib.or_w4a8_elems.argtypes = [i64, i64, i64, p, p, i32, i32, p, i64, i64, p, p, p]
             lib.or_w4a8_scale.argtypes = [i64, p, p, p, p, p, p]
             lib.or_quant_per_token.argtypes = [i64, i64, p, p, p]
+            lib.or_e4m3_decode_n.argtypes = [i64, p, p]
+            lib.or_e4m3_encode_n.argtypes = [i64, p, p]
+            lib.or_quant_per_token_fp8.argtypes = [i64, i64, p, p, p]
+            lib.or_w4a8_fp8.argtypes = [i64, i64, i64, p, p, i32, i32, p, p]
             lib.or_num_threads.restype = i32
             _lib = lib
     return _lib
@@ -225,3 +235,51 @@ def quant_per_token(a):
     s = np.empty(M, np.float32)
     _load().or_quant_per_token(M, K, _ptr(a), _ptr(q), _ptr(s))
     return q, s
+
+
+def _f32(a):
+    try:
+        import torch
+
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().to(torch.float32).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """fp64 values of E4M3 codes (uint8 array of any shape; NaN for 0x7F/0xFF)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, np.float64)
+    _load().or_e4m3_decode_n(c.size, _ptr(c), _ptr(out))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (uint8) of finite fp32 values, nearest-even, saturated at 448."""
+    x = _f32(x)
+    out = np.empty(x.shape, np.uint8)
+    _load().or_e4m3_encode_n(x.size, _ptr(x), _ptr(out))
+    return out
+
+
+def quant_per_token_fp8(a):
+    """Per-token E4M3 codes [M, K] (uint8) and fp32 scales [M]."""
+    a = _f32(a)
+    M, K = a.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty(M, np.float32)
+    _load().or_quant_per_token_fp8(M, K, _ptr(a), _ptr(q), _ptr(s))
+    return q, s
+
+
+def w4a8_fp8(a_codes, w, layout, wtype, K, N):
+    """Exact fp64 sum_k decode(a) * v(q) [M, N] and the sum of |terms|."""
+    a = np.ascontiguousarray(np.asarray(a_codes, dtype=np.uint8))
+    M = a.shape[0]
+    w = _np(w, np.int32)
+    ref = np.empty((M, N), np.float64)
+    absref = np.empty((M, N), np.float64)
+    _load().or_w4a8_fp8(M, N, K, _ptr(a), _ptr(w), layout, wtype, _ptr(ref), _ptr(absref))
+    return ref, absref

@@ -36,6 +36,9 @@
  *  - W4A8 epilogue: out = acc * s_tok[m] * s_ch[n] (exact here, in fp64).
  *  - dynamic per-token activation quantization: s = amax/127 and
  *    q = round-half-even(a/s), in fp32 (or_quant_per_token).
+ *  - fp8 activations are OCP E4M3 (bias 7, largest value 448, no
+ *    infinity), encoded to nearest-even and saturated at 448, with
+ *    per-token scales amax/448; W4A8-fp8 is per-channel.
  *
  * Arithmetic: floating-point results in fp64 with k ascending; integer
  * results in int64; the per-token quantizer in fp32, the precision its codes
@@ -246,6 +249,98 @@ void or_quant_per_token(int64_t M, int64_t K, const float* a, int8_t* q, float* 
       q[m * K + k] = (int8_t)r;
     }
   }
+}
+
+/* ---- fp8 activations (vLLM PR #9855 "[Kernel] Initial Machete W4A8
+ * support + Refactors": QQQ-style W4A8 "including fp8 activations", with an
+ * int4 -> fp8 weight converter).  The pages do not define the fp8 format;
+ * the reading taken is the E4M3 format of the OCP 8-bit floating point
+ * specification: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 holds the subnormals m/8 * 2^-6; the all-ones pattern
+ * S.1111.111 is NaN and there is no infinity, so the largest value is
+ * 1.75 * 2^8 = 448.  Every int4 weight value -8..7 is exact in it. */
+
+/* Value of an E4M3 code (NaN for S.1111.111). */
+double or_e4m3_decode(int code) {
+  const int sign = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* E4M3 code of a finite fp32 value: the nearest representable value, ties
+ * to the even mantissa, magnitudes at or above 448 saturated to 448 (the
+ * "satfinite" reading: rounding first, then clamping to the largest finite
+ * value, which gives 448 for every magnitude >= 448). */
+int or_e4m3_encode(float x) {
+  const int sign = signbit(x) ? 0x80 : 0;
+  const float a = fabsf(x);
+  if (a >= 448.0f) return sign | 0x7E;
+  if (a < 0x1p-6f) {                       /* subnormal range: steps of 2^-9 */
+    const int q = (int)rintf(a * 512.0f);  /* exact scaling; 8 becomes 0x08 */
+    return sign | q;
+  }
+  int e;
+  const float f = frexpf(a, &e);           /* a = f * 2^e, f in [0.5, 1) */
+  e -= 1;                                  /* a = (2f) * 2^e, 2f in [1, 2) */
+  int m = (int)rintf((2.0f * f - 1.0f) * 8.0f); /* exact before the rounding */
+  if (m == 8) {
+    m = 0;
+    e += 1;
+  }
+  return sign | ((e + 7) << 3) | m;
+}
+
+void or_e4m3_decode_n(int64_t n, const uint8_t* codes, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = or_e4m3_decode(codes[i]);
+}
+void or_e4m3_encode_n(int64_t n, const float* x, uint8_t* codes) {
+  for (int64_t i = 0; i < n; ++i) codes[i] = (uint8_t)or_e4m3_encode(x[i]);
+}
+
+/* Dynamic per-token fp8 quantization (vLLM PR #6547 "Enable Dynamic Per
+ * Token fp8": one scale per token from that token's values).  Reading, in
+ * fp32 as for the int8 codes: s_tok = amax / 448, and each code is the E4M3
+ * encoding of the quotient a / s_tok rounded once to fp32.  A zero row gets
+ * s_tok = 0 and codes 0. */
+void or_quant_per_token_fp8(int64_t M, int64_t K, const float* a, uint8_t* q, float* s_tok) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    const float* row = a + m * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = fabsf(row[k]);
+      if (v > amax) amax = v;
+    }
+    const float s = amax / 448.0f;
+    s_tok[m] = s;
+    for (int64_t k = 0; k < K; ++k)
+      q[m * K + k] = amax == 0.0f ? 0 : (uint8_t)or_e4m3_encode(row[k] / s);
+  }
+}
+
+/* W4A8 with fp8 activations, per-channel: ref[m][n] = sum_k
+ * decode(a[m][k]) * v(q[k][n]) in fp64 with k ascending (every product and
+ * partial sum is a multiple of 2^-9 below 2^44, so the sum is exact), and
+ * absref the sum of |terms|.  The output is ref * s_tok[m] * s_ch[n]. */
+void or_w4a8_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* a, const int32_t* w, int layout,
+                 int wtype, double* ref, double* absref) {
+  double lut[256];
+  for (int c = 0; c < 256; ++c) lut[c] = or_e4m3_decode(c);
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, aacc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double t = lut[a[m * K + k]] * (double)or_value(or_nibble(w, layout, K, N, k, n), wtype);
+        acc += t;
+        aacc += fabs(t);
+      }
+      ref[m * N + n] = acc;
+      absref[m * N + n] = aacc;
+    }
 }
 
 /* Threads the oracle's parallel loops use (1 when built without OpenMP). */

@@ -383,3 +383,107 @@ def test_quant_quotient_rounded_once_in_fp32():
     q, s = oracle.quant_per_token(a)
     assert s[0] == np.float32(0.00634765625) and s[1] == np.float32(24.488189697265625)
     assert q.tolist() == [[127, 6, 14], [127, 64, 0], [127, 63, 0]]
+
+
+# ------------------------------------------------- fp8 (E4M3) activations ---
+# vLLM PR #9855: QQQ-style W4A8 "including fp8 activations"; the format is
+# read as OCP E4M3 (bias 7, subnormals m/8 * 2^-6, S.1111.111 NaN, max 448).
+
+def test_e4m3_decode_worked_codes():
+    # values worked by hand from the format definition
+    table = {0x00: 0.0, 0x01: 2.0**-9, 0x07: 7 * 2.0**-9, 0x08: 2.0**-6, 0x30: 0.5, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x4C: 6.0, 0x50: 8.0, 0x77: 240.0,
+             0x78: 256.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xC0: -2.0, 0xFE: -448.0}
+    got = oracle.e4m3_decode(np.array(list(table), dtype=np.uint8))
+    assert list(got) == list(table.values())
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    assert np.signbit(oracle.e4m3_decode(np.array([0x80], np.uint8)))[0]
+
+
+def test_e4m3_decode_matches_torch_float8():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(ours)
+    assert np.array_equal(ours[ok], lib[ok])
+
+
+def test_e4m3_encode_ties_saturation_round_trip():
+    x = np.float32([1.0625, 1.1875, 3.125, 3.25, 0.5 * 2**-9, 1.5 * 2**-9, 7.5 * 2**-9, 448, 464,
+                    470, 500, -1e30, -0.0, 0.0])
+    # ties go to the even mantissa: 1.0625 -> 1.0 (m=0), 1.1875 -> 1.25 (m=2),
+    # 3.125 (between 3.0 = 1.5*2 and 3.25 = 1.625*2) -> 3.0 (m=4); 3.25 is exact
+    # (0x45); subnormal ties 0.5 and 1.5 steps of 2^-9 -> 0 and 2 steps;
+    # 7.5 * 2^-9 -> 2^-6 (0x08); 448 and above saturate to 448 (470 would round
+    # to the NaN pattern 0x7F without the saturation)
+    got = oracle.e4m3_encode(x).tolist()
+    assert got == [0x38, 0x3A, 0x44, 0x45, 0x00, 0x02, 0x08, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x80, 0x00]
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(finite).astype(np.float32)), finite)
+
+
+def test_e4m3_encode_matches_torch_in_range_and_is_nearest():
+    g = torch.Generator().manual_seed(8)
+    x = torch.cat([torch.randn(20000, generator=g) * 40, torch.randn(20000, generator=g) * 0.01,
+                   (torch.rand(5000, generator=g) - 0.5) * 895])
+    x = x[x.abs() < 448]
+    ours = oracle.e4m3_encode(x)
+    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, lib)
+    # nearest: no finite code is closer than the chosen one
+    vals = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    finite = vals[~np.isnan(vals)]
+    xs = x.double().numpy()[:500]
+    best = np.abs(finite[None, :] - xs[:, None]).min(axis=1)
+    assert np.array_equal(np.abs(oracle.e4m3_decode(ours[:500]) - xs), best)
+
+
+def test_quant_fp8_scale_bound_and_invariants():
+    g = torch.Generator().manual_seed(9)
+    a = torch.randn(16, 700, generator=g).to(torch.bfloat16)
+    a[3] = 0.0
+    q, s = oracle.quant_per_token_fp8(a)
+    x = a.double().numpy()
+    v = oracle.e4m3_decode(q)
+    amax = np.abs(x).max(axis=1)
+    s64 = s.astype(np.float64)
+    assert s[3] == 0 and not q[3].any()
+    live = amax > 0
+    assert np.all(np.abs(s64[live] * 448 - amax[live]) <= amax[live] * 2.0**-23)
+    # each code within half a step of E4M3 at its magnitude (relative 2^-4, or
+    # 2^-10 absolute in the subnormal range), on the scale of the row
+    t = x[live] / s64[live, None]
+    step = np.where(np.abs(t) >= 2.0**-6, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(t), 2.0**-6))) - 3),
+                    2.0**-9)
+    assert np.all(np.abs(v[live] - t) <= step / 2 * (1 + 1e-5) + 1e-12)
+    # the largest |a| of a row maps to +-448
+    r = np.flatnonzero(live)
+    am = np.abs(x[r]).argmax(axis=1)
+    assert np.array_equal(np.abs(v[r, am]), np.full(r.size, 448.0))
+    qn, sn = oracle.quant_per_token_fp8(-a)
+    assert np.array_equal(oracle.e4m3_decode(qn)[live], -v[live]) and np.array_equal(sn, s)
+    q2, s2 = oracle.quant_per_token_fp8(a.float() * 8.0)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s * np.float32(8.0))
+
+
+def test_w4a8_fp8_exact_matmul_and_bound():
+    M, N, K = 6, 40, 384
+    g = torch.Generator().manual_seed(10)
+    a = torch.randn(M, K, generator=g).to(torch.float16)
+    w = w4synth.random_words(w4synth.packed_shape(oracle.NK_EXLLAMA, K, N), g)
+    q, s = oracle.quant_per_token_fp8(a)
+    ref, absref = oracle.w4a8_fp8(q, w, oracle.NK_EXLLAMA, oracle.INT4, K, N)
+    v = np.vectorize(lambda t: oracle.value(int(t), oracle.INT4))(
+        oracle.unpack(w, oracle.NK_EXLLAMA, K, N)).astype(np.float64)
+    dec = oracle.e4m3_decode(q)
+    assert np.array_equal(ref, dec @ v)          # exact: multiples of 2^-9 below 2^44
+    assert np.array_equal(absref, np.abs(dec) @ np.abs(v))
+    # uint4b8 weights hold the same values as int4 once each nibble's top bit flips
+    flipped = (w.numpy().view(np.uint32) ^ np.uint32(0x88888888)).view(np.int32)
+    assert np.array_equal(oracle.w4a8_fp8(q, flipped, oracle.NK_EXLLAMA, oracle.UINT4B8, K, N)[0], ref)
+    # dequantized, the product stays within the codes' error of the fp64 a x v
+    exact = a.double().numpy() @ v
+    err = np.abs(ref * s.astype(np.float64)[:, None] - exact)
+    bound = (np.abs(a.double().numpy()) * 2.0**-4 + s.astype(np.float64)[:, None] * 2.0**-10) @ np.abs(v)
+    assert np.all(err <= bound)
