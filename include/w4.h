@@ -33,6 +33,13 @@
  *   - All matrices are dense, contiguous, row-major, in DEVICE memory owned
  *     by the caller.  The library allocates no memory and keeps no pointer
  *     after a call returns.
+ *   - Every array must be aligned to its element size (2 bytes for fp16 /
+ *     bf16, 4 for fp32 / int32), and the prepacked weights and packed int32
+ *     words to 4 bytes; a misaligned pointer is W4_ERR_INVALID_ARGUMENT.
+ *     The tensor-core and streamed GEMM schedules also want a, b_packed,
+ *     b_scales and b_zeros 16-byte aligned: without that the default
+ *     heuristic runs the CUDA-core schedule, and an explicit schedule
+ *     returns W4_ERR_UNSUPPORTED.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued on it; calls return after enqueue.
  *   - Argument errors are reported synchronously, before anything is

@@ -312,6 +312,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned_to(const void* p, uintptr_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
 
 struct Problem {
   int mode;
@@ -368,6 +369,16 @@ w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* 
     if (K > 0 && (!a || !b_packed))
       return fail(W4_ERR_INVALID_ARGUMENT, "a and b_packed are required");
   }
+  // every kernel reads or writes each array at least element by element;
+  // the prepacked weights as 32-bit words
+  const uintptr_t asz = a_type == W4_S8 ? 1 : 2;
+  const uintptr_t osz = (pr.mode == kW4A8 && out_type == W4_S32) ? 4 : 2;
+  const uintptr_t ssz = pr.mode == kW4A8 ? 1 : 2;
+  if (!aligned_to(a, asz) || !aligned_to(out, osz) || !aligned_to(b_packed, 4) ||
+      !aligned_to(b_scales, ssz) || !aligned_to(b_zeros, 2) || !aligned_to(s_tok, 4) ||
+      !aligned_to(s_ch, 4))
+    return fail(W4_ERR_INVALID_ARGUMENT,
+                "a pointer is not aligned to its element size (b_packed: 4 bytes)");
   if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
   if (K > 0 && gs % kStageK != 0)
     return fail(W4_ERR_UNSUPPORTED, "group_size must be a multiple of 64 (or K)");
@@ -408,6 +419,8 @@ w4_status w4_prepack_B(const int32_t* w_q, int wtype, int in_layout, int64_t K, 
   if (K <= 0 || N <= 0 || K % 8 != 0)
     return fail(W4_ERR_INVALID_ARGUMENT, "K and N must be positive, K a multiple of 8");
   if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
+  if (!aligned_to(w_q, 4) || !aligned_to(b_packed, 4))
+    return fail(W4_ERR_INVALID_ARGUMENT, "w_q and b_packed must be 4-byte aligned");
   cudaError_t e = launch_prepack(w_q, wtype, in_layout, K, N, static_cast<uint8_t*>(b_packed),
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "prepack launch");
@@ -422,6 +435,8 @@ w4_status w4_unprepack_B(const void* b_packed, int wtype, int out_layout, int64_
   if (K <= 0 || N <= 0 || K % 8 != 0)
     return fail(W4_ERR_INVALID_ARGUMENT, "K and N must be positive, K a multiple of 8");
   if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
+  if (!aligned_to(w_q, 4) || !aligned_to(b_packed, 4))
+    return fail(W4_ERR_INVALID_ARGUMENT, "w_q and b_packed must be 4-byte aligned");
   cudaError_t e = launch_unprepack(static_cast<const uint8_t*>(b_packed), wtype, out_layout, K,
                                    N, w_q, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "unprepack launch");
@@ -640,6 +655,8 @@ w4_status w4_quantize_per_token(const void* a, int a_type, int64_t M, int64_t K,
     return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16 or W4_BF16");
   if (M == 0) return W4_OK;
   if (!s_tok || (K > 0 && (!a || !a_q))) return fail(W4_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned_to(a, 2) || !aligned_to(s_tok, 4))
+    return fail(W4_ERR_INVALID_ARGUMENT, "a and s_tok must be aligned to their element size");
   if (M > 0x7fffffff) return fail(W4_ERR_UNSUPPORTED, "M above 2^31 - 1");
   cudaError_t e = launch_quant_per_token(a_type == W4_BF16, a, M, K, a_q, s_tok,
                                          static_cast<cudaStream_t>(stream));

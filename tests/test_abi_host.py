@@ -65,8 +65,9 @@ def test_workspace_size(lib):
 
 
 def _gemm(lib, **kw):
-    args = dict(a=1, a_type=0, M=4, K=128, b=1, wtype=0, N=128, s=1, st=0, z=None, gs=128,
-                tok=None, ch=None, out=1, ot=0, ws=1, wsb=1 << 20, stream=None, sched=-1)
+    # placeholder addresses (never dereferenced: every case fails on the host)
+    args = dict(a=256, a_type=0, M=4, K=128, b=256, wtype=0, N=128, s=256, st=0, z=None, gs=128,
+                tok=None, ch=None, out=256, ot=0, ws=256, wsb=1 << 20, stream=None, sched=-1)
     args.update(kw)
     return lib.w4_gemm_ex(args["a"], args["a_type"], args["M"], args["K"], args["b"],
                           args["wtype"], args["N"], args["s"], args["st"], args["z"], args["gs"],
@@ -135,4 +136,27 @@ def test_quantize_argument_errors(lib):
     assert q(1, 1, 4, 64, None, 1, None) == E          # codes needed
     assert q(1, 1, 4, 0, None, None, None) == E        # scales needed even at K == 0
     assert q(None, 0, 0, 64, None, None, None) == w4.OK  # M == 0: nothing launched
-    assert q(1, 0, 1 << 31, 64, 1, 1, None) == w4.ERR_UNSUPPORTED
+    assert q(256, 0, 1 << 31, 64, 256, 256, None) == w4.ERR_UNSUPPORTED
+
+
+def test_misaligned_pointers_rejected_on_host(lib):
+    """Every array must be aligned to its element size (the prepacked
+    weights to 4 bytes), else INVALID_ARGUMENT before anything runs."""
+    E = w4.ERR_INVALID_ARGUMENT
+    assert _gemm(lib, a=257) == E                    # fp16 activations
+    assert _gemm(lib, out=259) == E                  # fp16 output
+    assert _gemm(lib, b=258) == E                    # prepacked words
+    assert _gemm(lib, s=255) == E                    # fp16 scales
+    assert _gemm(lib, z=257, wtype=1) == E           # fp16 zero-points
+    w4a8 = dict(a_type=2, wtype=2, s=None, gs=-1, st=2)
+    assert _gemm(lib, **w4a8, ot=0, tok=258, ch=256) == E   # fp32 token scales
+    assert _gemm(lib, **w4a8, ot=0, tok=256, ch=254) == E   # fp32 channel scales
+    assert _gemm(lib, **w4a8, ot=3, out=258) == E            # int32 output
+    # int8 activations need no alignment: the call goes on to fail on its
+    # (too small) workspace, still on the host
+    assert _gemm(lib, **w4a8, ot=3, a=257, wsb=16) == w4.ERR_WORKSPACE
+    assert lib.w4_prepack_B(258, 0, 0, 64, 8, 256, None) == E
+    assert lib.w4_prepack_B(256, 0, 0, 64, 8, 258, None) == E
+    assert lib.w4_unprepack_B(256, 0, 0, 64, 8, 258, None) == E
+    assert lib.w4_quantize_per_token(257, 0, 4, 64, 256, 256, None) == E
+    assert lib.w4_quantize_per_token(256, 0, 4, 64, 256, 258, None) == E
