@@ -160,3 +160,33 @@ def test_misaligned_pointers_rejected_on_host(lib):
     assert lib.w4_unprepack_B(256, 0, 0, 64, 8, 258, None) == E
     assert lib.w4_quantize_per_token(257, 0, 4, 64, 256, 256, None) == E
     assert lib.w4_quantize_per_token(256, 0, 4, 64, 256, 258, None) == E
+
+
+def test_every_schedule_fits_in_the_published_workspace(lib):
+    """w4_gemm_workspace_size covers what every schedule that can run a
+    problem asks for (the need is read from the WORKSPACE error that a too
+    small workspace returns on the host, before anything is launched)."""
+    import re
+
+    shapes = [  # (M, N, K, a_type, group_size)
+        (1, 8192, 21760, 2, -1), (8, 8192, 21760, 2, 128), (16, 8192, 21760, 2, -1),
+        (32, 8192, 21760, 2, -1), (128, 8192, 21760, 2, -1), (1024, 8192, 21760, 2, 128),
+        (2048, 8192, 21760, 2, 128), (1, 4096, 4096, 1, 128), (16, 28672, 4096, 1, 128),
+        (64, 4096, 14336, 1, 128), (4096, 8192, 28672, 1, 128), (17, 136, 512, 1, 64),
+        (5, 13, 512, 0, 128), (300, 384, 2048, 0, -1)]
+    checked = 0
+    for M, N, K, at, gs in shapes:
+        published = lib.w4_gemm_workspace_size(M, N, K, at, gs)
+        w4a8 = at == 2
+        kw = dict(M=M, N=N, K=K, a_type=at, gs=gs, ws=256, wsb=16,
+                  wtype=2 if w4a8 else 0, ot=3 if w4a8 else at,
+                  s=(256 if gs != -1 else None) if w4a8 else 256, st=2 if w4a8 else at)
+        for sched in range(lib.w4_num_schedules()):
+            st = _gemm(lib, sched=sched, **kw)
+            if st == w4.ERR_UNSUPPORTED:
+                continue
+            assert st == w4.ERR_WORKSPACE, (M, N, K, sched, st)
+            need = int(re.search(r"(\d+) bytes", lib.w4_last_error().decode()).group(1))
+            assert need <= published, (M, N, K, lib.w4_schedule_name(sched), need, published)
+            checked += 1
+    assert checked > 60
