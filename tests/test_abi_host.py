@@ -190,3 +190,29 @@ def test_every_schedule_fits_in_the_published_workspace(lib):
             assert need <= published, (M, N, K, lib.w4_schedule_name(sched), need, published)
             checked += 1
     assert checked > 60
+
+
+def test_default_heuristic_always_runs_valid_shapes(lib):
+    """For any shape the API accepts, the default heuristic's schedule can
+    run it within the published workspace (seeded sweep over M, N, K,
+    group size and mode; each call stops on the host at the workspace)."""
+    import re
+
+    import numpy as np
+
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        at = int(rng.integers(0, 3))
+        M = int(rng.choice([1, 2, 7, 8, 9, 16, 17, 31, 32, 33, 64, 100, 128, 129, 256, 700, 4096]))
+        N = int(rng.choice([8, 13, 64, 120, 128, 136, 1000, 4096, 8192]))
+        K = 64 * int(rng.integers(1, 64))
+        divisors = [g for g in (64, 128, 256, 512, 1024) if K % g == 0]
+        gs = int(rng.choice([-1] + divisors))
+        published = lib.w4_gemm_workspace_size(M, N, K, at, gs)
+        w4a8 = at == 2
+        st = _gemm(lib, M=M, N=N, K=K, a_type=at, gs=gs, ws=256, wsb=16, sched=-1,
+                   wtype=2 if w4a8 else 0, ot=3 if w4a8 else at,
+                   s=(256 if gs not in (-1, K) else None) if w4a8 else 256, st=2 if w4a8 else at)
+        assert st == w4.ERR_WORKSPACE, (M, N, K, at, gs, st, lib.w4_last_error())
+        need = int(re.search(r"(\d+) bytes", lib.w4_last_error().decode()).group(1))
+        assert need <= published, (M, N, K, at, gs)
