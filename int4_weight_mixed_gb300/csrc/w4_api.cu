@@ -69,13 +69,19 @@ int mode_of(int a_type) {
 }
 
 TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs);
+DkPlan make_dk_plan(int si, int mode, int64_t M, int64_t N, int64_t K, size_t* ws_partials,
+                    size_t* ws_total);
+constexpr size_t kMaxDynSmem = 227 * 1024;  // dynamic shared memory a CTA may opt into
 
 // Whether schedule `si` can run this (already validated) problem shape.
 bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
   const Schedule& sc = kSchedules[si];
   if (sc.engine == kEngineSimt) return true;
-  if (sc.engine == kEngineDk)  // M rows in 8-row tiles; a 128-wide K block in one group
-    return M <= sc.bm && (gs == K || gs % 128 == 0);
+  if (sc.engine == kEngineDk) {  // M rows in 8-row tiles; a 128-wide K block in one group
+    if (M > sc.bm || (gs != K && gs % 128 != 0)) return false;
+    size_t wp, wt;  // and the staged activations of a unit fit in shared memory
+    return make_dk_plan(si, mode, M, N, K, &wp, &wt).smem_bytes <= kMaxDynSmem;
+  }
   if (sc.engine == kEngineDs)  // also bulk copies of 16-byte-multiple scale rows
     return M <= sc.bm && (gs == K || gs % 128 == 0) && N % 8 == 0 &&
            !(mode == kW4A8 && has_sg && N % 16 != 0);
@@ -209,6 +215,8 @@ DkPlan make_dk_plan(int si, int mode, int64_t M, int64_t N, int64_t K, size_t* w
   double best = 1e30;
   int best_s = 1;
   for (int ks = 1; ks <= 64 && ks <= p.kblocks; ++ks) {
+    // a K split counts its contributors in one counter per weight tile
+    if (ks > 1 && static_cast<size_t>(p.n_tiles) * 4 > kCounterBytes) break;
     const int kbu = (p.kblocks + ks - 1) / ks;
     if (dk_smem_bytes(p.nj, kbu) > 100 * 1024) continue;
     const int64_t units = static_cast<int64_t>(p.n_tiles) * ks;

@@ -216,3 +216,35 @@ def test_default_heuristic_always_runs_valid_shapes(lib):
         assert st == w4.ERR_WORKSPACE, (M, N, K, at, gs, st, lib.w4_last_error())
         need = int(re.search(r"(\d+) bytes", lib.w4_last_error().decode()).group(1))
         assert need <= published, (M, N, K, at, gs)
+
+
+def test_dk_does_not_split_k_beyond_its_counters(lib):
+    """dk counts the contributors of a K split in one 32-bit counter per
+    128-column tile inside a 64 KB region: with more tiles than that it
+    runs unsplit (its workspace need is then the header and counters only)."""
+    import re
+
+    dk8 = [i for i in range(lib.w4_num_schedules()) if lib.w4_schedule_name(i) == b"dk8_sk"][0]
+
+    def need(N, K):
+        st = _gemm(lib, M=1, N=N, K=K, a_type=0, gs=-1, ws=256, wsb=16, sched=dk8, wtype=0, ot=0)
+        assert st == w4.ERR_WORKSPACE
+        return int(re.search(r"(\d+) bytes", lib.w4_last_error().decode()).group(1))
+
+    assert need(1000, 4096) > 256 + 64 * 1024                # few tiles: K is split
+    # K = 8192 does not fit one dk CTA's preferred shared memory unsplit, so the
+    # planner would split it; with more tiles than counters it must not
+    assert need(16384 * 128 + 8, 8192) == 256 + 64 * 1024
+
+
+def test_dk_gives_way_when_its_staging_does_not_fit(lib):
+    """A K so long that even the largest K split leaves dk's staged
+    activations beyond a CTA's shared memory: dk reports UNSUPPORTED and the
+    default heuristic takes the CUDA-core schedule (N % 8 != 0 rules out
+    the others)."""
+    dk8 = [i for i in range(lib.w4_num_schedules()) if lib.w4_schedule_name(i) == b"dk8_sk"][0]
+    kw = dict(M=1, a_type=0, gs=-1, ws=256, wsb=16, wtype=0, ot=0)
+    assert _gemm(lib, N=16384 * 128 + 8, K=65536, sched=dk8, **kw) == w4.ERR_UNSUPPORTED
+    assert _gemm(lib, N=1001, K=1 << 22, sched=dk8, **kw) == w4.ERR_UNSUPPORTED
+    assert lib.w4_schedule_name(lib.w4_default_schedule(1, 1001, 1 << 22, 0, -1)) == b"simt"
+    assert lib.w4_schedule_name(lib.w4_default_schedule(1, 1001, 4096, 0, -1)) == b"dk8_sk"
