@@ -39,8 +39,11 @@
 // W4A8 (pytorch/ao PR #1113 "support W4A8 Marlin kernel") runs on the same
 // bf16 tensor cores: int8 activations and int4 (x int8 group scale)
 // weights are exact in bf16, their products are exact in fp32, and the
-// accumulator is drained into an int32 copy in tensor memory before any
-// partial sum can exceed 2^24, so the int32 result is exact.
+// accumulator is drained into an int32 running sum before any partial sum
+// can exceed 2^24, so the int32 result is exact.  The running sum sits in
+// tensor memory beside the accumulator for tiles of up to 128 rows, and in a
+// per-CTA global scratch for 256-row tiles (whose accumulator and converted
+// stages fill tensor memory).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
