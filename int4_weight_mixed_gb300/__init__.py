@@ -110,6 +110,18 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def _dense_on(device, **tensors):
+    """The kernels read every array densely from its first element: each
+    given tensor must be a contiguous CUDA tensor on `device`."""
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda or t.device != device:
+            raise ValueError(f"{name} must be a CUDA tensor on {device} (got {t.device})")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
 def layout_version() -> int:
     return load().w4_layout_version()
 
@@ -185,6 +197,8 @@ def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
     output, or out_dtype=torch.int32 for the raw accumulator.
     """
     lib = load()
+    _dense_on(a.device, a=a, b_packed=b_packed, scales=scales, zeros=zeros,
+              token_scales=token_scales, channel_scales=channel_scales, out=out, ws=ws)
     M, K = a.shape
     a_code = _DTYPE_CODE[a.dtype]
     if out_dtype is None:

@@ -248,3 +248,15 @@ def test_dk_gives_way_when_its_staging_does_not_fit(lib):
     assert _gemm(lib, N=1001, K=1 << 22, sched=dk8, **kw) == w4.ERR_UNSUPPORTED
     assert lib.w4_schedule_name(lib.w4_default_schedule(1, 1001, 1 << 22, 0, -1)) == b"simt"
     assert lib.w4_schedule_name(lib.w4_default_schedule(1, 1001, 4096, 0, -1)) == b"dk8_sk"
+
+
+def test_binding_rejects_host_and_strided_tensors(lib):
+    """The binding checks that every tensor it passes is a contiguous
+    device tensor before calling the library (CPU tensors here)."""
+    import torch
+
+    a = torch.zeros(4, 128, dtype=torch.float16)
+    b = torch.zeros(w4.prepacked_size(128, 128), dtype=torch.uint8)
+    s = torch.zeros(1, 128, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        w4.gemm(a, b, w4.UINT4B8, 128, scales=s, group_size=-1)
