@@ -135,6 +135,7 @@ def prepack_B(w_q: torch.Tensor, wtype: int, layout: int, K: int, N: int,
     """w4_prepack_B: packed int32 words (device) -> prepacked uint8 buffer."""
     lib = load()
     assert w_q.dtype == torch.int32 and w_q.is_cuda and w_q.is_contiguous()
+    _dense_on(w_q.device, out=out)
     nbytes = prepacked_size(K, N)
     if out is None:
         out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=w_q.device)
@@ -145,6 +146,7 @@ def prepack_B(w_q: torch.Tensor, wtype: int, layout: int, K: int, N: int,
 
 def unprepack_B(b_packed: torch.Tensor, wtype: int, layout: int, K: int, N: int) -> torch.Tensor:
     lib = load()
+    _dense_on(b_packed.device, b_packed=b_packed)
     shape = (K // 8, N) if layout == KN_SEQ else (N, K // 8)
     w_q = torch.empty(shape, dtype=torch.int32, device=b_packed.device)
     _check(lib.w4_unprepack_B(_ptr(b_packed), wtype, layout, K, N, _ptr(w_q),
