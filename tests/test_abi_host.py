@@ -260,3 +260,25 @@ def test_binding_rejects_host_and_strided_tensors(lib):
     s = torch.zeros(1, 128, dtype=torch.float16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         w4.gemm(a, b, w4.UINT4B8, 128, scales=s, group_size=-1)
+
+
+def test_binding_argtypes_match_the_header(lib):
+    """Every entry point the binding declares to ctypes takes as many
+    arguments as include/w4.h declares for it (ABI drift check)."""
+    import re
+
+    text = open(os.path.join(ROOT, "include", "w4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = dict(
+        (m.group(1), m.group(2))
+        for m in re.finditer(r"\b(w4_[A-Za-z0-9_]+)\s*\(([^)]*)\)\s*;", text))
+    assert len(decls) >= 15
+    checked = 0
+    for name, params in decls.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        checked += 1
+    assert checked >= 10
