@@ -5,12 +5,20 @@ K=21760 — one GEMM for each M in {1, 8, 32, 128, 512, 1024} (int8
 activations with per-token fp32 scales, int4 weights with per-channel fp32
 scales, fp16 output), the shape of the pytorch/ao PR #1113 "support W4A8
 Marlin kernel" speedup sweep.  Weights are prepacked once (offline step,
-timed separately under "prepack").  Four copies of every input are rotated
-so that no launch finds its operands in L2 (4 x 89 MB > 2 x 129 MB L2).
+timed separately under "prepack").  Every GEMM of a step reads its own
+weight copy: ROTATE copies of the weights and activations rotate GEMM by
+GEMM, so a copy is read again only after ROTATE - 1 other 89 MB copies
+(more than 2x the 129 MB L2) have streamed through.
 
-metric: TFLOP/s of the whole sweep (sum 2*M*N*K / step time); the per-M
-breakdown (microseconds, TFLOP/s, weight GB/s, roofline fraction) is in
-"sweep".  --impl reference times the CPU oracle (plain fp64/int64 C) on a
+metric: TFLOP/s of the whole sweep (sum 2*M*N*K / step time).  The timed
+region is `--steps` steps between barriers; it is repeated until at least
+MIN_TIMED_S seconds of timed regions have run (so that the clocks sampled
+during them mean something), and the step time is the median over repeats.
+"sweep" has the per-M breakdown (isolated graph replays of one GEMM: us,
+TFLOP/s, weight GB/s, roofline fraction against the burst peaks); "extra"
+has the same for the other workloads: W4A8 g128 (N=8192, K=21760), W4A16
+decode on the Llama-3-8B linear shapes and W4A16 prefill on the Llama-3-70B
+MLP shapes.  --impl reference times the CPU oracle (plain fp64/int64 C) on a
 bounded sample of the same workload.
 
 Multi-GPU (torchrun): replicas only; every rank runs the same sweep on its
@@ -20,6 +28,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -36,14 +45,16 @@ import w4synth  # noqa: E402
 
 N, K = w4synth.QQQ_N, w4synth.QQQ_K
 M_SWEEP = w4synth.QQQ_CH_M
-ROTATE = 4
+ROTATE = 8            # weight + activation copies of the step, rotated GEMM by GEMM
+L2_BYTES = 129 * 2 ** 20
+MIN_TIMED_S = 2.0     # repeat the K-step timed region until this much has run
 METRIC = "int4-weight GEMM TFLOP/s & weight GB/s vs M (N=8192,K=21760), % roofline"
 UNIT = "TFLOP/s"
 WORKLOAD = "W4A8 QQQ per-channel sweep M in {1,8,32,128,512,1024}, N=8192, K=21760"
 
 
-def flops(M):
-    return 2.0 * M * N * K
+def flops(M, n=N, k=K):
+    return 2.0 * M * n * k
 
 
 def weight_bytes():
@@ -55,6 +66,19 @@ def algo_bytes(M):
     return weight_bytes() + M * K + 4 * M + 2 * M * N
 
 
+def w4a8_g128_bytes(M, n=N, k=K):
+    """W4A8 per-group: packed int4 + int8 group scales + fp32 channel scales,
+    int8 activations + token scales, fp16 output."""
+    return k * n // 2 + (k // 128) * n + 4 * n + M * k + 4 * M + 2 * M * n
+
+
+def w4a16_bytes(M, n, k, zeros, gs=128):
+    """W4A16: packed int4 + 16-bit scales (+ zero-points), 16-bit activations
+    and output."""
+    G = k // gs
+    return k * n // 2 + G * n * 2 * (2 if zeros else 1) + M * k * 2 + M * n * 2
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -63,6 +87,18 @@ def peaks():
         return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
                     bf16_sus=p.get("bf16_tflops_sustained", p["bf16_tflops"]), src="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def roofline_entry(us, fl, nbytes, pk):
+    """Roofline of one isolated launch: the larger of the HBM time of its
+    algorithmic bytes and the tensor time of its flops (burst bf16 peak),
+    over the measured time."""
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    t_tc = fl / (pk["bf16"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {"us": round(us, 2), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
+            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bound": bound,
+            "roofline_frac": round(max(t_hbm, t_tc) / (us * 1e-6), 3)}
 
 
 def measured_traffic(kernel, M):
@@ -98,6 +134,23 @@ def job_tflops(step_flops, world, ms_per_step):
     return step_flops * world / (ms_per_step * 1e-3) / 1e12
 
 
+def rotation(step, j, nper=len(M_SWEEP), copies=ROTATE):
+    """Copy read by GEMM j of step `step`: consecutive GEMMs read different
+    copies, and a copy comes back only after copies - 1 others."""
+    return (step * nper + j) % copies
+
+
+def rotation_period(nper=len(M_SWEEP), copies=ROTATE):
+    """Steps after which the rotation pattern repeats (graphs to capture)."""
+    return copies // math.gcd(nper, copies)
+
+
+def copies_for(nbytes, minimum=2):
+    """Copies of a problem whose rotation streams more than 2x L2 between two
+    reads of the same copy."""
+    return max(minimum, 2 * L2_BYTES // max(nbytes, 1) + 2)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -128,8 +181,6 @@ class ClockSampler:
     def stop(self, t0=None, t1=None):
         """Median SM clock and the throttle reasons seen between t0 and t1
         (time.time() values; all samples when not given)."""
-        import datetime
-
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -138,59 +189,182 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sms, maxes, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                sm, mx = float(parts[1]), float(parts[2])
-            except ValueError:
-                continue
-            if t0 is not None and not (t0 <= ts <= t1):
-                continue
-            sms.append(sm)
-            maxes.append(mx)
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sms:
-            return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        return parse_clocks(out, t0, t1)
+
+
+def parse_clocks(text, t0=None, t1=None):
+    """Median SM clock, the largest max clock, the largest power draw and the
+    throttle reasons seen in nvidia-smi CSV lines (FIELDS order) between t0
+    and t1."""
+    import datetime
+
+    sms, maxes, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, mx = float(parts[1]), float(parts[2])
+        except ValueError:
+            continue
+        if t0 is not None and not (t0 <= ts <= t1):
+            continue
+        sms.append(sm)
+        maxes.append(mx)
+        try:
+            power.append(float(parts[3]))
+        except ValueError:
+            pass
+        for nm, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    if not sms:
+        return None
+    return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+            "reasons": sorted(reasons), "samples": len(sms),
+            "power_w_max": max(power) if power else None}
 
 
 def make_inputs(dev):
-    """ROTATE copies of every input, resident in HBM (prepacked weights)."""
+    """ROTATE copies of every input of the step, resident in HBM: one seeded
+    weight (prepacked) and one set of activations per M, cloned so that each
+    copy lives at its own addresses."""
     import int4_weight_mixed_gb300 as w4
 
+    e = w4synth.gen_w4a8(1, N, K, group_size=-1, seed=100)
+    w_dev = e["w"].to(dev)
+    b0 = w4.prepack_B(w_dev, e["wtype"], e["layout"], K, N)
+    del w_dev
+    acts0 = {}
+    for M in M_SWEEP:
+        x = w4synth.gen_w4a8(M, 8, K, seed=1000 + M)  # its a [M,K] and s_tok [M]
+        acts0[M] = (x["a"].to(dev), x["s_tok"].to(dev))
+    s_ch = e["s_ch"].to(dev)
     sets = []
     for r in range(ROTATE):
-        e = w4synth.gen_w4a8(1, N, K, group_size=-1, seed=100 + r)
-        w_dev = e["w"].to(dev)
-        b = w4.prepack_B(w_dev, e["wtype"], e["layout"], K, N)
-        del w_dev
-        acts = {}
-        for M in M_SWEEP:
-            x = w4synth.gen_w4a8(M, 8, K, seed=1000 * r + M)  # its a [M,K] and s_tok [M]
-            acts[M] = (x["a"].to(dev), x["s_tok"].to(dev))
-        sets.append(dict(b=b, s_ch=e["s_ch"].to(dev), acts=acts, wq=e["w"], wtype=e["wtype"]))
+        b = b0 if r == 0 else b0.clone()
+        acts = acts0 if r == 0 else {M: (a.clone(), s.clone()) for M, (a, s) in acts0.items()}
+        sets.append(dict(b=b, s_ch=s_ch if r == 0 else s_ch.clone(), acts=acts, wq=e["w"],
+                         wtype=e["wtype"]))
     return sets
 
 
+def launches_per_gemm(name):
+    """Kernels of this library one GEMM launches: the streamed skinny-M
+    schedule three (activation staging, GEMM, reduction); the tensor-core W4A8
+    schedule two (int8->bf16 staging, GEMM); the others one."""
+    return 3 if name.startswith("ds") else 2 if name.startswith("tc") else 1
+
+
 def launches_per_step(w4):
-    """Kernels of this library one step launches: the streamed skinny-M
-    schedule is three launches (activation staging, GEMM, reduction); the
-    tensor-core W4A8 schedule is two (int8->bf16 staging, GEMM); the
-    register-fed skinny-M and CUDA-core schedules one."""
     names = w4.schedule_names()
-    n = 0
-    for M in M_SWEEP:
-        name = names[w4.default_schedule(M, N, K, torch.int8, -1)]
-        n += 3 if name.startswith("ds") else 2 if name.startswith("tc") else 1
-    return n
+    return sum(launches_per_gemm(names[w4.default_schedule(M, N, K, torch.int8, -1)])
+               for M in M_SWEEP)
+
+
+def capture(fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def time_isolated(fns, reps, stream, eager=False):
+    """Microseconds per launch of one GEMM: a graph per rotated copy, `reps`
+    replays round-robin between CUDA events on the launching stream."""
+    for f in fns:  # eager first: kernel attributes are set outside any capture
+        f()
+    torch.cuda.synchronize()
+    if eager:
+        runs = fns
+    else:
+        graphs = [capture(f) for f in fns]
+        runs = [g.replay for g in graphs]
+    for r in runs:
+        r()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for i in range(reps):
+        runs[i % len(runs)]()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    return a0.elapsed_time(a1) * 1e3 / reps
+
+
+def extra_workloads(w4, dev, stream, pk, reps, eager=False):
+    """The other configurations, one isolated GEMM at a time (default
+    schedule), each with its roofline fraction: W4A8 per-group g128 at N=8192,
+    K=21760; W4A16 decode on the Llama-3-8B linear shapes (uint4 + bf16
+    zero-points); W4A16 prefill on the Llama-3-70B MLP shapes at M=4096."""
+    names = w4.schedule_names()
+    out = {"w4a8_g128_n8192_k21760": [], "w4a16_decode_llama3_8b": [],
+           "w4a16_prefill_llama3_70b": []}
+
+    # W4A8 g128
+    e = w4synth.gen_w4a8(1, N, K, group_size=128, seed=200)
+    b = w4.prepack_B(e["w"].to(dev), e["wtype"], e["layout"], K, N)
+    sg, s_ch = e["sg"].to(dev), e["s_ch"].to(dev)
+    for M in w4synth.QQQ_G128_M:
+        x = w4synth.gen_w4a8(M, 8, K, seed=300 + M)
+        R = copies_for(w4a8_g128_bytes(M))
+        cp = [(b, sg, s_ch, x["a"].to(dev), x["s_tok"].to(dev))]
+        cp += [tuple(t.clone() for t in cp[0]) for _ in range(R - 1)]
+        o = torch.empty((M, N), dtype=torch.float16, device=dev)
+        fns = [lambda c=c, M=M: w4.gemm(c[3], c[0], e["wtype"], N, scales=c[1], group_size=128,
+                                       token_scales=c[4], channel_scales=c[2], out=o)
+               for c in cp]
+        us = time_isolated(fns, reps, stream, eager)
+        ent = roofline_entry(us, flops(M), w4a8_g128_bytes(M), pk)
+        ent.update(M=M, schedule=names[w4.default_schedule(M, N, K, torch.int8, 128)])
+        out["w4a8_g128_n8192_k21760"].append(ent)
+        del cp, fns
+    del b, sg, s_ch
+
+    # W4A16 decode, Llama-3-8B shapes (uint4 + pre-scaled bf16 zero-points, g128)
+    for (n, k) in w4synth.DECODE_SHAPES:
+        d = w4synth.gen_w4a16(max(w4synth.DECODE_M), n, k, act_dtype=torch.bfloat16,
+                              wtype=w4synth.UINT4, layout=w4synth.NK_EXLLAMA, group_size=128,
+                              zeros=True, seed=n + k)
+        b = w4.prepack_B(d["w"].to(dev), d["wtype"], d["layout"], k, n)
+        s, z, a_all = d["s"].to(dev), d["z"].to(dev), d["a"].to(dev)
+        for M in w4synth.DECODE_M:
+            nb = w4a16_bytes(M, n, k, zeros=True)
+            R = copies_for(nb)
+            base = (b, s, z, a_all[:M].contiguous())
+            cp = [base] + [tuple(t.clone() for t in base) for _ in range(R - 1)]
+            o = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+            fns = [lambda c=c: w4.gemm(c[3], c[0], d["wtype"], n, scales=c[1], zeros=c[2],
+                                       group_size=128, out=o) for c in cp]
+            us = time_isolated(fns, reps, stream, eager)
+            ent = roofline_entry(us, flops(M, n, k), nb, pk)
+            ent.update(M=M, N=n, K=k, copies=R,
+                       schedule=names[w4.default_schedule(M, n, k, torch.bfloat16, 128)])
+            out["w4a16_decode_llama3_8b"].append(ent)
+            del cp, fns
+        del b, s, z, a_all
+
+    # W4A16 prefill, Llama-3-70B MLP shapes at M=4096 (uint4b8, bf16 scales, g128)
+    M = 4096
+    for (n, k) in w4synth.PREFILL_SHAPES:
+        d = w4synth.gen_w4a16(M, n, k, act_dtype=torch.bfloat16, wtype=w4synth.UINT4B8,
+                              layout=w4synth.NK_EXLLAMA, group_size=128, zeros=False,
+                              seed=n + k)
+        b = w4.prepack_B(d["w"].to(dev), d["wtype"], d["layout"], k, n)
+        base = (b, d["s"].to(dev), d["a"].to(dev))
+        cp = [base, tuple(t.clone() for t in base)]
+        o = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        fns = [lambda c=c: w4.gemm(c[2], c[0], d["wtype"], n, scales=c[1], group_size=128, out=o)
+               for c in cp]
+        us = time_isolated(fns, max(5, reps // 4), stream, eager)
+        ent = roofline_entry(us, flops(M, n, k), w4a16_bytes(M, n, k, zeros=False), pk)
+        ent.update(M=M, N=n, K=k, schedule=names[w4.default_schedule(M, n, k, torch.bfloat16, 128)])
+        out["w4a16_prefill_llama3_70b"].append(ent)
+        del cp, fns, b, base
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_gpu(args):
@@ -203,6 +377,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w4.load()
+    pk = peaks()
     sets = make_inputs(dev)
     outs = {M: torch.empty((M, N), dtype=torch.float16, device=dev) for M in M_SWEEP}
     ws = w4.workspace(dev, w4.workspace_size(max(M_SWEEP), N, K, torch.int8, -1))
@@ -213,6 +388,10 @@ def run_gpu(args):
         a, s_tok = st["acts"][M]
         w4.gemm(a, st["b"], st["wtype"], N, scales=None, group_size=-1, token_scales=s_tok,
                 channel_scales=st["s_ch"], out=outs[M], ws=ws)
+
+    def step(i):
+        for j, M in enumerate(M_SWEEP):
+            gemm(rotation(i, j), M)
 
     def barrier():
         if world > 1:
@@ -236,88 +415,81 @@ def run_gpu(args):
 
     # per-token int8 quantization of fp16 activations at the largest sweep M
     # (the step before a W4A8 GEMM; timed beside the step, not inside it):
-    # ROTATE input copies > L2, 2 bytes read + 1 written per element
+    # 4 input copies > L2, 2 bytes read + 1 written per element
     qm = max(M_SWEEP)
-    qa = [w4synth.gen_act16(qm, K, torch.float16, seed=50 + r).to(dev) for r in range(ROTATE)]
+    qa = [w4synth.gen_act16(qm, K, torch.float16, seed=50 + r).to(dev) for r in range(4)]
     qo = [(torch.empty(qm, K, dtype=torch.int8, device=dev),
-           torch.empty(qm, dtype=torch.float32, device=dev)) for _ in range(ROTATE)]
+           torch.empty(qm, dtype=torch.float32, device=dev)) for _ in range(4)]
     for r in range(3):
-        w4.quantize_per_token(qa[r % ROTATE], out=qo[r % ROTATE][0], scales=qo[r % ROTATE][1])
+        w4.quantize_per_token(qa[r % 4], out=qo[r % 4][0], scales=qo[r % 4][1])
     e0.record(stream)
     for r in range(20):
-        w4.quantize_per_token(qa[r % ROTATE], out=qo[r % ROTATE][0], scales=qo[r % ROTATE][1])
+        w4.quantize_per_token(qa[r % 4], out=qo[r % 4][0], scales=qo[r % 4][1])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     quant_us = e0.elapsed_time(e1) * 1e3 / 20
     quant_gbs = (3 * qm * K + 4 * qm) / (quant_us * 1e-6) / 1e9
     del qa, qo
 
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        return g
-
-    # eager warm-up (sets kernel attributes), then one graph per input rotation
+    # eager warm-up (sets kernel attributes), then one graph per step of the
+    # rotation pattern
+    period = rotation_period()
     for i in range(args.warmup):
-        for M in M_SWEEP:
-            gemm(i % ROTATE, M)
+        step(i)
     barrier()
     if args.eager:  # plain launches (for profilers that do not follow graphs)
         class _Eager:
-            def __init__(self, r):
-                self.r = r
+            def __init__(self, i):
+                self.i = i
 
             def replay(self):
-                for M in M_SWEEP:
-                    gemm(self.r, M)
-        step_graphs = [_Eager(r) for r in range(ROTATE)]
+                step(self.i)
+        step_graphs = [_Eager(i) for i in range(period)]
     else:
-        step_graphs = [capture(lambda r=r: [gemm(r, M) for M in M_SWEEP]) for r in range(ROTATE)]
+        step_graphs = [capture(lambda i=i: step(i)) for i in range(period)]
     for i in range(args.warmup):
-        step_graphs[i % ROTATE].replay()
+        step_graphs[i % period].replay()
     barrier()
 
-    # timed region: K steps of the whole sweep, graph replays on one stream
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # timed region: K steps of the whole sweep, graph replays on one stream,
+    # repeated until MIN_TIMED_S of timed regions have run
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    barrier()
+    rep_ms = []
+    timed_s = 0.0
     wall0 = time.time()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step_graphs[i % ROTATE].replay()
-    t_end.record(stream)
-    barrier()
+    while True:
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step_graphs[i % period].replay()
+        t_end.record(stream)
+        barrier()
+        ms = t_start.elapsed_time(t_end)
+        rep_ms.append(ms)
+        timed_s += ms * 1e-3
+        if timed_s >= args.min_timed_s or len(rep_ms) >= 100000:
+            break
     wall1 = time.time()
     time.sleep(0.2)
     clk = clocks.stop(wall0, wall1)
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = slowest_rank_ms(statistics.median(rep_ms), world, dev)
 
-    # per-M launch durations: graphs of one GEMM per rotation, events on the
-    # launching stream around `reps` replays
+    # per-M launch durations: graphs of one GEMM per rotated copy, events on
+    # the launching stream around `reps` replays
     per_m = {}
     reps = max(8, min(args.steps, 100))
     for M in M_SWEEP:
-        if args.eager:
-            break
-        gs_m = [capture(lambda r=r, M=M: gemm(r, M)) for r in range(ROTATE)]
-        for r in range(ROTATE):
-            gs_m[r].replay()
-        barrier()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for i in range(reps):
-            gs_m[i % ROTATE].replay()
-        a1.record(stream)
-        barrier()
-        per_m[M] = [a0.elapsed_time(a1) * 1e3 / reps]
-        del gs_m
+        per_m[M] = time_isolated([lambda r=r, M=M: gemm(r, M) for r in range(ROTATE)], reps,
+                                 stream, args.eager)
     if w4.check_status(ws) != w4.OK:
         raise RuntimeError("a device-side wait timed out during the benchmark")
 
-    total_ms = slowest_rank_ms(total_ms, world, dev)
+    extra = None
+    if not args.skip_extra:
+        extra = extra_workloads(w4, dev, stream, pk, reps, args.eager)
 
     # end-to-end through the public API from pinned host buffers
     e2e = None
@@ -333,7 +505,8 @@ def run_gpu(args):
         # the current GEMM runs, and each result comes back while the next GEMM
         # runs. Two sets of device buffers, used by alternate steps, let a
         # step's GEMMs start while the previous step's last result is still
-        # being copied back (allocated once, outside the timing).
+        # being copied back (allocated once, outside the timing).  The weights
+        # rotate GEMM by GEMM as in the device-timed step.
         h2d_stream = torch.cuda.Stream(device=dev)
         d2h_stream = torch.cuda.Stream(device=dev)
         bufs = [dict(a={M: torch.empty_like(host_a[M], device=dev) for M in M_SWEEP},
@@ -346,7 +519,8 @@ def run_gpu(args):
         step_no = [0]
 
         def e2e_step():
-            b = bufs[step_no[0] % 2]
+            i = step_no[0]
+            b = bufs[i % 2]
             step_no[0] += 1
             with torch.cuda.stream(h2d_stream):
                 if b["free"] is not None:  # this set's previous GEMMs and copies are done
@@ -355,10 +529,11 @@ def run_gpu(args):
                     b["a"][M].copy_(host_a[M], non_blocking=True)
                     b["s"][M].copy_(host_s[M], non_blocking=True)
                     ev_in[M].record(h2d_stream)
-            for M in M_SWEEP:
+            for j, M in enumerate(M_SWEEP):
+                wset = sets[rotation(i, j)]
                 stream.wait_event(ev_in[M])
-                w4.gemm(b["a"][M], sets[0]["b"], sets[0]["wtype"], N, scales=None,
-                        group_size=-1, token_scales=b["s"][M], channel_scales=sets[0]["s_ch"],
+                w4.gemm(b["a"][M], wset["b"], wset["wtype"], N, scales=None,
+                        group_size=-1, token_scales=b["s"][M], channel_scales=wset["s_ch"],
                         out=b["o"][M], ws=ws)
                 ev_out[M].record(stream)
             with torch.cuda.stream(d2h_stream):
@@ -391,46 +566,55 @@ def run_gpu(args):
             dist.destroy_process_group()
         return
 
-    pk = peaks()
+    names = w4.schedule_names()
     step_flops = sum(flops(M) for M in M_SWEEP)
     ms_per_step = total_ms / args.steps
     value = job_tflops(step_flops, world, ms_per_step)
     sweep = []
     for M in M_SWEEP:
-        if M not in per_m:
-            per_m[M] = [ms_per_step * 1e3 / len(M_SWEEP)]
-        us = statistics.median(per_m[M])
-        tf = flops(M) / (us * 1e-6) / 1e12
-        gbs = weight_bytes() / (us * 1e-6) / 1e9
-        t_hbm = algo_bytes(M) / (pk["hbm"] * 1e9)
-        t_tc = flops(M) / (pk["bf16_sus"] * 1e12)
-        bound = "hbm" if t_hbm >= t_tc else "tensor"
-        frac = max(t_hbm, t_tc) / (us * 1e-6)
-        sweep.append({"M": M, "us": round(us, 2), "tflops": round(tf, 1),
-                      "weight_gbs": round(gbs, 1), "bound": bound, "roofline_frac": round(frac, 3)})
+        ent = roofline_entry(per_m[M], flops(M), algo_bytes(M), pk)
+        ent["weight_gbs"] = round(weight_bytes() / (per_m[M] * 1e-6) / 1e9, 1)
+        ent["M"] = M
+        ent["schedule"] = names[w4.default_schedule(M, N, K, torch.int8, -1)]
+        sweep.append(ent)
     # dominant kernel: the largest share of the step
-    dom = max(M_SWEEP, key=lambda M: statistics.mean(per_m[M]))
-    dom_us = statistics.mean(per_m[dom])
-    roofline = {"kernel": "tc_gemm_kernel<W4A8> (+ its int8->bf16 staging launch)",
-                "M": dom, "bound": "tensor", "achieved": round(flops(dom) / (dom_us * 1e-6) / 1e12, 1),
-                "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "peak_source": f"{pk['src']} bf16 dense, sustained",
-                "traffic": measured_traffic("tc_gemm_kernel<W4A8>", dom)}
+    dom = max(M_SWEEP, key=lambda M: per_m[M])
+    dom_us = per_m[dom]
+    dom_ent = next(e for e in sweep if e["M"] == dom)
+    kname = ("tc_gemm_kernel<W4A8> (+ its int8->bf16 staging launch)"
+             if dom_ent["schedule"].startswith("tc") else f"{dom_ent['schedule']} launches")
+    if dom_ent["bound"] == "tensor":
+        roofline = {"kernel": kname, "M": dom, "bound": "tensor",
+                    "achieved": round(flops(dom) / (dom_us * 1e-6) / 1e12, 1),
+                    "peak": pk["bf16"], "unit": "TFLOP/s",
+                    "peak_source": f"{pk['src']} bf16 dense, burst (isolated graph replays of "
+                                   "this GEMM, ~30 ms each)"}
+    else:
+        roofline = {"kernel": kname, "M": dom, "bound": "hbm",
+                    "achieved": round(algo_bytes(dom) / (dom_us * 1e-6) / 1e9, 1),
+                    "peak": pk["hbm"], "unit": "GB/s", "peak_source": f"{pk['src']} HBM copy"}
+    roofline["traffic"] = measured_traffic("tc_gemm_kernel<W4A8>", dom)
     roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 3)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": f"{ROTATE} rotated input copies > 2x L2",
+        "config": {"workload": WORKLOAD,
+                   "l2": f"{ROTATE} weight+activation copies rotated GEMM by GEMM "
+                         f"({ROTATE - 1} x 89 MB between two reads of a copy > 2x L2)",
+                   "timing": f"{len(rep_ms)} repeats of the {args.steps}-step timed region "
+                             f"({timed_s:.2f} s timed); median repeat",
+                   "arith": "int8 x int4 exact on bf16 tensor cores, fp32 chunks drained "
+                            "to int32, fp16 epilogue",
                    "parallelism": f"replicas x{world}"},
-        "sweep": sweep, "roofline": roofline, "e2e": e2e,
+        "sweep": sweep, "roofline": roofline, "e2e": e2e, "extra": extra,
         "prepack": {"us": round(prepack_us, 1),
                     "gbs": round(2 * K * N // 2 / (prepack_us * 1e-6) / 1e9, 1)},
         "quantize": {"kernel": "quant_per_token_kernel<fp16>", "M": qm, "K": K,
                      "us": round(quant_us, 2), "gbs": round(quant_gbs, 1), "bound": "hbm",
                      "frac": round(quant_gbs / pk["hbm"], 3)},
-        "gpu_launches": launches_per_step(w4) * args.steps,
+        "gpu_launches": launches_per_step(w4) * args.steps * len(rep_ms),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -448,17 +632,20 @@ def run_single(args):
 
     dev = torch.device("cuda", 0)
     M = args.single
-    e = w4synth.gen_w4a8(M, N, K, group_size=-1, seed=0)
+    gs = args.group_size
+    e = w4synth.gen_w4a8(M, N, K, group_size=gs, seed=0)
     b = w4.prepack_B(e["w"].to(dev), e["wtype"], e["layout"], K, N)
     a, s_tok, s_ch = e["a"].to(dev), e["s_tok"].to(dev), e["s_ch"].to(dev)
-    ws = w4.workspace(dev, w4.workspace_size(M, N, K, torch.int8, -1))
+    sg = None if e["sg"] is None else e["sg"].to(dev)
+    ws = w4.workspace(dev, w4.workspace_size(M, N, K, torch.int8, gs))
     out = torch.empty((M, N), dtype=torch.float16, device=dev)
     for _ in range(args.warmup + args.steps):
-        w4.gemm(a, b, e["wtype"], N, scales=None, group_size=-1, token_scales=s_tok,
+        w4.gemm(a, b, e["wtype"], N, scales=sg, group_size=gs, token_scales=s_tok,
                 channel_scales=s_ch, out=out, ws=ws, schedule=args.schedule)
     torch.cuda.synchronize()
     st = w4.check_status(ws)
-    print(json.dumps({"single_M": M, "launches": args.warmup + args.steps, "status": st}))
+    print(json.dumps({"single_M": M, "group_size": gs, "launches": args.warmup + args.steps,
+                      "status": st}))
     if st != w4.OK:
         sys.exit(1)
 
@@ -549,12 +736,17 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
+                    help="repeat the K-step timed region until this many seconds have run")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="leave out the other workloads (shorter launch lists)")
     ap.add_argument("--single", type=int, default=0, help="run only the GEMM with this M")
+    ap.add_argument("--group-size", type=int, default=-1, help="group size of --single")
     ap.add_argument("--schedule", type=int, default=-1)
     ap.add_argument("--quant-single", type=int, default=0,
                     help="run only the per-token quantization of this many rows")

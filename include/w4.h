@@ -118,8 +118,8 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
  *
  *   a         [M,K] activations: W4_F16 / W4_BF16 (W4A16) or W4_S8 (W4A8).
  *   b_packed  output of w4_prepack_B for this K, N and wtype.
- *   group_size  128-multiple dividing K, or -1 / K for one group per
- *             column ([RDNA]: -1 resolves to K).  G = K / group_size.
+ *   group_size  a multiple of 64 that divides K, or -1 / K for one group
+ *             per column ([RDNA]: -1 resolves to K).  G = K / group_size.
  *   W4A16: b_scales [G,N] with scale_type == a_type; b_zeros [G,N] of the
  *          same type holding PRE-SCALED zero-points w_z, or NULL.
  *          w_hat[k][n] = v(q) * s[g][n] - w_z[g][n], rounded once to the
@@ -193,7 +193,14 @@ w4_status w4_check_status(void* workspace, size_t workspace_bytes, void* stream)
  *     threads) race and may corrupt each other's results.  Order them.
  *   - A problem whose scratch need is above W4_NOALLOC_SCRATCH_BYTES is
  *     rejected before anything runs, with W4_ERR_WORKSPACE (w4_last_error()
- *     names the bytes it would need); use w4_gemm with a workspace then. */
+ *     names the bytes it would need); use w4_gemm with a workspace then.
+ *   - A device-side wait that gives up (see w4_check_status) is NOT reported
+ *     on this path: its record lives in the shared scratch, which the next
+ *     call clears.  Callers that must detect such timeouts use w4_gemm with
+ *     their own workspace and w4_check_status.
+ *   - The scratch address is looked up once per device and kept for the life
+ *     of the process: do not use this entry point after cudaDeviceReset (or
+ *     anything else that destroys the device's primary context). */
 #define W4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 w4_status w4_gemm_noalloc(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
                           int wtype, int64_t N, const void* b_scales, int scale_type,

@@ -50,7 +50,6 @@ const Schedule kSchedules[] = {
     {"ds32_sk", kEngineDs, 32, kStreamK, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
-constexpr size_t kCounterBytes = 64 * 1024;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -569,12 +568,10 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   args.counters = reinterpret_cast<int*>(ws + plan.ws_counters);
   args.partials = ws + plan.ws_partials;
   args.icopy = reinterpret_cast<int32_t*>(ws + plan.ws_icopy);
-  const void* act = a;
-  if (pr.mode == kW4A8) {
-    cudaError_t e = launch_a8_to_bf16(static_cast<const int8_t*>(a), M * K, ws + plan.ws_act, s);
-    if (e != cudaSuccess) return cuda_fail(e, "int8->bf16 launch");
-    act = ws + plan.ws_act;
-  }
+  // W4A8 runs on the bf16 copy of its int8 activations in the workspace
+  // (staged below, once every tensor map is encoded: an error before that
+  // point leaves nothing enqueued)
+  const void* act = pr.mode == kW4A8 ? static_cast<const void*>(ws + plan.ws_act) : a;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   CUtensorMap amap, smap, zmap;
@@ -642,6 +639,10 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
             plan.nsub, plan.stages, plan.tstages, plan.icol, plan.gicopy, plan.acol, plan.gps, plan.a3d,
             tc_mma2(plan) ? 1 : 0, plan.tiles, plan.kb_total, plan.grid, plan.decomp, plan.ksplit,
             plan.max_segs, plan.smem_bytes);
+  if (pr.mode == kW4A8) {
+    cudaError_t e = launch_a8_to_bf16(static_cast<const int8_t*>(a), M * K, ws + plan.ws_act, s);
+    if (e != cudaSuccess) return cuda_fail(e, "int8->bf16 launch");
+  }
   cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
 }

@@ -217,7 +217,10 @@ __global__ void __launch_bounds__(128 * NJ) ds_prep_kernel(const void* __restric
   int is = 0;
   if (m < M && k0 < K) {  // K % 64 == 0: the 8 values are all inside or all outside
     // fp16 fragments (W4A8, f16): the values of odd pairs (positions 2, 3, 6,
-    // 7) are divided by 16, exactly, to match weights read 16x too large
+    // 7) are divided by 16, to match weights read 16x too large.  Exact for
+    // int8 values; for fp16 activations exact when |a| >= 2^-10, while a
+    // smaller |a| gives a subnormal quotient rounded to the nearest multiple
+    // of 2^-24 (an absolute error of at most 2^-25 in that activation).
     if (MODE == kW4A8) {
       const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + m * K + k0);
       const int8_t* b8 = reinterpret_cast<const int8_t*>(&raw);

@@ -43,6 +43,9 @@ constexpr int kTcOtherRegs = 64;
 static_assert(32 * kConvWarps * kTcConvRegs + 128 * kTcOtherRegs <= kTcThreads * kTcLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr size_t kWsHeader = 256;                // status word + spare
+// Split-K tile counters after the header: zero on entry, left zero by every
+// call (and re-zeroed by w4_check_status after a timeout).
+constexpr size_t kCounterBytes = 64 * 1024;
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
 

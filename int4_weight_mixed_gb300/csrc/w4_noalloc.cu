@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/w4.h"
+#include "w4_internal.h"
 
 namespace {
 
@@ -31,7 +32,7 @@ std::mutex g_mutex;
 // Header plus split-K tile counters: the part of the scratch that must be
 // zero when a call starts (the library leaves it zero after a normal call,
 // but a call that timed out may not).
-constexpr size_t kZeroBytes = 256 + 64 * 1024;
+constexpr size_t kZeroBytes = w4::kWsHeader + w4::kCounterBytes;
 
 }  // namespace
 

@@ -47,9 +47,13 @@ def oracle_w4a16(d):
 
 
 def samples(M, N, count=384, seed=0):
+    """Random output elements plus the corners, and 16 elements of the last
+    row tile x last column tile (ragged or not)."""
     rng = np.random.default_rng(seed)
-    rows = np.concatenate([[0, M - 1, M // 2], rng.integers(0, M, count)])
-    cols = np.concatenate([[0, N - 1, min(127, N - 1)], rng.integers(0, N, count)])
+    tail_r = M - 1 - rng.integers(0, min(M, 256), 16)
+    tail_c = N - 1 - rng.integers(0, min(N, 128), 16)
+    rows = np.concatenate([[0, M - 1, M // 2], tail_r, rng.integers(0, M, count)])
+    cols = np.concatenate([[0, N - 1, min(127, N - 1)], tail_c, rng.integers(0, N, count)])
     return rows.astype(np.int64), cols.astype(np.int64)
 
 
@@ -103,14 +107,33 @@ def test_tiny_w4a16_every_schedule(gpu_lib, name):
 
 @pytest.mark.parametrize("name", ALL)
 @pytest.mark.parametrize("zeros", [False, True])
-def test_w4a16_bf16_several_tiles(gpu_lib, name, zeros):
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_w4a16_several_tiles(gpu_lib, name, zeros, dt):
+    """Every schedule, both activation types, with and without pre-scaled
+    zero-points (fp16 with zero-points on every tensor-core schedule)."""
     w4 = gpu_lib
-    d = w4synth.gen_w4a16(40, 384, 1024, act_dtype=torch.bfloat16,
+    d = w4synth.gen_w4a16(40, 384, 1024, act_dtype=dt,
                           wtype=w4.UINT4 if zeros else w4.UINT4B8, layout=w4.KN_SEQ,
                           group_size=128, zeros=zeros, seed=3)
     got = run_w4a16(w4, d, sched(w4, name))
     ref, absref = oracle_w4a16(d)
-    assert_within(got.double().numpy(), ref, absref, "bf16", f"bf16 {name} zeros={zeros}")
+    assert_within(got.double().numpy(), ref, absref, fmt(dt), f"{fmt(dt)} {name} zeros={zeros}")
+
+
+@pytest.mark.parametrize("M", [256, 1000])
+@pytest.mark.parametrize("name", ["tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp"])
+def test_w4a16_f16_zero_points_large_m(gpu_lib, name, M):
+    """fp16 activations with uint4 + pre-scaled zero-points on the wide
+    tensor-core tiles (the large-M path), ragged N, several K groups."""
+    w4 = gpu_lib
+    d = w4synth.gen_w4a16(M, 1160, 2048, act_dtype=torch.float16, wtype=w4.UINT4,
+                          layout=w4.NK_EXLLAMA, group_size=128, zeros=True, seed=M + 7)
+    got = run_w4a16(w4, d, sched(w4, name))
+    rows, cols = samples(M, d["N"], count=384, seed=M)
+    sub = got[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
+    ref, absref = oracle.w4a16_elems(d["a"], d["w"], d["layout"], d["wtype"], d["s"], d["z"], 128,
+                                     d["K"], d["N"], rows, cols)
+    assert_within(sub, ref, absref, "f16", f"f16 zero-points {name} M={M}")
 
 
 @pytest.mark.parametrize("M,N,K,gs,dt", [
@@ -162,18 +185,22 @@ def test_ds_ragged(gpu_lib, name, M, N, K, gs, dt):
     assert_within(got.double().numpy(), ref, absref, fmt(dt), f"{name} {M}x{N}x{K}")
 
 
-def test_w4a16_power_of_two_scales_exact(gpu_lib):
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("name", ["default", "ds8_sk", "ds16_sk", "ds32_sk", "dk16_sk", "tc16_sk",
+                                  "tc64_sk", "simt"])
+def test_w4a16_power_of_two_scales_exact(gpu_lib, dt, name):
     # exact products and sums: the GPU output must equal the exact result
-    # rounded once (to nearest even) to bf16
+    # rounded once (to nearest even) to the output type.  The activations are
+    # small integers, so the fp16 staging of the streamed schedule (odd pairs
+    # divided by 16) is exact too.
     w4 = gpu_lib
-    M, N, K = 16, 256, 512
-    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4B8, group_size=128,
-                          seed=5)
+    M, N, K = 8, 256, 512
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=dt, wtype=w4.UINT4B8, group_size=128, seed=5)
     d["s"] = torch.full_like(d["s"], 0.0625)
-    d["a"] = torch.randint(-4, 5, (M, K), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
-    got = run_w4a16(w4, d)
+    d["a"] = torch.randint(-4, 5, (M, K), generator=torch.Generator().manual_seed(5)).to(dt)
+    got = run_w4a16(w4, d, -1 if name == "default" else sched(w4, name))
     ref, _ = oracle_w4a16(d)
-    assert torch.equal(got, torch.from_numpy(ref).to(torch.bfloat16))
+    assert torch.equal(got, torch.from_numpy(ref).to(dt))
 
 
 def test_w4a16_zero_point_eight_equals_symmetric(gpu_lib):
@@ -199,9 +226,11 @@ def test_decode_sweep_llama3_8b(gpu_lib, N, K, M):
     assert_within(got[rows, cols], ref, absref, "bf16", f"decode {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("N,K,M", [(57344, 8192, 4096), (8192, 28672, 4096),
-                                   (57344, 8192, 16384)])
+@pytest.mark.parametrize("N,K", w4synth.PREFILL_SHAPES)
+@pytest.mark.parametrize("M", w4synth.PREFILL_M)
 def test_prefill_llama3_70b(gpu_lib, N, K, M):
+    """Every (N, K) x M point of the Llama-3-70B MLP prefill workload, on
+    sampled elements that include the last row and column tiles."""
     w4 = gpu_lib
     d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4B8,
                           layout=w4.NK_EXLLAMA, group_size=128, zeros=False, seed=0)
