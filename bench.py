@@ -271,27 +271,35 @@ def capture(fn):
     return g
 
 
+CHAIN = 16  # GEMMs per timing graph
+
+
 def time_isolated(fns, reps, stream, eager=False):
-    """Microseconds per launch of one GEMM: a graph per rotated copy, `reps`
-    replays round-robin between CUDA events on the launching stream."""
+    """Microseconds per GEMM of one shape: one graph holding CHAIN (or more)
+    back-to-back launches that cycle through the rotated copies, as a decode
+    step runs them (launch gaps between graphs and host launch costs stay out
+    of the figure), replayed between CUDA events on the launching stream;
+    `reps` GEMMs in all (at least two replays)."""
     for f in fns:  # eager first: kernel attributes are set outside any capture
         f()
     torch.cuda.synchronize()
-    if eager:
-        runs = fns
+    L = max(CHAIN, len(fns))
+    seq = [fns[i % len(fns)] for i in range(L)]
+    if eager:  # plain launches (profilers); host-bound for small GEMMs
+        run = lambda: [f() for f in seq]
     else:
-        graphs = [capture(f) for f in fns]
-        runs = [g.replay for g in graphs]
-    for r in runs:
-        r()
+        g = capture(lambda: [f() for f in seq])
+        run = g.replay
+    run()
     torch.cuda.synchronize()
+    n_rep = max(2, reps // L)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for i in range(reps):
-        runs[i % len(runs)]()
+    for _ in range(n_rep):
+        run()
     a1.record(stream)
     torch.cuda.synchronize()
-    return a0.elapsed_time(a1) * 1e3 / reps
+    return a0.elapsed_time(a1) * 1e3 / (n_rep * L)
 
 
 def extra_workloads(w4, dev, stream, pk, reps, eager=False):
@@ -313,8 +321,9 @@ def extra_workloads(w4, dev, stream, pk, reps, eager=False):
         cp = [(b, sg, s_ch, x["a"].to(dev), x["s_tok"].to(dev))]
         cp += [tuple(t.clone() for t in cp[0]) for _ in range(R - 1)]
         o = torch.empty((M, N), dtype=torch.float16, device=dev)
+        ws = w4.workspace(dev, w4.workspace_size(M, N, K, torch.int8, 128))
         fns = [lambda c=c, M=M: w4.gemm(c[3], c[0], e["wtype"], N, scales=c[1], group_size=128,
-                                       token_scales=c[4], channel_scales=c[2], out=o)
+                                       token_scales=c[4], channel_scales=c[2], out=o, ws=ws)
                for c in cp]
         us = time_isolated(fns, reps, stream, eager)
         ent = roofline_entry(us, flops(M), w4a8_g128_bytes(M), pk)
@@ -336,8 +345,9 @@ def extra_workloads(w4, dev, stream, pk, reps, eager=False):
             base = (b, s, z, a_all[:M].contiguous())
             cp = [base] + [tuple(t.clone() for t in base) for _ in range(R - 1)]
             o = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+            ws = w4.workspace(dev, w4.workspace_size(M, n, k, torch.bfloat16, 128))
             fns = [lambda c=c: w4.gemm(c[3], c[0], d["wtype"], n, scales=c[1], zeros=c[2],
-                                       group_size=128, out=o) for c in cp]
+                                       group_size=128, out=o, ws=ws) for c in cp]
             us = time_isolated(fns, reps, stream, eager)
             ent = roofline_entry(us, flops(M, n, k), nb, pk)
             ent.update(M=M, N=n, K=k, copies=R,
@@ -356,7 +366,9 @@ def extra_workloads(w4, dev, stream, pk, reps, eager=False):
         base = (b, d["s"].to(dev), d["a"].to(dev))
         cp = [base, tuple(t.clone() for t in base)]
         o = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
-        fns = [lambda c=c: w4.gemm(c[2], c[0], d["wtype"], n, scales=c[1], group_size=128, out=o)
+        ws = w4.workspace(dev, w4.workspace_size(M, n, k, torch.bfloat16, 128))
+        fns = [lambda c=c: w4.gemm(c[2], c[0], d["wtype"], n, scales=c[1], group_size=128, out=o,
+                                   ws=ws)
                for c in cp]
         us = time_isolated(fns, max(5, reps // 4), stream, eager)
         ent = roofline_entry(us, flops(M, n, k), w4a16_bytes(M, n, k, zeros=False), pk)

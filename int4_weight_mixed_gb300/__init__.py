@@ -162,8 +162,14 @@ def workspace(device, nbytes: int) -> torch.Tensor:
     """A zero-filled workspace of at least nbytes, cached per (device, stream).
 
     Calls on the same stream are ordered, so sharing is safe; the library
-    leaves its counters at zero after every call."""
+    leaves its counters at zero after every call.  Not available while the
+    stream is capturing a CUDA graph: an allocation there would come from the
+    graph's private pool and its zero-fill would be recorded into the graph,
+    so callers that capture pass a workspace allocated beforehand."""
     dev = torch.device(device)
+    if torch.cuda.is_current_stream_capturing():
+        raise RuntimeError("w4: pass ws= (allocated before capture) to calls captured in a "
+                           "CUDA graph")
     key = (dev.index, _stream(dev))
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < nbytes:

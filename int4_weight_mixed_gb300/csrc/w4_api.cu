@@ -48,6 +48,8 @@ const Schedule kSchedules[] = {
     {"ds8_sk", kEngineDs, 8, kStreamK, 1},            {"ds16_sk", kEngineDs, 16, kStreamK, 1},
     {"tc256_kp", kEngineTc, 256, kSplitK, 1},
     {"ds32_sk", kEngineDs, 32, kStreamK, 1},
+    {"gv8_cl", kEngineGv, 8, kSplitK, 1},             {"gv16_cl", kEngineGv, 16, kSplitK, 1},
+    {"gv32_cl", kEngineGv, 32, kSplitK, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 
@@ -81,7 +83,7 @@ bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs
     size_t wp, wt;  // and the staged activations of a unit fit in shared memory
     return make_dk_plan(si, mode, M, N, K, &wp, &wt).smem_bytes <= kMaxDynSmem;
   }
-  if (sc.engine == kEngineDs)  // also bulk copies of 16-byte-multiple scale rows
+  if (sc.engine == kEngineDs || sc.engine == kEngineGv)  // also bulk copies of 16-byte-multiple scale rows
     return M <= sc.bm && (gs == K || gs % 128 == 0) && N % 8 == 0 &&
            !(mode == kW4A8 && has_sg && N % 16 != 0);
   if (N % 8 != 0) return false;                      // 16-byte scale rows
@@ -278,13 +280,64 @@ DsPlan make_ds_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
   return p;
 }
 
+// Plan of the clustered skinny-M schedule: the cluster size C (CTAs per
+// 128-column tile, each streaming an equal share of the tile's K blocks) is
+// the smallest that minimizes the K blocks of the busiest CTA while every
+// cluster of the grid is resident at once.
+GvPlan make_gv_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
+  GvPlan p{};
+  p.mode = mode;
+  p.nj = kSchedules[si].bm / 8;
+  p.n_tiles = static_cast<int>((N + kTileN - 1) / kTileN);
+  p.kblocks = static_cast<int>((K + 127) / 128);
+  p.stages = p.nj == 1 ? 4 : 3;
+  p.smem_bytes = gv_smem_bytes(p.nj, mode, p.stages);
+  // resident clusters per cluster size, from the occupancy calculator when a
+  // device is present (cached per mode, row tiles and size), else from the
+  // design's CTAs per SM
+  static std::mutex mu;
+  static int cache[3][3][17];  // resident clusters + 1 (0: not yet queried)
+  const int mi = mode, ni = p.nj == 1 ? 0 : p.nj == 2 ? 1 : 2;
+  const int per_sm = gv_ctas_per_sm(p.nj);
+  const int sms = sm_count();
+  int best_c = 1, best_nkb = p.kblocks;
+  for (int C = 1; C <= 16 && C <= p.kblocks; ++C) {
+    int clusters;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (cache[mi][ni][C] == 0) {
+        const int q = gv_max_clusters(mode, p.nj, C, p.smem_bytes);
+        cache[mi][ni][C] = (q >= 0 ? q : sms * per_sm / C) + 1;
+      }
+      clusters = cache[mi][ni][C] - 1;
+    }
+    if (static_cast<int64_t>(p.n_tiles) > clusters) continue;  // more than one wave
+    const int nkb = (p.kblocks + C - 1) / C;
+    if (nkb < best_nkb) {
+      best_nkb = nkb;
+      best_c = C;
+    }
+  }
+  p.cluster = best_c;
+  p.grid = p.n_tiles * p.cluster;
+  (void)M;
+  return p;
+}
+
 int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
-  // skinny M (up to 32 rows with the streamed schedule, 16 with the
-  // register-fed one where the streamed one cannot run: N not a multiple of
-  // 8): warp-level MMAs on dequantized weights
-  for (int eng : {kEngineDs, kEngineDk})
+  // skinny M (up to 32 rows with the clustered or streamed schedule, 16 with
+  // the register-fed one where neither can run: N not a multiple of 8):
+  // warp-level MMAs on dequantized weights
+  // The clustered schedule (one launch) wins while its fixed costs dominate:
+  // up to 16 rows on at most 16 MiB of packed weights; the streamed one
+  // (stream-K with its own reduction launch) keeps more bytes in flight per
+  // SM on larger weights.
+  const bool small_w = K * N / 2 <= (int64_t{16} << 20);
+  for (int eng : {kEngineGv, kEngineDs, kEngineDk})
     for (int si = 1; si < kNumSchedules; ++si)
-      if (kSchedules[si].engine == eng && schedule_fits(si, mode, M, N, K, gs, has_sg))
+      if (kSchedules[si].engine == eng &&
+          !(eng == kEngineGv && (kSchedules[si].bm > 16 || !small_w)) &&
+          schedule_fits(si, mode, M, N, K, gs, has_sg))
         return si;
   int bm = 16;
   while (bm < M && bm < 256) bm *= 2;
@@ -400,6 +453,7 @@ size_t ws_needed(int si, const Problem& pr) {
     return wt;
   }
   if (kSchedules[si].engine == kEngineDs) return make_ds_plan(si, pr.mode, pr.M, pr.N, pr.K).ws_total;
+  if (kSchedules[si].engine == kEngineGv) return kWsHeader;  // the status word only
   return make_plan(si, pr.mode, pr.M, pr.N, pr.K, pr.gs).ws_total;
 }
 
@@ -562,6 +616,48 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
               dp.kblocks, dp.sb, dp.stages, dp.grid, dp.max_segs, dp.smem_bytes);
     cudaError_t e = launch_ds(dp, a, args, ws + dp.ws_prep, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "ds launch");
+  }
+
+  if (kSchedules[si].engine == kEngineGv) {
+    GvPlan gp = make_gv_plan(si, pr.mode, M, N, K);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    CUtensorMap amap;
+    CUresult r;
+    const cuuint32_t rows = static_cast<cuuint32_t>(8 * gp.nj);
+    if (pr.mode == kW4A8) {
+      // int8 [M][K]: one box of 128 K x all rows per K block
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+      const cuuint32_t box[2] = {128, rows};
+      const cuuint32_t estr[2] = {1, 1};
+      r = enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      // 16-bit [M][K] as (k % 64, m, k / 64): one box {64, rows, 2} per K block
+      const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(M),
+                                  static_cast<cuuint64_t>(K / kStageK)};
+      const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+      const cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), rows, 2};
+      const cuuint32_t estr[3] = {1, 1, 1};
+      r = enc(&amap,
+              pr.mode == kW4A16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              3, const_cast<void*>(a), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS)
+      return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed (%d)", (int)r);
+    static const bool debug = getenv("W4_DEBUG") != nullptr;
+    if (debug)
+      fprintf(stderr, "w4: %s M=%lld N=%lld K=%lld nj=%d tiles=%d kblocks=%d cluster=%d "
+                      "stages=%d grid=%d smem=%zu\n",
+              kSchedules[si].name, (long long)M, (long long)N, (long long)K, gp.nj, gp.n_tiles,
+              gp.kblocks, gp.cluster, gp.stages, gp.grid, gp.smem_bytes);
+    cudaError_t e = launch_gv(gp, amap, args, s);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "gv launch");
   }
 
   TcPlan plan = make_plan(si, pr.mode, M, N, K, pr.gs);

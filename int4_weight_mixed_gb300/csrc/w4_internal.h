@@ -49,7 +49,7 @@ constexpr size_t kCounterBytes = 64 * 1024;
 
 enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
 
-enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2, kEngineDs = 3 };
+enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2, kEngineDs = 3, kEngineGv = 4 };
 enum Decomp { kDataParallel = 0, kStreamK = 1, kSplitK = 2 };
 
 struct Schedule {
@@ -143,6 +143,23 @@ struct DsPlan {
   size_t ws_partials, ws_prep, ws_total;  // workspace byte offsets / size
 };
 
+// Clustered skinny-M schedule (one launch: each 128-column tile split along K
+// over a cluster of `cluster` CTAs, reduced through distributed shared
+// memory).
+// CTAs per SM of the clustered skinny-M kernel: four for up to 8 rows, three
+// for up to 16, two for up to 32
+__host__ __device__ constexpr int gv_ctas_per_sm(int nj) { return nj == 1 ? 4 : nj == 2 ? 3 : 2; }
+struct GvPlan {
+  int mode;
+  int nj;          // 8-row activation tiles: M <= 8 * nj
+  int n_tiles;     // 128-column weight tiles
+  int kblocks;     // 128-wide K blocks: ceil(K / 128)
+  int cluster;     // CTAs per tile (cluster size, 1..16)
+  int stages;      // shared-memory pipeline stages
+  int grid;        // n_tiles * cluster
+  size_t smem_bytes;
+};
+
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_prepack(const int32_t* w_q, int wtype, int layout, int64_t K, int64_t N,
                            uint8_t* out, cudaStream_t s);
@@ -160,6 +177,10 @@ cudaError_t launch_ds(const DsPlan& plan, const void* a, const TcArgs& args, uin
                       cudaStream_t s);
 size_t ds_smem_bytes(int sb, int nj, int m, int stages);
 size_t ds_prep_bytes(int nj, int m, int kblocks);
+size_t gv_smem_bytes(int nj, int mode, int stages);
+int gv_max_clusters(int mode, int nj, int C, size_t smem);
+cudaError_t launch_gv(const GvPlan& plan, const CUtensorMap& amap, const TcArgs& args,
+                      cudaStream_t s);
 size_t tc_stage_bytes(int bm, int nsub, int nt);
 size_t tc_smem_bytes(int bm, int nsub, int nt, int stages);
 int tc_max_stages(int bm, int nsub, int nt);

@@ -45,7 +45,10 @@ def test_default_heuristic(lib):
     name = lambda M, N, K, dt, g: w4.schedule_names()[w4.default_schedule(M, N, K, dt, g)]
     assert name(1, 8192, 21760, torch.int8, -1) == "ds8_sk"
     assert name(8, 8192, 21760, torch.int8, 128) == "ds8_sk"
-    assert name(16, 4096, 4096, torch.bfloat16, 128) == "ds16_sk"
+    assert name(16, 4096, 4096, torch.bfloat16, 128) == "gv16_cl"  # 8 MiB of weights: one launch
+    assert name(1, 6144, 4096, torch.bfloat16, 128) == "gv8_cl"
+    assert name(1, 28672, 4096, torch.bfloat16, 128) == "ds8_sk"  # 56 MiB: streamed
+    assert name(12, 4096, 14336, torch.bfloat16, 128) == "ds16_sk"
     assert name(16, 4096, 4096, torch.bfloat16, 64) == "tc16_sk"   # group 64 splits a K block
     assert name(32, 8192, 21760, torch.int8, -1) == "ds32_sk"
     assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"

@@ -21,7 +21,9 @@ ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_s
        "tc128x2_sk", "tc128x2_dp", "tc128x2_kp"]
 DK = ["dk8_sk", "dk16_sk"]
 DS = ["ds8_sk", "ds16_sk", "ds32_sk"]
-ROWS = {"dk8_sk": 8, "dk16_sk": 16, "ds8_sk": 8, "ds16_sk": 16, "ds32_sk": 32}
+GV = ["gv8_cl", "gv16_cl", "gv32_cl"]
+ROWS = {"dk8_sk": 8, "dk16_sk": 16, "ds8_sk": 8, "ds16_sk": 16, "ds32_sk": 32, "gv8_cl": 8,
+        "gv16_cl": 16, "gv32_cl": 32}
 
 
 def sched(w4, name):
@@ -154,7 +156,7 @@ def test_w4a16_ragged(gpu_lib, M, N, K, gs, dt):
     assert_within(got.double().numpy(), ref, absref, fmt(dt), f"ragged {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("name", DK + DS)
+@pytest.mark.parametrize("name", DK + DS + GV)
 @pytest.mark.parametrize("M", [1, 3, 8, 13, 16, 27, 32])
 @pytest.mark.parametrize("dt,zeros,gs", [(torch.bfloat16, True, 128), (torch.float16, False, 128),
                                           (torch.bfloat16, False, -1), (torch.float16, True, 256)])
@@ -169,7 +171,7 @@ def test_dk_w4a16(gpu_lib, name, M, dt, zeros, gs):
     assert_within(got.double().numpy(), ref, absref, fmt(dt), f"{name} M={M}")
 
 
-@pytest.mark.parametrize("name", DS)
+@pytest.mark.parametrize("name", DS + GV)
 @pytest.mark.parametrize("M,N,K,gs,dt", [
     (5, 200, 576, -1, torch.bfloat16),    # K not a multiple of 128: half-full last block
     (8, 136, 640, 128, torch.float16),    # ragged N, odd number of K blocks
@@ -187,7 +189,7 @@ def test_ds_ragged(gpu_lib, name, M, N, K, gs, dt):
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("name", ["default", "ds8_sk", "ds16_sk", "ds32_sk", "dk16_sk", "tc16_sk",
-                                  "tc64_sk", "simt"])
+                                  "tc64_sk", "simt", "gv8_cl", "gv16_cl", "gv32_cl"])
 def test_w4a16_power_of_two_scales_exact(gpu_lib, dt, name):
     # exact products and sums: the GPU output must equal the exact result
     # rounded once (to nearest even) to the output type.  The activations are
@@ -275,11 +277,13 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
                                   "tc128x2_kp", "tc256_kp", "tc256_sk", "tc256_dp", "dk8_sk",
-                                  "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk"])
+                                  "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk", "gv8_cl", "gv16_cl",
+                                  "gv32_cl"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
-    M = {"dk8_sk": 8, "dk16_sk": 13, "ds8_sk": 7, "ds16_sk": 16, "ds32_sk": 29}.get(name, 40)
+    M = {"dk8_sk": 8, "dk16_sk": 13, "ds8_sk": 7, "ds16_sk": 16, "ds32_sk": 29, "gv8_cl": 5,
+         "gv16_cl": 11, "gv32_cl": 32}.get(name, 40)
     e = w4synth.gen_w4a8(M, 384, 2048, group_size=gs, seed=7)
     acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
     ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, e["K"], e["N"])
@@ -301,7 +305,8 @@ def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
     a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(0)).to(torch.int8)
     sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
     e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
-    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk", "ds8_sk", "tc256_sk", "tc256_dp") + (
+    names = ("tc16_sk", "tc128_dp", "simt", "dk8_sk", "ds8_sk", "tc256_sk", "tc256_dp", "gv8_cl",
+             "gv32_cl") + (
         ("tc128x2_kp", "tc256_kp") if gs == -1 else ())
     for name in names:
         acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
@@ -394,6 +399,30 @@ def test_stream_k_many_contributors(gpu_lib, name):
     assert torch.equal(o1, o2)  # partial sums are added in K order
     ref, absref = oracle_w4a16(d)
     assert_within(o1.double().numpy(), ref, absref, "bf16", f"{name} many contributors")
+
+
+@pytest.mark.parametrize("name", GV)
+@pytest.mark.parametrize("N,K", [(128, 32768), (200, 21760), (1032, 4160), (8, 64)])
+def test_gv_cluster_reduction(gpu_lib, name, N, K):
+    """The clustered schedule splits each 128-column tile's K blocks over up
+    to 16 CTAs and adds their partial sums through distributed shared memory
+    in K order: int32 bit-exact (W4A8 per-channel and g128), bf16 within the
+    bound and bitwise repeatable; ragged N, K not a multiple of 128, a single
+    64-wide K block."""
+    w4 = gpu_lib
+    M = ROWS[name] - 3
+    for gs in ([-1, 128] if K % 128 == 0 and N % 16 == 0 else [-1]):
+        e = w4synth.gen_w4a8(M, N, K, group_size=gs, seed=N + K)
+        got = run_w4a8(w4, e, torch.int32, schedule=sched(w4, name))
+        ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, K, N)
+        assert np.array_equal(got.numpy().astype(np.int64), ref), f"{name} gs={gs}"
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4,
+                          group_size=128 if K % 128 == 0 else -1, zeros=True, seed=N + K + 1)
+    o1 = run_w4a16(w4, d, schedule=sched(w4, name))
+    o2 = run_w4a16(w4, d, schedule=sched(w4, name))
+    assert torch.equal(o1, o2)
+    ref, absref = oracle_w4a16(d)
+    assert_within(o1.double().numpy(), ref, absref, "bf16", f"{name} {N}x{K}")
 
 
 def test_misaligned_workspace_rejected(gpu_lib):
