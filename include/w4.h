@@ -159,11 +159,40 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
                      const float* ch_scales, void* out, int out_type, void* workspace,
                      size_t workspace_bytes, void* stream, int schedule);
 
+/* w4_gemm_ex with a bias added to every output row ([RDNA]
+ * _rdna_hybrid_w4a16_apply_impl: the layer bias is added to the product).
+ *   bias  [N] device array of the output type (fp16 / bf16 for W4A16, fp16
+ *         for W4A8), or NULL (then this is exactly w4_gemm_ex).  It is added
+ *         in fp32 to the product before the single rounding to the output
+ *         type: W4A16 out = round(sum_k a*w_hat + bias[n]); W4A8
+ *         out = fp16_rn((float)acc * s_tok[m] * s_ch[n] + bias[n]).
+ * Errors as w4_gemm_ex, plus INVALID_ARGUMENT for a bias with the raw int32
+ * output (out_type W4_S32) or a bias not aligned to 2 bytes.  With K == 0
+ * every output is its column's bias. */
+w4_status w4_gemm_bias(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                       int wtype, int64_t N, const void* b_scales, int scale_type,
+                       const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                       const float* ch_scales, const void* bias, void* out, int out_type,
+                       void* workspace, size_t workspace_bytes, void* stream, int schedule);
+
 /* Schedules: their count, names, and the one the default heuristic picks
  * for a problem (-1 when none can run it). */
 int w4_num_schedules(void);
 const char* w4_schedule_name(int schedule);
 int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size);
+
+/* Install a per-shape override of the default heuristic ([MR] Code
+ * Generation: per-shape schedule choices; [RDNA] a per-shape override
+ * table): problems of this activation type with M in [m_lo, m_hi] and
+ * exactly this N, K and group_size (-1 = K) run `schedule` by default,
+ * when it can run them (else the heuristic decides).  A later entry for the
+ * same key replaces the earlier one; schedule -1 removes it.  Entries
+ * installed here are consulted before the library's built-in table, which
+ * holds measured exceptions to the heuristic.  Host-side only; thread-safe;
+ * at most 256 entries (UNSUPPORTED beyond).  Errors: INVALID_ARGUMENT for
+ * a bad a_type, range, shape, group size or schedule index. */
+w4_status w4_override_schedule(int a_type, int64_t m_lo, int64_t m_hi, int64_t N, int64_t K,
+                               int64_t group_size, int schedule);
 
 /* Synchronize `stream`, then report (and clear) a device-side timeout that
  * a kernel recorded in `workspace`: W4_ERR_TIMEOUT, else W4_OK.  On a

@@ -77,11 +77,15 @@ def load():
         lib.w4_gemm.restype = i32
         lib.w4_gemm_ex.argtypes = gemm_args + [i32]
         lib.w4_gemm_ex.restype = i32
+        lib.w4_gemm_bias.argtypes = gemm_args[:13] + [p] + gemm_args[13:] + [i32]
+        lib.w4_gemm_bias.restype = i32
         lib.w4_num_schedules.restype = i32
         lib.w4_schedule_name.argtypes = [i32]
         lib.w4_schedule_name.restype = ctypes.c_char_p
         lib.w4_default_schedule.argtypes = [i64, i64, i64, i32, i64]
         lib.w4_default_schedule.restype = i32
+        lib.w4_override_schedule.argtypes = [i32, i64, i64, i64, i64, i64, i32]
+        lib.w4_override_schedule.restype = i32
         lib.w4_quantize_per_token.argtypes = [p, i32, i64, i64, p, p, p]
         lib.w4_quantize_per_token.restype = i32
         lib.w4_check_status.argtypes = [p, sz, p]
@@ -191,22 +195,74 @@ def default_schedule(M: int, N: int, K: int, a_dtype: torch.dtype, group_size: i
     return load().w4_default_schedule(M, N, K, _DTYPE_CODE[a_dtype], group_size)
 
 
+def override_schedule(a_dtype: torch.dtype, m_lo: int, m_hi: int, N: int, K: int,
+                      group_size: int, schedule) -> None:
+    """w4_override_schedule: problems of this shape with M in [m_lo, m_hi]
+    run `schedule` (index or name) by default; None / -1 removes the entry."""
+    if schedule is None:
+        schedule = -1
+    elif isinstance(schedule, str):
+        schedule = schedule_names().index(schedule)
+    _check(load().w4_override_schedule(_DTYPE_CODE[a_dtype], m_lo, m_hi, N, K, group_size,
+                                       schedule), "w4_override_schedule")
+
+
+def autotune(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int, install: bool = True,
+             reps: int = 20, **kw) -> dict:
+    """Time every schedule that can run this problem (the arguments of
+    gemm()) with CUDA events on the current stream, and, with install=True,
+    make the fastest the default for exactly this shape (w4_override_schedule
+    for this M).  Returns {schedule name: microseconds per call}.  The calls
+    write `out` (or a scratch output) and use `ws` (or the cached workspace)."""
+    M, K = a.shape
+    names = schedule_names()
+    kw = dict(kw)
+    kw.pop("schedule", None)
+    group_size = kw.get("group_size", -1)
+    if kw.get("ws") is None:
+        kw["ws"] = workspace(a.device, workspace_size(M, N, K, a.dtype, group_size))
+    times = {}
+    stream = torch.cuda.current_stream(a.device)
+    for si, name in enumerate(names):
+        if name == "simt" and M * N * K > (1 << 31):
+            continue  # the CUDA-core schedule is a correctness path
+        try:
+            gemm(a, b_packed, wtype, N, schedule=si, **kw)  # warm-up; UNSUPPORTED -> skip
+        except W4Error as e:
+            if e.status == ERR_UNSUPPORTED:
+                continue
+            raise
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gemm(a, b_packed, wtype, N, schedule=si, **kw)
+        e1.record(stream)
+        e1.synchronize()
+        times[name] = e0.elapsed_time(e1) * 1e3 / reps
+    if install and times:
+        best = min(times, key=times.get)
+        override_schedule(a.dtype, M, M, N, K, group_size, best)
+    return times
+
+
 def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
          scales: torch.Tensor | None = None, zeros: torch.Tensor | None = None,
          group_size: int = -1, token_scales: torch.Tensor | None = None,
          channel_scales: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
          out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-         schedule: int = -1) -> torch.Tensor:
-    """w4_gemm / w4_gemm_ex: out[M,N] = a[M,K] x dequant(W).
+         schedule: int = -1, bias: torch.Tensor | None = None) -> torch.Tensor:
+    """w4_gemm_ex / w4_gemm_bias: out[M,N] = a[M,K] x dequant(W) (+ bias).
 
     W4A16: a fp16/bf16, scales [G,N] of a's dtype, zeros [G,N] pre-scaled or
     None.  W4A8: a int8, scales = int8 group scales [G,N] or None
     (per-channel), token_scales [M] and channel_scales [N] fp32 for fp16
-    output, or out_dtype=torch.int32 for the raw accumulator.
+    output, or out_dtype=torch.int32 for the raw accumulator.  bias: [N] of
+    the output dtype, added before the output rounding, or None.
     """
     lib = load()
     _dense_on(a.device, a=a, b_packed=b_packed, scales=scales, zeros=zeros,
-              token_scales=token_scales, channel_scales=channel_scales, out=out, ws=ws)
+              token_scales=token_scales, channel_scales=channel_scales, out=out, ws=ws,
+              bias=bias)
     M, K = a.shape
     a_code = _DTYPE_CODE[a.dtype]
     if out_dtype is None:
@@ -217,11 +273,21 @@ def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
     if ws is None:
         ws = workspace(a.device, nbytes)
     scale_code = _DTYPE_CODE[scales.dtype] if scales is not None else a_code
-    st = lib.w4_gemm_ex(_ptr(a), a_code, M, K, _ptr(b_packed), wtype, N, _ptr(scales),
-                        scale_code, _ptr(zeros), group_size, _ptr(token_scales),
-                        _ptr(channel_scales), _ptr(out), _DTYPE_CODE[out_dtype], _ptr(ws),
-                        ws.numel(), _stream(a.device), schedule)
-    _check(st, "w4_gemm")
+    if bias is None:
+        st = lib.w4_gemm_ex(_ptr(a), a_code, M, K, _ptr(b_packed), wtype, N, _ptr(scales),
+                            scale_code, _ptr(zeros), group_size, _ptr(token_scales),
+                            _ptr(channel_scales), _ptr(out), _DTYPE_CODE[out_dtype], _ptr(ws),
+                            ws.numel(), _stream(a.device), schedule)
+        _check(st, "w4_gemm")
+    else:
+        if bias.dtype != out_dtype or bias.numel() != N:
+            raise ValueError(f"bias must be [{N}] of {out_dtype}")
+        st = lib.w4_gemm_bias(_ptr(a), a_code, M, K, _ptr(b_packed), wtype, N, _ptr(scales),
+                              scale_code, _ptr(zeros), group_size, _ptr(token_scales),
+                              _ptr(channel_scales), _ptr(bias), _ptr(out),
+                              _DTYPE_CODE[out_dtype], _ptr(ws), ws.numel(), _stream(a.device),
+                              schedule)
+        _check(st, "w4_gemm_bias")
     return out
 
 

@@ -324,7 +324,59 @@ GvPlan make_gv_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
   return p;
 }
 
+// Per-shape overrides of the default heuristic ("Machete Readme", "Code
+// Generation": a default heuristic with per-shape exceptions; the vLLM
+// "rdna_hybrid_w4a16" page keeps a table of them, _GFX1X_PREFILL_OVERRIDES).
+// Built-in entries come from A/B timings of the candidate schedules on
+// GB300 (graphs of 16 back-to-back launches over rotated weight copies, more
+// than 2x L2 between two reads of a copy); entries installed at run time
+// (w4_override_schedule) are consulted first.  M in [m_lo, m_hi]; group_size
+// as resolved (K for one group per column).
+struct Override {
+  int mode;
+  int64_t m_lo, m_hi, N, K, gs;
+  int schedule;
+};
+const char* const kBuiltinOverrideNames[] = {"tc256_sk", "tc256_sk"};
+const Override kBuiltinOverrides[] = {
+    // W4A16 bf16, Llama-3-70B MLP down projection (N=8192, K=28672):
+    // tc256_sk 1619 us vs tc256_dp 1674 us at M=4096, 3296 vs 3316 at 8192
+    {kW4A16_BF16, 4096, 8192, 8192, 28672, 128, -1},
+    // W4A16 bf16, Llama-3-70B MLP gate/up (N=57344, K=8192):
+    // tc256_sk 3447.5 vs 3448.4 us at M=4096, 6815.6 vs 6820.9 at 8192
+    {kW4A16_BF16, 4096, 8192, 57344, 8192, 128, -1},
+};
+constexpr int kMaxOverrides = 256;
+std::mutex g_ov_mutex;
+Override g_overrides[kMaxOverrides];
+int g_num_overrides = 0;
+
+int schedule_index(const char* name) {
+  for (int i = 0; i < kNumSchedules; ++i)
+    if (strcmp(kSchedules[i].name, name) == 0) return i;
+  return -1;
+}
+
+bool override_matches(const Override& o, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) {
+  return o.mode == mode && M >= o.m_lo && M <= o.m_hi && N == o.N && K == o.K && gs == o.gs;
+}
+
+// The schedule an override names for this problem, or -1.
+int override_for(int mode, int64_t M, int64_t N, int64_t K, int64_t gs) {
+  {
+    std::lock_guard<std::mutex> lock(g_ov_mutex);
+    for (int i = g_num_overrides - 1; i >= 0; --i)  // the latest installed wins
+      if (override_matches(g_overrides[i], mode, M, N, K, gs)) return g_overrides[i].schedule;
+  }
+  for (size_t i = 0; i < sizeof(kBuiltinOverrides) / sizeof(kBuiltinOverrides[0]); ++i)
+    if (override_matches(kBuiltinOverrides[i], mode, M, N, K, gs))
+      return schedule_index(kBuiltinOverrideNames[i]);
+  return -1;
+}
+
 int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
+  const int ov = override_for(mode, M, N, K, gs);
+  if (ov >= 0 && schedule_fits(ov, mode, M, N, K, gs, has_sg)) return ov;
   // skinny M (up to 32 rows with the clustered or streamed schedule, 16 with
   // the register-fed one where neither can run: N not a multiple of 8):
   // warp-level MMAs on dequantized weights
@@ -517,6 +569,32 @@ int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t gro
   return default_schedule_impl(mode_of(a_type), M, N, K, gs, gs != K);
 }
 
+w4_status w4_override_schedule(int a_type, int64_t m_lo, int64_t m_hi, int64_t N, int64_t K,
+                               int64_t group_size, int schedule) {
+  if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8)
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16, W4_BF16 or W4_S8");
+  if (m_lo < 1 || m_hi < m_lo || N < 1 || K < 1 || K % kStageK != 0)
+    return fail(W4_ERR_INVALID_ARGUMENT, "bad M range or shape");
+  const int64_t gs = group_size == -1 ? K : group_size;
+  if (gs <= 0 || K % gs != 0) return fail(W4_ERR_INVALID_ARGUMENT, "bad group_size");
+  if (schedule >= kNumSchedules)
+    return fail(W4_ERR_INVALID_ARGUMENT, "bad schedule index");
+  const int mode = mode_of(a_type);
+  std::lock_guard<std::mutex> lock(g_ov_mutex);
+  // drop earlier entries for exactly this range, then add (schedule >= 0)
+  int n = 0;
+  for (int i = 0; i < g_num_overrides; ++i) {
+    const Override& o = g_overrides[i];
+    if (!(o.mode == mode && o.m_lo == m_lo && o.m_hi == m_hi && o.N == N && o.K == K && o.gs == gs))
+      g_overrides[n++] = o;
+  }
+  g_num_overrides = n;
+  if (schedule < 0) return W4_OK;
+  if (g_num_overrides == kMaxOverrides) return fail(W4_ERR_UNSUPPORTED, "override table full");
+  g_overrides[g_num_overrides++] = Override{mode, m_lo, m_hi, N, K, gs, schedule};
+  return W4_OK;
+}
+
 size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size) {
   Problem pr{};
   pr.mode = mode_of(a_type);
@@ -535,22 +613,35 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
   return need;
 }
 
-w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
-                     int wtype, int64_t N, const void* b_scales, int scale_type,
-                     const void* b_zeros, int64_t group_size, const float* a_token_scales,
-                     const float* ch_scales, void* out, int out_type, void* workspace,
-                     size_t workspace_bytes, void* stream, int schedule) {
+}  // extern "C"
+
+namespace {
+w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                    int wtype, int64_t N, const void* b_scales, int scale_type,
+                    const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                    const float* ch_scales, const void* bias, void* out, int out_type,
+                    void* workspace, size_t workspace_bytes, void* stream, int schedule) {
   Problem pr{};
   w4_status st = validate(a, a_type, M, K, b_packed, wtype, N, b_scales, scale_type, b_zeros,
                           group_size, a_token_scales, ch_scales, out, out_type, pr);
   if (st != W4_OK) return st;
+  if (bias) {
+    if (pr.mode == kW4A8 && out_type == W4_S32)
+      return fail(W4_ERR_INVALID_ARGUMENT, "the raw int32 output takes no bias");
+    if (!aligned_to(bias, 2))
+      return fail(W4_ERR_INVALID_ARGUMENT, "bias is not aligned to its element size");
+  }
   if (schedule >= kNumSchedules) return fail(W4_ERR_INVALID_ARGUMENT, "bad schedule index");
   if (M == 0 || N == 0) return W4_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (K == 0) {
+  if (K == 0 && !bias) {
     const size_t esz = (pr.mode == kW4A8 && out_type == W4_S32) ? 4 : 2;
     cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(M) * N * esz, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "memset");
+  }
+  if (K == 0) {  // every output is its column's bias
+    cudaError_t e = launch_bias_rows(pr.mode, M, N, bias, a_token_scales != nullptr, out, s);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "bias launch");
   }
   int si = schedule;
   const bool forced = schedule >= 0;
@@ -577,6 +668,7 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   args.s_tok = a_token_scales;
   args.s_ch = ch_scales;
   args.out = out;
+  args.bias = bias;
   args.out_s32 = (pr.mode == kW4A8 && out_type == W4_S32) ? 1 : 0;
   args.wbias = (wtype == W4_UINT4) ? 0 : 8;
   args.M = M;
@@ -741,6 +833,30 @@ w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void
   }
   cudaError_t e = launch_tc(plan, amap, smap, zmap, args, s);
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                     int wtype, int64_t N, const void* b_scales, int scale_type,
+                     const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                     const float* ch_scales, void* out, int out_type, void* workspace,
+                     size_t workspace_bytes, void* stream, int schedule) {
+  return gemm_impl(a, a_type, M, K, b_packed, wtype, N, b_scales, scale_type, b_zeros,
+                   group_size, a_token_scales, ch_scales, nullptr, out, out_type, workspace,
+                   workspace_bytes, stream, schedule);
+}
+
+w4_status w4_gemm_bias(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                       int wtype, int64_t N, const void* b_scales, int scale_type,
+                       const void* b_zeros, int64_t group_size, const float* a_token_scales,
+                       const float* ch_scales, const void* bias, void* out, int out_type,
+                       void* workspace, size_t workspace_bytes, void* stream, int schedule) {
+  return gemm_impl(a, a_type, M, K, b_packed, wtype, N, b_scales, scale_type, b_zeros,
+                   group_size, a_token_scales, ch_scales, bias, out, out_type, workspace,
+                   workspace_bytes, stream, schedule);
 }
 
 w4_status w4_gemm(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,

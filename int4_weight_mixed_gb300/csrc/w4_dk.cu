@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "w4_epilogue.cuh"
 #include "w4_internal.h"
 
 namespace w4 {
@@ -375,15 +376,7 @@ __global__ void __launch_bounds__(kDkThreads, 2)
   // ---- epilogue: direct store, or split-K partials + last-arriver reduce
   auto store = [&](int64_t m, int64_t n, float vf, int32_t vi) {
     if (m >= M || n >= N) return;
-    const int64_t o = m * N + n;
-    if (MODE == kW4A8) {
-      if (args.out_s32) static_cast<int32_t*>(args.out)[o] = vi;
-      else
-        static_cast<__half*>(args.out)[o] =
-            __float2half_rn(static_cast<float>(vi) * args.s_tok[m] * args.s_ch[n]);
-    } else {
-      static_cast<T16*>(args.out)[o] = from_f32<T16>(vf);
-    }
+    store_out<MODE>(args, m, n, vf, vi);
   };
   if (p.ksplit == 1) {
 #pragma unroll

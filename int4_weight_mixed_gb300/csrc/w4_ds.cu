@@ -40,6 +40,7 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include "w4_epilogue.cuh"
 #include "w4_internal.h"
 #include "w4_ptx.cuh"
 
@@ -410,15 +411,7 @@ __global__ void __launch_bounds__(DsShape<NJ>::Threads, ds_ctas_per_sm(NJ))
       pc ? (MODE == kW4A8 ? 64 : (1 << 30)) : static_cast<int>(args.group_size / kBlkK);
   auto store = [&](int64_t m, int64_t n, float vf, int32_t vi) {
     if (m >= M || n >= N) return;
-    const int64_t o = m * N + n;
-    if (MODE == kW4A8) {
-      if (args.out_s32) static_cast<int32_t*>(args.out)[o] = vi;
-      else
-        static_cast<__half*>(args.out)[o] =
-            __float2half_rn(static_cast<float>(vi) * args.s_tok[m] * args.s_ch[n]);
-    } else {
-      static_cast<T16*>(args.out)[o] = ds_t16<T16>(vf);
-    }
+    store_out<MODE>(args, m, n, vf, vi);
   };
 
   uint32_t it = 0, cs = 0, cph = 0;  // stage count, it % S, (it / S) & 1
@@ -674,15 +667,7 @@ __global__ void __launch_bounds__(kDsRedThreads) ds_reduce_kernel(const DsPlan p
       else af = sl == 0 ? __uint_as_float(x[q]) : af + __uint_as_float(x[q]);
     }
   }
-  const int64_t o = m * N + n;
-  if (MODE == kW4A8) {
-    if (args.out_s32) static_cast<int32_t*>(args.out)[o] = ai;
-    else
-      static_cast<__half*>(args.out)[o] =
-          __float2half_rn(static_cast<float>(ai) * args.s_tok[m] * args.s_ch[n]);
-  } else {
-    static_cast<T16*>(args.out)[o] = ds_t16<T16>(af);
-  }
+  store_out<MODE>(args, m, n, af, ai);
 }
 
 namespace {

@@ -51,6 +51,7 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include "w4_epilogue.cuh"
 #include "w4_internal.h"
 #include "w4_ptx.cuh"
 
@@ -497,17 +498,7 @@ __global__ void __launch_bounds__(GvShape<NJ>::Threads, gv_ctas_per_sm(NJ))
           for (int e = 0; e < 4; ++e) {
             const int64_t m = j * 8 + 2 * t + (e & 1);
             const int64_t n = n0 + Cols * w + 16 * R + g + 8 * (e >> 1);
-            if (m < M && n < N) {
-              const int64_t o = m * N + n;
-              if (MODE == kW4A8) {
-                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = ires[R][j][e];
-                else
-                  static_cast<__half*>(args.out)[o] = __float2half_rn(
-                      static_cast<float>(ires[R][j][e]) * args.s_tok[m] * args.s_ch[n]);
-              } else {
-                static_cast<T16*>(args.out)[o] = gv_t16<T16>(res[R][j][e]);
-              }
-            }
+            if (m < M && n < N) store_out<MODE>(args, m, n, res[R][j][e], ires[R][j][e]);
           }
     } else {
 #pragma unroll
@@ -541,22 +532,18 @@ __global__ void __launch_bounds__(GvShape<NJ>::Threads, gv_ctas_per_sm(NJ))
       for (int q = 0; q < 16; ++q)
         if (q < C) parts[q] = ld_dsmem(dsmem_addr(local, static_cast<uint32_t>(q)));
       if (n >= N) continue;
-      const int64_t o = static_cast<int64_t>(m) * N + n;
       if (MODE == kW4A8) {
         int32_t a = 0;
 #pragma unroll
         for (int q = 0; q < 16; ++q)
           if (q < C) a += static_cast<int32_t>(parts[q]);
-        if (args.out_s32) static_cast<int32_t*>(args.out)[o] = a;
-        else
-          static_cast<__half*>(args.out)[o] =
-              __float2half_rn(static_cast<float>(a) * args.s_tok[m] * args.s_ch[n]);
+        store_out<MODE>(args, m, n, 0.f, a);
       } else {
         float a = __uint_as_float(parts[0]);
 #pragma unroll
         for (int q = 1; q < 16; ++q)
           if (q < C) a += __uint_as_float(parts[q]);
-        static_cast<T16*>(args.out)[o] = gv_t16<T16>(a);
+        store_out<MODE>(args, m, n, a, 0);
       }
     }
   }

@@ -101,6 +101,7 @@ struct TcArgs {
   const float* s_tok;      // W4A8
   const float* s_ch;       // W4A8
   void* out;
+  const void* bias;        // [N] of the output type, added before rounding, or null
   int out_s32;             // W4A8 raw int32 output
   int wbias;               // 8 for uint4b8 / int4 (offset binary), 0 for uint4
   int64_t M, N, K;
@@ -166,6 +167,9 @@ cudaError_t launch_prepack(const int32_t* w_q, int wtype, int layout, int64_t K,
 cudaError_t launch_unprepack(const uint8_t* packed, int wtype, int layout, int64_t K,
                              int64_t N, int32_t* w_q, cudaStream_t s);
 cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_t s);
+// K == 0 with a bias: out[m][n] = bias[n] (W4A16), fp16_rn(0 * s_tok * s_ch + bias) (W4A8)
+cudaError_t launch_bias_rows(int mode, int64_t M, int64_t N, const void* bias, bool w4a8,
+                             void* out, cudaStream_t s);
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s);
 cudaError_t launch_quant_per_token(bool bf16, const void* a, int64_t M, int64_t K, int8_t* q,
                                    float* s_tok, cudaStream_t s);

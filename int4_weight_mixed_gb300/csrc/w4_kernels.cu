@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "w4_epilogue.cuh"
 #include "w4_internal.h"
 
 namespace w4 {
@@ -141,7 +142,7 @@ __global__ void simt_w4a16_kernel(const T* __restrict__ a, TcArgs args) {
         acc = fmaf(to_f(a[m * K + k0 + j]), to_f(w), acc);
       }
     }
-    static_cast<T*>(args.out)[m * N + n] = from_f<T>(acc);
+    store_out<std::is_same<T, __half>::value ? kW4A16_F16 : kW4A16_BF16>(args, m, n, acc, 0);
   }
 }
 
@@ -163,12 +164,7 @@ __global__ void simt_w4a8_kernel(const int8_t* __restrict__ a, TcArgs args) {
         acc += static_cast<int32_t>(a[m * K + k0 + j]) * v * mul;
       }
     }
-    if (args.out_s32) {
-      static_cast<int32_t*>(args.out)[m * N + n] = acc;
-    } else {
-      float r = static_cast<float>(acc) * args.s_tok[m] * args.s_ch[n];
-      static_cast<__half*>(args.out)[m * N + n] = __float2half_rn(r);
-    }
+    store_out<kW4A8>(args, m, n, 0.f, acc);
   }
 }
 
@@ -198,6 +194,24 @@ cudaError_t launch_unprepack(const uint8_t* packed, int wtype, int layout, int64
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s) {
   int64_t c8 = count / 8;
   a8_to_bf16_kernel<<<grid_for(c8, 256), 256, 0, s>>>(a, c8, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+// K == 0 with a bias: every output element is its column's bias (a product
+// over no K values is zero), rounded to the output type.
+__global__ void bias_rows_kernel(int64_t M, int64_t N, const uint16_t* __restrict__ bias,
+                                 uint16_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < M * N;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = bias[i % N];
+}
+
+cudaError_t launch_bias_rows(int mode, int64_t M, int64_t N, const void* bias, bool w4a8,
+                             void* out, cudaStream_t s) {
+  (void)mode;
+  (void)w4a8;  // 0 * s_tok * s_ch + bias rounds to bias: the output type is the bias type
+  bias_rows_kernel<<<grid_for(M * N, 256), 256, 0, s>>>(
+      M, N, static_cast<const uint16_t*>(bias), static_cast<uint16_t*>(out));
   return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "w4_epilogue.cuh"
 #include "w4_internal.h"
 #include "w4_ptx.cuh"
 
@@ -904,18 +905,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int64_t m = m0 + cc + i;
-            if (nrow < N && m < M) {
-              const int64_t o = m * N + nrow;
-              if (MODE == kW4A8) {
-                const int32_t acc = static_cast<int32_t>(d[i]);
-                if (args.out_s32) static_cast<int32_t*>(args.out)[o] = acc;
-                else
-                  static_cast<__half*>(args.out)[o] = __float2half_rn(
-                      static_cast<float>(acc) * args.s_tok[m] * args.s_ch[nrow]);
-              } else {
-                static_cast<T16*>(args.out)[o] = to_t16<T16>(__uint_as_float(d[i]));
-              }
-            }
+            if (nrow < N && m < M)
+              store_out<MODE>(args, m, nrow, __uint_as_float(d[i]), static_cast<int32_t>(d[i]));
           }
         }
         tc_fence_before();

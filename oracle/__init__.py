@@ -29,6 +29,8 @@ What each function computes, and the page it follows:
   round-to-nearest-even encoding saturated at 448, per-token scales
   amax/448, and the exact fp64 product of decoded activations with int4
   weights.
+* ``add_bias`` — the vLLM API page "rdna_hybrid_w4a16",
+  ``_rdna_hybrid_w4a16_apply_impl``: the layer bias added to the product.
 * ``quant_per_token`` — vLLM PR #6547 "Enable Dynamic Per Token fp8" (one
   activation scale per token, computed from that token at run time) with
   the symmetric int8 activations of pytorch/ao PR #1113: s = amax/127 and
@@ -217,6 +219,19 @@ def w4a8_scale(acc, rows, cols, s_tok, s_ch):
     _load().or_w4a8_scale(acc.shape[0], _ptr(acc), _ptr(rows), _ptr(cols), _ptr(s_tok),
                           _ptr(s_ch), _ptr(ref))
     return ref
+
+
+def add_bias(ref, cols, bias):
+    """The bias step after the product: ref[i] + bias[cols[i]] in fp64 (the
+    bias, fp16 / bf16, converted exactly).  vLLM API page "rdna_hybrid_w4a16",
+    _rdna_hybrid_w4a16_apply_impl: the layer bias is added to the GEMM
+    result.  Works on flat (ref, cols) lists or on a full [M, N] ref (cols
+    None)."""
+    ref = np.asarray(ref, dtype=np.float64)
+    b = _np(bias, np.float64).reshape(-1)
+    if cols is None:
+        return ref + b[np.newaxis, :]
+    return ref + b[_np(cols, np.int64).reshape(-1)]
 
 
 def quant_per_token(a):

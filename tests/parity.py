@@ -41,3 +41,17 @@ def assert_fp16_within_ulp(got, ref, what: str = ""):
         i = np.flatnonzero(bad.ravel())[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} fp16 outputs off by > 1 ulp: got "
                              f"{got.ravel()[i]}, ref {ref.ravel()[i]}")
+
+
+def assert_fp16_near(got, ref, scale, what: str = ""):
+    """W4A8 fp16 output with a bias: within one fp16 ulp of the fp64
+    reference, plus the fp32 rounding of the epilogue (2^-21 of the
+    magnitudes it adds: |acc * s_tok * s_ch| + |bias|), which a bias close to
+    minus the product can expose."""
+    got = np.asarray(got, dtype=np.float64)
+    bound = ulp(ref, "f16") + 2.0 ** -21 * np.asarray(scale, dtype=np.float64)
+    bad = ~(np.abs(got - ref) <= bound)
+    if bad.any():
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} fp16 outputs outside 1 ulp + epilogue "
+                             f"rounding: got {got.ravel()[i]}, ref {ref.ravel()[i]}")

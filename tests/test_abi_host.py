@@ -285,3 +285,34 @@ def test_binding_argtypes_match_the_header(lib):
         assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
         checked += 1
     assert checked >= 10
+
+
+def test_override_table(lib):
+    """Built-in measured exceptions to the heuristic, and entries installed at
+    run time: consulted first, replaced by a later entry for the same key,
+    removed with -1, ignored where the schedule cannot run the shape, and
+    validated on the host."""
+    import torch
+    name = lambda M, N, K, dt, g: w4.schedule_names()[w4.default_schedule(M, N, K, dt, g)]
+    # built-in: Llama-3-70B prefill shapes prefer the stream-K 256-row tiles
+    assert name(4096, 8192, 28672, torch.bfloat16, 128) == "tc256_sk"
+    assert name(8192, 57344, 8192, torch.bfloat16, 128) == "tc256_sk"
+    assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"  # outside the range
+    # installed at run time
+    assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
+    w4.override_schedule(torch.bfloat16, 33, 64, 4096, 4096, 128, "tc128_sk")
+    assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc128_sk"
+    assert name(64, 4096, 4096, torch.float16, 128) == "tc64_sk"     # other dtype: untouched
+    assert name(64, 4096, 4096, torch.bfloat16, -1) == "tc64_sk"     # other group size
+    w4.override_schedule(torch.bfloat16, 33, 64, 4096, 4096, 128, "tc64_sk")
+    assert name(48, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
+    w4.override_schedule(torch.bfloat16, 33, 64, 4096, 4096, 128, "ds8_sk")  # cannot run M=64
+    assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
+    w4.override_schedule(torch.bfloat16, 33, 64, 4096, 4096, 128, None)       # removed
+    assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
+    E = w4.ERR_INVALID_ARGUMENT
+    assert lib.w4_override_schedule(7, 1, 2, 8, 64, -1, 1) == E      # a_type
+    assert lib.w4_override_schedule(1, 5, 2, 8, 64, -1, 1) == E      # empty range
+    assert lib.w4_override_schedule(1, 1, 2, 8, 72, -1, 1) == E      # K % 64
+    assert lib.w4_override_schedule(1, 1, 2, 8, 256, 96, 1) == E     # group size
+    assert lib.w4_override_schedule(1, 1, 2, 8, 64, -1, 99) == E     # schedule index

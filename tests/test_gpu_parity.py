@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import w4synth
-from parity import assert_fp16_within_ulp, assert_within
+from parity import assert_fp16_near, assert_fp16_within_ulp, assert_within
 
 pytestmark = pytest.mark.gpu
 
@@ -577,3 +577,94 @@ def test_quantize_feeds_w4a8(gpu_lib, M):
     refo = oracle.w4a8_scale(ref.reshape(-1), rows.reshape(-1), cols.reshape(-1),
                              rs.astype(np.float64), e["s_ch"])
     assert_fp16_within_ulp(out.cpu().double().numpy().reshape(-1), refo, f"quantized W4A8 M={M}")
+
+
+
+# ------------------------------------------------------------------- bias ---
+# out = round(sum + bias[n]) (W4A16) / fp16_rn(acc * s_tok * s_ch + bias[n]) (W4A8)
+
+BIAS_SCHEDULES = ["simt", "tc16_sk", "tc64_sk", "tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp",
+                  "dk8_sk", "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk", "gv8_cl", "gv16_cl",
+                  "gv32_cl"]
+
+
+@pytest.mark.parametrize("name", BIAS_SCHEDULES)
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_w4a16_bias_every_engine(gpu_lib, name, dt):
+    w4 = gpu_lib
+    M = min(ROWS.get(name, 40), 40) - 1
+    N, K = 392 if not name.startswith("tc") else 384, 1280
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=dt, wtype=w4.UINT4, layout=w4.NK_EXLLAMA,
+                          group_size=128, zeros=True, seed=M + 77)
+    bias = (torch.randn(N, generator=torch.Generator().manual_seed(5)) * 0.5).to(dt)
+    b = w4.prepack_B(d["w"].to(DEV), d["wtype"], d["layout"], K, N)
+    got = w4.gemm(d["a"].to(DEV), b, d["wtype"], N, scales=d["s"].to(DEV), zeros=d["z"].to(DEV),
+                  group_size=128, schedule=sched(w4, name), bias=bias.to(DEV))
+    torch.cuda.synchronize()
+    ref, absref = oracle_w4a16(d)
+    assert_within(got.cpu().double().numpy(), oracle.add_bias(ref, None, bias), absref, fmt(dt),
+                  f"bias {name}")
+
+
+@pytest.mark.parametrize("name", BIAS_SCHEDULES)
+def test_w4a8_bias_every_engine(gpu_lib, name):
+    w4 = gpu_lib
+    M = min(ROWS.get(name, 40), 40) - 2
+    N, K = 384, 2048
+    e = w4synth.gen_w4a8(M, N, K, group_size=128, seed=M + 88)
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], K, N)
+    rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    rows, cols = rows.reshape(-1), cols.reshape(-1)
+    acc = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], 128, K, N).reshape(-1)
+    prod = oracle.w4a8_scale(acc, rows, cols, e["s_tok"], e["s_ch"])
+    # a bias near minus the product in some columns (cancellation), random elsewhere
+    bias = torch.from_numpy(-prod.reshape(M, N)[0]).to(torch.float16)
+    bias[1::2] = (torch.randn(N // 2, generator=torch.Generator().manual_seed(6))).half()
+    got = w4.gemm(e["a"].to(DEV), b, e["wtype"], N, scales=e["sg"].to(DEV), group_size=128,
+                  token_scales=e["s_tok"].to(DEV), channel_scales=e["s_ch"].to(DEV),
+                  schedule=sched(w4, name), bias=bias.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.add_bias(prod, cols, bias)
+    assert_fp16_near(got.cpu().double().numpy().reshape(-1), ref,
+                     np.abs(prod) + np.abs(bias.double().numpy()[cols]), f"bias {name}")
+
+
+def test_bias_k_zero_and_rejections(gpu_lib):
+    w4 = gpu_lib
+    N = 136
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(DEV)
+    b = torch.zeros(1, dtype=torch.uint8, device=DEV)
+    s = torch.ones(1, N, dtype=torch.bfloat16, device=DEV)
+    out = w4.gemm(torch.empty(3, 0, dtype=torch.bfloat16, device=DEV), b, w4.UINT4B8, N,
+                  scales=s, group_size=-1, bias=bias)
+    torch.cuda.synchronize()
+    assert torch.equal(out, bias.expand(3, N))  # a product over no K is zero
+    e = w4synth.gen_w4a8(4, N, 256, group_size=-1, seed=8)
+    bp = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], 256, N)
+    with pytest.raises(w4.W4Error) as ei:  # the raw int32 output takes no bias
+        w4.gemm(e["a"].to(DEV), bp, e["wtype"], N, group_size=-1, out_dtype=torch.int32,
+                bias=torch.zeros(N, dtype=torch.int32, device=DEV))
+    assert ei.value.status == w4.ERR_INVALID_ARGUMENT
+
+
+def test_autotune_installs_the_fastest_schedule(gpu_lib):
+    """autotune() times every schedule that can run the problem on the GPU,
+    installs the fastest as the default for that shape, and the default
+    call then runs it, with results still equal to the oracle."""
+    w4 = gpu_lib
+    M, N, K = 24, 1024, 2048
+    e = w4synth.gen_w4a8(M, N, K, group_size=-1, seed=61)
+    a = e["a"].to(DEV)
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], K, N)
+    times = w4.autotune(a, b, e["wtype"], N, group_size=-1, out_dtype=torch.int32, reps=5)
+    names = w4.schedule_names()
+    assert len(times) >= 5 and all(t > 0 for t in times.values())
+    best = min(times, key=times.get)
+    try:
+        assert names[w4.default_schedule(M, N, K, torch.int8, -1)] == best
+        acc = w4.gemm(a, b, e["wtype"], N, group_size=-1, out_dtype=torch.int32)
+        torch.cuda.synchronize()
+        ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], None, -1, K, N)
+        assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref)
+    finally:
+        w4.override_schedule(torch.int8, M, M, N, K, -1, None)

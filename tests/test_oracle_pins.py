@@ -487,3 +487,39 @@ def test_w4a8_fp8_exact_matmul_and_bound():
     err = np.abs(ref * s.astype(np.float64)[:, None] - exact)
     bound = (np.abs(a.double().numpy()) * 2.0**-4 + s.astype(np.float64)[:, None] * 2.0**-10) @ np.abs(v)
     assert np.all(err <= bound)
+
+
+def test_bias_worked_examples():
+    """The bias step: the hand-worked W4A16 and W4A8 examples of
+    tests/golden/worked_examples.txt plus a bias on their column."""
+    g = golden_kv("worked_examples.txt")
+    a = np.array([float(x) for x in g["w4a16_a"]]).reshape(1, 8)
+    q = np.array([int(x) for x in g["w4a16_q"]], dtype=np.uint8).reshape(8, 1)
+    w = oracle.pack(q, oracle.NK_EXLLAMA)
+    s = np.full((1, 1), float(g["w4a16_s"][0]))
+    ref, _ = oracle.w4a16(a, w, oracle.NK_EXLLAMA, oracle.UINT4B8, s, None, -1, 8, 1)
+    got = oracle.add_bias(ref, None, np.array([float(g["w4a16_bias"][0])]))
+    assert got[0, 0] == float(g["w4a16_ref_bias"][0])
+    a8 = np.array([int(x) for x in g["w4a8_a"]], dtype=np.int8).reshape(1, 8)
+    q8 = np.array([int(x) for x in g["w4a8_q"]], dtype=np.uint8).reshape(8, 1)
+    w8 = oracle.pack(q8, oracle.NK_EXLLAMA)
+    acc = oracle.w4a8(a8, w8, oracle.NK_EXLLAMA, oracle.INT4, None, -1, 8, 1)
+    st, sc, bias = (float(x) for x in g["w4a8_scales_bias"])
+    r = oracle.w4a8_scale(acc.reshape(-1), np.array([0]), np.array([0]), np.array([st]),
+                          np.array([sc]))
+    assert oracle.add_bias(r, np.array([0]), np.array([bias]))[0] == float(g["w4a8_ref_bias"][0])
+
+
+def test_bias_is_a_per_column_shift():
+    """A zero bias changes nothing; the bias shifts every row of a column by
+    the same amount, independently of the product; flat and full forms
+    agree."""
+    rng = np.random.default_rng(3)
+    ref = rng.integers(-1000, 1000, (5, 7)).astype(np.float64)  # sums stay exact
+    assert np.array_equal(oracle.add_bias(ref, None, np.zeros(7)), ref)
+    b = (rng.integers(-64, 64, 7) / 8).astype(np.float16)
+    full = oracle.add_bias(ref, None, b)
+    assert np.array_equal(full - ref, np.broadcast_to(b.astype(np.float64), (5, 7)))
+    rows, cols = np.meshgrid(np.arange(5), np.arange(7), indexing="ij")
+    flat = oracle.add_bias(ref.reshape(-1), cols.reshape(-1), b)
+    assert np.array_equal(flat, full.reshape(-1))
