@@ -80,7 +80,10 @@ typedef enum w4_layout {
                               K-value j at bits (j/2)*4 + (j%2)*16 ([RDNA]) */
 } w4_layout;
 
-typedef enum w4_dtype { W4_F16 = 0, W4_BF16 = 1, W4_S8 = 2, W4_S32 = 3 } w4_dtype;
+/* Element types.  W4_E4M3: OCP fp8 E4M3 activations (bias 7, largest value
+ * 448, S.1111.111 NaN), one byte each ([PR9855]: W4A8 "including fp8
+ * activations"). */
+typedef enum w4_dtype { W4_F16 = 0, W4_BF16 = 1, W4_S8 = 2, W4_S32 = 3, W4_E4M3 = 4 } w4_dtype;
 
 /* Version of the prepacked weight layout produced by w4_prepack_B.  A
  * buffer prepacked under one version must not be used with another. */
@@ -135,6 +138,11 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
  *          multiplied left to right in fp32, with a_token_scales = s_tok [M]
  *          and ch_scales = s_ch [N] (fp32, device).
  *          out_type W4_S32: out = acc, both scale pointers NULL.
+ *   W4A8 with fp8 activations (a_type W4_E4M3): per-channel only (b_scales
+ *          NULL, group_size -1 / K), K a multiple of 128, fp16 output:
+ *          out = fp16_rn(acc * s_tok[m] * s_ch[n]) with acc the fp32 sum of
+ *          the exact products decode(a) * v(q) (every int4 value is an E4M3
+ *          value); NaN codes (0x7F, 0xFF) are outside the contract.
  *   workspace  device buffer of at least w4_gemm_workspace_size(...) bytes,
  *             16-byte aligned (W4_ERR_WORKSPACE otherwise).
  *

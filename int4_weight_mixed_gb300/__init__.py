@@ -24,10 +24,11 @@ from . import _build_lib
 
 UINT4B8, UINT4, INT4 = 0, 1, 2
 KN_SEQ, NK_SEQ, NK_EXLLAMA = 0, 1, 2
-F16, BF16, S8, S32 = 0, 1, 2, 3
+F16, BF16, S8, S32, E4M3 = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 
-_DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.int8: S8, torch.int32: S32}
+_DTYPE_CODE = {torch.float16: F16, torch.bfloat16: BF16, torch.int8: S8, torch.int32: S32,
+               torch.float8_e4m3fn: E4M3}
 _CODE_DTYPE = {v: k for k, v in _DTYPE_CODE.items()}
 
 _lib = None
@@ -266,7 +267,7 @@ def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
     M, K = a.shape
     a_code = _DTYPE_CODE[a.dtype]
     if out_dtype is None:
-        out_dtype = torch.float16 if a.dtype == torch.int8 else a.dtype
+        out_dtype = torch.float16 if a.dtype in (torch.int8, torch.float8_e4m3fn) else a.dtype
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     nbytes = workspace_size(M, N, K, a.dtype, group_size)

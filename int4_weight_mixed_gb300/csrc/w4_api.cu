@@ -66,7 +66,13 @@ int sm_count() {
 }
 
 int mode_of(int a_type) {
-  return a_type == W4_F16 ? kW4A16_F16 : a_type == W4_BF16 ? kW4A16_BF16 : kW4A8;
+  return a_type == W4_F16    ? kW4A16_F16
+         : a_type == W4_BF16 ? kW4A16_BF16
+         : a_type == W4_E4M3 ? kW4A8F8
+                             : kW4A8;
+}
+bool valid_a_type(int a_type) {
+  return a_type == W4_F16 || a_type == W4_BF16 || a_type == W4_S8 || a_type == W4_E4M3;
 }
 
 TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs);
@@ -78,6 +84,8 @@ constexpr size_t kMaxDynSmem = 227 * 1024;  // dynamic shared memory a CTA may o
 bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs, bool has_sg) {
   const Schedule& sc = kSchedules[si];
   if (sc.engine == kEngineSimt) return true;
+  // fp8 activations: the clustered skinny-M and the tensor-core schedules
+  if (mode == kW4A8F8 && sc.engine != kEngineGv && sc.engine != kEngineTc) return false;
   if (sc.engine == kEngineDk) {  // M rows in 8-row tiles; a 128-wide K block in one group
     if (M > sc.bm || (gs != K && gs % 128 != 0)) return false;
     size_t wp, wt;  // and the staged activations of a unit fit in shared memory
@@ -100,6 +108,10 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   p.mode = mode;
   p.bm = sc.bm;
   p.nt = sc.nt;
+  // K block: 64 16-bit values (4 KB of nibbles per tile), or 128 E4M3 values
+  // (8 KB) for fp8 activations
+  const int bk = mode == kW4A8F8 ? 128 : kStageK;
+  const int wblk = mode == kW4A8F8 ? 8192 : 4096;
   // K depth of a pipeline stage: skinny tiles need >= 8 KB of nibbles per
   // stage to hide the per-stage cost of the producer; wide tiles are
   // compute-bound and take shallower stages so that several fit in shared
@@ -111,13 +123,13 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
     while (nsub > 1 && (nsub * kStageK) % gs != 0 && gs % (nsub * kStageK) != 0) nsub /= 2;
   p.nsub = nsub;
   p.gps = (G > 1 && gs < nsub * kStageK) ? static_cast<int>(nsub * kStageK / gs) : 1;
-  p.stages = tc_max_stages(p.bm, nsub, p.nt);
-  p.smem_bytes = tc_smem_bytes(p.bm, nsub, p.nt, p.stages);
+  p.stages = tc_max_stages(p.bm, nsub, p.nt, wblk);
+  p.smem_bytes = tc_smem_bytes(p.bm, nsub, p.nt, p.stages, wblk);
   p.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
   p.n128 = static_cast<int>((N + kTileN - 1) / kTileN);
   p.n_tiles = (p.n128 + p.nt - 1) / p.nt;
   p.tiles = p.m_tiles * p.n_tiles;
-  p.k64 = static_cast<int>(K / kStageK);
+  p.k64 = static_cast<int>(K / bk);
   p.kb_total = (p.k64 + nsub - 1) / nsub;
   // W4A8 exactness: |a| <= 128 and |v*sg| <= 128 (group) or |v| <= 8
   // (per-channel) keep every fp32 partial sum of a chunk within 2^24.
@@ -296,7 +308,7 @@ GvPlan make_gv_plan(int si, int mode, int64_t M, int64_t N, int64_t K) {
   // device is present (cached per mode, row tiles and size), else from the
   // design's CTAs per SM
   static std::mutex mu;
-  static int cache[3][3][17];  // resident clusters + 1 (0: not yet queried)
+  static int cache[4][3][17];  // resident clusters + 1 (0: not yet queried)
   const int mi = mode, ni = p.nj == 1 ? 0 : p.nj == 2 ? 1 : 2;
   const int per_sm = gv_ctas_per_sm(p.nj);
   const int sms = sm_count();
@@ -388,7 +400,7 @@ int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs,
   for (int eng : {kEngineGv, kEngineDs, kEngineDk})
     for (int si = 1; si < kNumSchedules; ++si)
       if (kSchedules[si].engine == eng &&
-          !(eng == kEngineGv && (kSchedules[si].bm > 16 || !small_w)) &&
+          !(eng == kEngineGv && (kSchedules[si].bm > 16 || (!small_w && mode != kW4A8F8))) &&
           schedule_fits(si, mode, M, N, K, gs, has_sg))
         return si;
   int bm = 16;
@@ -437,8 +449,8 @@ w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* 
                    const void* b_zeros, int64_t group_size, const float* s_tok,
                    const float* s_ch, void* out, int out_type, Problem& pr) {
   if (M < 0 || N < 0 || K < 0) return fail(W4_ERR_INVALID_ARGUMENT, "negative size");
-  if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8)
-    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16, W4_BF16 or W4_S8");
+  if (!valid_a_type(a_type))
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16, W4_BF16, W4_S8 or W4_E4M3");
   if (wtype < W4_UINT4B8 || wtype > W4_INT4) return fail(W4_ERR_INVALID_ARGUMENT, "bad wtype");
   if (K % 8 != 0) return fail(W4_ERR_INVALID_ARGUMENT, "K must be a multiple of 8");
   const int64_t gs = (group_size == -1) ? K : group_size;
@@ -452,7 +464,19 @@ w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* 
   pr.has_sg = b_scales != nullptr;
   if (M == 0 || N == 0) return W4_OK;
   if (!out) return fail(W4_ERR_INVALID_ARGUMENT, "out is null");
-  if (pr.mode != kW4A8) {
+  if (pr.mode == kW4A8F8) {
+    // W4A8 with E4M3 activations: symmetric weights, one scale per column
+    if (wtype == W4_UINT4)
+      return fail(W4_ERR_UNSUPPORTED, "W4A8 supports symmetric weights only (int4 / uint4b8)");
+    if (b_zeros) return fail(W4_ERR_UNSUPPORTED, "W4A8 takes no zero-points");
+    if (b_scales || gs != K)
+      return fail(W4_ERR_UNSUPPORTED, "fp8 activations: per-channel weights only");
+    if (out_type != W4_F16) return fail(W4_ERR_UNSUPPORTED, "fp8 activations: fp16 output only");
+    if (!s_tok || !s_ch)
+      return fail(W4_ERR_INVALID_ARGUMENT, "W4A8 fp16 out needs token and channel scales");
+    if (K > 0 && (!a || !b_packed))
+      return fail(W4_ERR_INVALID_ARGUMENT, "a and b_packed are required");
+  } else if (pr.mode != kW4A8) {
     if (out_type != a_type)
       return fail(W4_ERR_INVALID_ARGUMENT, "W4A16: out_type must equal a_type");
     if (K > 0 && (!a || !b_packed || !b_scales))
@@ -483,7 +507,7 @@ w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* 
   }
   // every kernel reads or writes each array at least element by element;
   // the prepacked weights as 32-bit words
-  const uintptr_t asz = a_type == W4_S8 ? 1 : 2;
+  const uintptr_t asz = (a_type == W4_S8 || a_type == W4_E4M3) ? 1 : 2;
   const uintptr_t osz = (pr.mode == kW4A8 && out_type == W4_S32) ? 4 : 2;
   const uintptr_t ssz = pr.mode == kW4A8 ? 1 : 2;
   if (!aligned_to(a, asz) || !aligned_to(out, osz) || !aligned_to(b_packed, 4) ||
@@ -492,6 +516,8 @@ w4_status validate(const void* a, int a_type, int64_t M, int64_t K, const void* 
     return fail(W4_ERR_INVALID_ARGUMENT,
                 "a pointer is not aligned to its element size (b_packed: 4 bytes)");
   if (K % kStageK != 0) return fail(W4_ERR_UNSUPPORTED, "K must be a multiple of 64");
+  if (pr.mode == kW4A8F8 && K % 128 != 0)
+    return fail(W4_ERR_UNSUPPORTED, "fp8 activations: K must be a multiple of 128");
   if (K > 0 && gs % kStageK != 0)
     return fail(W4_ERR_UNSUPPORTED, "group_size must be a multiple of 64 (or K)");
   return W4_OK;
@@ -564,15 +590,16 @@ const char* w4_schedule_name(int schedule) {
 
 int w4_default_schedule(int64_t M, int64_t N, int64_t K, int a_type, int64_t group_size) {
   if (M <= 0 || N <= 0 || K <= 0 || K % kStageK != 0) return -1;
-  if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8) return -1;
+  if (!valid_a_type(a_type)) return -1;
+  if (a_type == W4_E4M3 && K % 128 != 0) return -1;
   const int64_t gs = group_size == -1 ? K : group_size;
   return default_schedule_impl(mode_of(a_type), M, N, K, gs, gs != K);
 }
 
 w4_status w4_override_schedule(int a_type, int64_t m_lo, int64_t m_hi, int64_t N, int64_t K,
                                int64_t group_size, int schedule) {
-  if (a_type != W4_F16 && a_type != W4_BF16 && a_type != W4_S8)
-    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16, W4_BF16 or W4_S8");
+  if (!valid_a_type(a_type))
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16, W4_BF16, W4_S8 or W4_E4M3");
   if (m_lo < 1 || m_hi < m_lo || N < 1 || K < 1 || K % kStageK != 0)
     return fail(W4_ERR_INVALID_ARGUMENT, "bad M range or shape");
   const int64_t gs = group_size == -1 ? K : group_size;
@@ -717,8 +744,8 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
     CUtensorMap amap;
     CUresult r;
     const cuuint32_t rows = static_cast<cuuint32_t>(8 * gp.nj);
-    if (pr.mode == kW4A8) {
-      // int8 [M][K]: one box of 128 K x all rows per K block
+    if (pr.mode == kW4A8 || pr.mode == kW4A8F8) {
+      // int8 / E4M3 [M][K]: one box of 128 K x all rows per K block
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
       const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
       const cuuint32_t box[2] = {128, rows};
@@ -767,7 +794,19 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
   memset(&zmap, 0, sizeof(zmap));
   const CUtensorMapDataType t16 =
       pr.mode == kW4A16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  {
+  if (pr.mode == kW4A8F8) {
+    // E4M3 [M][K]: one 2-D box of 128 K x BM rows per K block (128-byte rows)
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(plan.bm)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(act), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(W4_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed (%d)", (int)r);
+    plan.a3d = 0;
+  } else {
     // Preferred: one 3-D box {64, BM, nsub} per stage over the view
     // (k % 64, m, k / 64); strides K*2 and 128 bytes.  Fallback: 2-D boxes.
     const cuuint64_t dims3[3] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(M),

@@ -3,7 +3,8 @@
 //
 //   W4A16: out[m][n] = round_T(sum + bias[n])            (T = fp16 / bf16)
 //   W4A8 : out[m][n] = fp16_rn((float)acc * s_tok[m] * s_ch[n] + bias[n])
-//          or the raw int32 accumulator (no scales, no bias)
+//          or the raw int32 accumulator (no scales, no bias); with fp8
+//          activations acc is the fp32 sum of the exact products
 //
 // The sum is the fp32 (W4A16) or exact int32 (W4A8) result of the product;
 // the products by the per-token and per-channel scales are taken left to
@@ -42,7 +43,11 @@ template <int MODE>
 __device__ __forceinline__ void store_out(const TcArgs& args, int64_t m, int64_t n, float vf,
                                           int32_t vi) {
   const int64_t o = m * args.N + n;
-  if constexpr (MODE == kW4A8) {
+  if constexpr (MODE == kW4A8F8) {  // fp32 sum of the exact E4M3 x int4 products
+    float r = vf * args.s_tok[m] * args.s_ch[n];
+    if (args.bias) r += ep_f32(static_cast<const __half*>(args.bias)[n]);
+    static_cast<__half*>(args.out)[o] = __float2half_rn(r);
+  } else if constexpr (MODE == kW4A8) {
     if (args.out_s32) {
       static_cast<int32_t*>(args.out)[o] = vi;
       return;

@@ -174,6 +174,21 @@ __device__ __forceinline__ uint4 gv_i8x8_to_f16(uint2 raw) {
                     *reinterpret_cast<uint32_t*>(&r2), *reinterpret_cast<uint32_t*>(&r3));
 }
 
+// Eight E4M3 activations (two words) as four fp16 pairs (exact: every E4M3
+// value is an fp16 value), the second and fourth pair divided by 16 (exact:
+// the quotients are multiples of 2^-13 of magnitude at most 28).
+__device__ __forceinline__ uint4 gv_e4m3x8_to_f16(uint2 raw) {
+  uint32_t h[4];
+  const uint16_t b[4] = {static_cast<uint16_t>(raw.x), static_cast<uint16_t>(raw.x >> 16),
+                         static_cast<uint16_t>(raw.y), static_cast<uint16_t>(raw.y >> 16)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[i]) : "h"(b[i]));
+  const __half2 k16 = __float2half2_rn(0.0625f);
+  __half2 r1 = __hmul2(*reinterpret_cast<__half2*>(&h[1]), k16);
+  __half2 r3 = __hmul2(*reinterpret_cast<__half2*>(&h[3]), k16);
+  return make_uint4(h[0], *reinterpret_cast<uint32_t*>(&r1), h[2], *reinterpret_cast<uint32_t*>(&r3));
+}
+
 }  // namespace
 
 // Shared-memory layout: S stages of [W 8 KB][A rows x 128 K], then S scale /
@@ -181,7 +196,7 @@ __device__ __forceinline__ uint4 gv_i8x8_to_f16(uint2 raw) {
 // cluster reduction [8*NJ][128] x 4 B, and the barriers.  Every A tile
 // starts on a 1024-byte boundary (128-byte swizzle).
 __host__ __device__ inline uint32_t gv_act_bytes(int nj, int mode) {
-  return (mode == kW4A8 ? 128u : 256u) * 8u * static_cast<uint32_t>(nj);
+  return (mode == kW4A8 || mode == kW4A8F8 ? 128u : 256u) * 8u * static_cast<uint32_t>(nj);
 }
 __host__ __device__ inline uint32_t gv_stage_bytes(int nj, int mode) {
   return kGvWBlk + gv_act_bytes(nj, mode);
@@ -201,7 +216,8 @@ __global__ void __launch_bounds__(GvShape<NJ>::Threads, gv_ctas_per_sm(NJ))
   // fp16 MMAs with the offset subtracted before the MMA (W4A8, fp16
   // activations); bf16 MMAs with the offset folded out with the row sums
   constexpr bool kFp16Mma = MODE != kW4A16_BF16;
-  constexpr uint32_t kActBytes = (MODE == kW4A8 ? 128u : 256u) * 8u * NJ;
+  constexpr bool k8Bit = MODE == kW4A8 || MODE == kW4A8F8;  // 1-byte activations
+  constexpr uint32_t kActBytes = (k8Bit ? 128u : 256u) * 8u * NJ;
   constexpr uint32_t kStage = kGvWBlk + kActBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -256,7 +272,7 @@ __global__ void __launch_bounds__(GvShape<NJ>::Threads, gv_ctas_per_sm(NJ))
   auto issue_a = [&](int kb, int s) {
     const uint32_t bar = smem_addr(&full[s]);
     const uint32_t dst = sbase + s * kStage + kGvWBlk;
-    if (MODE == kW4A8) tma_load_2d_a(dst, &amap, kb * kGvBlkK, 0, bar);
+    if (k8Bit) tma_load_2d_a(dst, &amap, kb * kGvBlkK, 0, bar);
     else tma_load_3d_a(dst, &amap, 0, 0, 2 * kb, bar);
   };
 
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(GvShape<NJ>::Threads, gv_ctas_per_sm(NJ))
       cq[q] = 0.f;
       isq[q] = 1;
     }
-    if (pc && MODE != kW4A8) {
+    if (pc && (MODE == kW4A16_F16 || MODE == kW4A16_BF16)) {
 #pragma unroll
       for (int q = 0; q < 2 * RP; ++q) {
         const int64_t n = n0 + Cols * w + 8 * q + g;
@@ -384,11 +400,11 @@ __global__ void __launch_bounds__(GvShape<NJ>::Threads, gv_ctas_per_sm(NJ))
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           const int row = j * 8 + g;
-          if (MODE == kW4A8) {
-            // int8 row of 128 K: 16-byte column 2c + t/2, half t%2
+          if (k8Bit) {
+            // 8-bit row of 128 K: 16-byte column 2c + t/2, half t%2
             const uint2 raw = gv_lds64(at + row * 128 + ((((2 * c) | (t >> 1)) ^ g) << 4) +
                                        8 * (t & 1));
-            v[j] = gv_i8x8_to_f16(raw);
+            v[j] = MODE == kW4A8 ? gv_i8x8_to_f16(raw) : gv_e4m3x8_to_f16(raw);
           } else {
             // 16-bit: half-block z = c/2 of 64 K, 16-byte column 4(c%2) + t
             const uint32_t col = static_cast<uint32_t>(((c & 1) << 2) | t);
@@ -555,10 +571,17 @@ template <int MODE, int NJ>
 const void* gv_fn() {
   return reinterpret_cast<const void*>(&gv_gemm_kernel<MODE, NJ>);
 }
+template <int NJ>
+const void* gv_select_nj(int mode) {
+  switch (mode) {
+    case kW4A16_F16: return gv_fn<kW4A16_F16, NJ>();
+    case kW4A16_BF16: return gv_fn<kW4A16_BF16, NJ>();
+    case kW4A8F8: return gv_fn<kW4A8F8, NJ>();
+    default: return gv_fn<kW4A8, NJ>();
+  }
+}
 const void* gv_select(int mode, int nj) {
-  if (nj == 1) return mode == kW4A16_F16 ? gv_fn<kW4A16_F16, 1>() : mode == kW4A16_BF16 ? gv_fn<kW4A16_BF16, 1>() : gv_fn<kW4A8, 1>();
-  if (nj == 2) return mode == kW4A16_F16 ? gv_fn<kW4A16_F16, 2>() : mode == kW4A16_BF16 ? gv_fn<kW4A16_BF16, 2>() : gv_fn<kW4A8, 2>();
-  return mode == kW4A16_F16 ? gv_fn<kW4A16_F16, 4>() : mode == kW4A16_BF16 ? gv_fn<kW4A16_BF16, 4>() : gv_fn<kW4A8, 4>();
+  return nj == 1 ? gv_select_nj<1>(mode) : nj == 2 ? gv_select_nj<2>(mode) : gv_select_nj<4>(mode);
 }
 }  // namespace
 

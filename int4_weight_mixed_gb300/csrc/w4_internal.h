@@ -47,7 +47,7 @@ constexpr size_t kWsHeader = 256;                // status word + spare
 // call (and re-zeroed by w4_check_status after a timeout).
 constexpr size_t kCounterBytes = 64 * 1024;
 
-enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2 };
+enum Mode { kW4A16_F16 = 0, kW4A16_BF16 = 1, kW4A8 = 2, kW4A8F8 = 3 };  // kW4A8F8: E4M3 activations
 
 enum Engine { kEngineSimt = 0, kEngineTc = 1, kEngineDk = 2, kEngineDs = 3, kEngineGv = 4 };
 enum Decomp { kDataParallel = 0, kStreamK = 1, kSplitK = 2 };
@@ -185,8 +185,8 @@ size_t gv_smem_bytes(int nj, int mode, int stages);
 int gv_max_clusters(int mode, int nj, int C, size_t smem);
 cudaError_t launch_gv(const GvPlan& plan, const CUtensorMap& amap, const TcArgs& args,
                       cudaStream_t s);
-size_t tc_stage_bytes(int bm, int nsub, int nt);
-size_t tc_smem_bytes(int bm, int nsub, int nt, int stages);
-int tc_max_stages(int bm, int nsub, int nt);
+size_t tc_stage_bytes(int bm, int nsub, int nt, int wblk);
+size_t tc_smem_bytes(int bm, int nsub, int nt, int stages, int wblk);
+int tc_max_stages(int bm, int nsub, int nt, int wblk);
 
 }  // namespace w4

@@ -3,6 +3,7 @@
 // of the GEMM, which runs any shape the API accepts.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "w4_epilogue.cuh"
 #include "w4_internal.h"
@@ -168,6 +169,28 @@ __global__ void simt_w4a8_kernel(const int8_t* __restrict__ a, TcArgs args) {
   }
 }
 
+// CUDA-core W4A8 with E4M3 activations: fp32 accumulation, k ascending, of
+// the exact products decode(a) * v.
+__global__ void simt_w4a8f8_kernel(const __nv_fp8_storage_t* __restrict__ a, TcArgs args) {
+  const int64_t n = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (n >= args.N) return;
+  const uint32_t* wp = reinterpret_cast<const uint32_t*>(args.b_packed);
+  const int64_t K = args.K;
+  for (int64_t m = blockIdx.y; m < args.M; m += gridDim.y) {
+    float acc = 0.f;
+    for (int64_t k0 = 0; k0 < K; k0 += 8) {
+      uint32_t word = wp[packed_word_index(K, n, k0)];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float v = static_cast<float>(static_cast<int>((word >> exl_bit(j)) & 0xFu) - 8);
+        const __half h = __half(__nv_cvt_fp8_to_halfraw(a[m * K + k0 + j], __NV_E4M3));
+        acc = fmaf(__half2float(h), v, acc);
+      }
+    }
+    store_out<kW4A8F8>(args, m, n, acc, 0);
+  }
+}
+
 static int grid_for(int64_t total, int threads) {
   int64_t b = (total + threads - 1) / threads;
   if (b > (1 << 20)) b = 1 << 20;
@@ -223,6 +246,8 @@ cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_
   else if (mode == kW4A16_BF16)
     simt_w4a16_kernel<__nv_bfloat16>
         <<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(a), args);
+  else if (mode == kW4A8F8)
+    simt_w4a8f8_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_fp8_storage_t*>(a), args);
   else
     simt_w4a8_kernel<<<grid, 128, 0, s>>>(static_cast<const int8_t*>(a), args);
   return cudaGetLastError();

@@ -220,32 +220,60 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Four MMAs covering one 64-wide K block: A columns a0 + 8*kk, B
-// descriptors desc + 2*kk (32 bytes further along the 128-byte swizzled rows
-// each).  Operands are formed before the asm block; the first MMA
-// overwrites D when `accumulate` is 0.
+// Four MMAs covering one K block (64 K of f16 / bf16, or 128 K of E4M3):
+// A columns a0 + 8*kk, B descriptors desc + 2*kk (32 bytes further along the
+// 128-byte swizzled rows each).  Operands are formed before the asm block;
+// the first MMA overwrites D when `accumulate` is 0.  F8: kind::f8f6f4
+// (E4M3 x E4M3, 32 K per MMA) instead of kind::f16 (16 K per MMA).
+#define W4_MMA4_STR(KIND)                                  \
+  "{\n\t.reg .pred p, t;\n\t"                              \
+  "setp.ne.b32 p, %4, 0;\n\t"                              \
+  "setp.eq.b32 t, %4, %4;\n\t"                             \
+  "tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%1], %2, %3, p;\n\t"  \
+  "tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%5], %6, %3, t;\n\t"  \
+  "tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%7], %8, %3, t;\n\t"  \
+  "tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%9], %10, %3, t;\n\t}"
+template <bool F8 = false>
 __device__ __forceinline__ void mma_ts_stage(uint32_t d_tmem, uint32_t a0, uint64_t desc,
                                              uint32_t idesc, uint32_t accumulate) {
   const uint32_t a1 = a0 + 8, a2 = a0 + 16, a3 = a0 + 24;
   const uint64_t d1 = desc + 2, d2 = desc + 4, d3 = desc + 6;
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.eq.b32 t, %4, %4;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, t;\n\t}" ::"r"(d_tmem),
-      "r"(a0), "l"(desc), "r"(idesc), "r"(accumulate), "r"(a1), "l"(d1), "r"(a2), "l"(d2),
-      "r"(a3), "l"(d3)
-      : "memory");
+  if constexpr (F8)
+    asm volatile(W4_MMA4_STR("f8f6f4")::"r"(d_tmem), "r"(a0), "l"(desc), "r"(idesc),
+                 "r"(accumulate), "r"(a1), "l"(d1), "r"(a2), "l"(d2), "r"(a3), "l"(d3)
+                 : "memory");
+  else
+    asm volatile(W4_MMA4_STR("f16")::"r"(d_tmem), "r"(a0), "l"(desc), "r"(idesc),
+                 "r"(accumulate), "r"(a1), "l"(d1), "r"(a2), "l"(d2), "r"(a3), "l"(d3)
+                 : "memory");
 }
 
-// Sixteen MMAs covering a 256-wide K stage made of four 64-wide blocks:
-// A columns a0 + 8*i (i = 0..15); B descriptors desc + j*sub + 2*kk for
-// block j and 16-wide step kk.  All 32 operands are formed first (independent
-// adds from three registers), then the 16 MMAs issue back to back: an add
-// between two MMAs that depends on the previous operand stalls the issue.
+// Sixteen MMAs covering a stage made of four K blocks: A columns a0 + 8*i
+// (i = 0..15); B descriptors desc + j*sub + 2*kk for block j and step kk.
+// All 32 operands are formed first (independent adds from three
+// registers), then the 16 MMAs issue back to back: an add between two MMAs
+// that depends on the previous operand stalls the issue.
+#define W4_MMA16_LINE(KIND, A, B, P) \
+  "tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%" #A "], %" #B ", %1, " P ";\n\t"
+#define W4_MMA16_STR(KIND)                                                              \
+  "{\n\t.reg .pred p, t;\n\t"                                                           \
+  "setp.ne.b32 p, %2, 0;\n\t"                                                           \
+  "setp.eq.b32 t, %2, %2;\n\t" W4_MMA16_LINE(KIND, 3, 19, "p")                          \
+      W4_MMA16_LINE(KIND, 4, 20, "t") W4_MMA16_LINE(KIND, 5, 21, "t")                   \
+      W4_MMA16_LINE(KIND, 6, 22, "t") W4_MMA16_LINE(KIND, 7, 23, "t")                   \
+      W4_MMA16_LINE(KIND, 8, 24, "t") W4_MMA16_LINE(KIND, 9, 25, "t")                   \
+      W4_MMA16_LINE(KIND, 10, 26, "t") W4_MMA16_LINE(KIND, 11, 27, "t")                 \
+      W4_MMA16_LINE(KIND, 12, 28, "t") W4_MMA16_LINE(KIND, 13, 29, "t")                 \
+      W4_MMA16_LINE(KIND, 14, 30, "t") W4_MMA16_LINE(KIND, 15, 31, "t")                 \
+      W4_MMA16_LINE(KIND, 16, 32, "t") W4_MMA16_LINE(KIND, 17, 33, "t")                 \
+      W4_MMA16_LINE(KIND, 18, 34, "t") "}"
+#define W4_MMA16_OPS                                                                     \
+  "r"(d_tmem), "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]),  \
+      "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]),     \
+      "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15]), "l"(b[0]), "l"(b[1]),  \
+      "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "l"(b[8]),       \
+      "l"(b[9]), "l"(b[10]), "l"(b[11]), "l"(b[12]), "l"(b[13]), "l"(b[14]), "l"(b[15])
+template <bool F8 = false>
 __device__ __forceinline__ void mma_ts_stage16(uint32_t d_tmem, uint32_t a0, uint64_t desc,
                                                uint64_t sub, uint32_t idesc,
                                                uint32_t accumulate) {
@@ -256,75 +284,58 @@ __device__ __forceinline__ void mma_ts_stage16(uint32_t d_tmem, uint32_t a0, uin
     a[i] = a0 + 8 * i;
     b[i] = desc + static_cast<uint64_t>(i >> 2) * sub + 2 * (i & 3);
   }
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t"
-      "setp.ne.b32 p, %2, 0;\n\t"
-      "setp.eq.b32 t, %2, %2;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %19, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %20, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %21, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %22, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %23, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %24, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %25, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %26, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %27, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%12], %28, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %29, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%14], %30, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %31, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%16], %32, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%17], %33, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%18], %34, %1, t;\n\t}" ::"r"(d_tmem),
-      "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
-      "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]),
-      "r"(a[13]), "r"(a[14]), "r"(a[15]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]),
-      "l"(b[5]), "l"(b[6]), "l"(b[7]), "l"(b[8]), "l"(b[9]), "l"(b[10]), "l"(b[11]), "l"(b[12]),
-      "l"(b[13]), "l"(b[14]), "l"(b[15])
-      : "memory");
+  if constexpr (F8)
+    asm volatile(W4_MMA16_STR("f8f6f4")::W4_MMA16_OPS : "memory");
+  else
+    asm volatile(W4_MMA16_STR("f16")::W4_MMA16_OPS : "memory");
 }
 
-// Eight MMAs from explicit operands (A tensor-memory columns a[i], B
-// descriptors b[i]), all formed before the first one issues.  The issuing
-// thread is held inside each MMA for about its execution time, so the work
-// it does between MMA groups leaves the tensor pipe idle: the more MMAs per
-// group, the less that costs.
-// Four MMAs into one accumulator (a, b: four operand addresses each); the
-// first accumulates only when `accumulate` is non-zero.
+// Four / eight MMAs from explicit operands (A tensor-memory columns a[i], B
+// descriptors b[i]), all formed before the first one issues, into one
+// accumulator; the first accumulates only when `accumulate` is non-zero.
+// The issuing thread is held inside each MMA for about its execution time,
+// so the work it does between MMA groups leaves the tensor pipe idle: the
+// more MMAs per group, the less that costs.
+#define W4_MMA_N_LINE(KIND, A, B, P) \
+  "tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%" #A "], %" #B ", %1, " P ";\n\t"
+#define W4_MMA_X4_STR(KIND)                                                         \
+  "{\n\t.reg .pred p, t;\n\t"                                                      \
+  "setp.ne.b32 p, %2, 0;\n\t"                                                      \
+  "setp.eq.b32 t, %2, %2;\n\t" W4_MMA_N_LINE(KIND, 3, 7, "p")                      \
+      W4_MMA_N_LINE(KIND, 4, 8, "t") W4_MMA_N_LINE(KIND, 5, 9, "t")                \
+      W4_MMA_N_LINE(KIND, 6, 10, "t") "}"
+#define W4_MMA_X4_OPS                                                               \
+  "r"(d_tmem), "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), \
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+template <bool F8 = false>
 __device__ __forceinline__ void mma_ts_4(uint32_t d_tmem, const uint32_t* a, const uint64_t* b,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t"
-      "setp.ne.b32 p, %2, 0;\n\t"
-      "setp.eq.b32 t, %2, %2;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %9, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %10, %1, t;\n\t}" ::"r"(d_tmem),
-      "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]),
-      "l"(b[1]), "l"(b[2]), "l"(b[3])
-      : "memory");
+  if constexpr (F8)
+    asm volatile(W4_MMA_X4_STR("f8f6f4")::W4_MMA_X4_OPS : "memory");
+  else
+    asm volatile(W4_MMA_X4_STR("f16")::W4_MMA_X4_OPS : "memory");
 }
 
+#define W4_MMA_X8_STR(KIND)                                                         \
+  "{\n\t.reg .pred p, t;\n\t"                                                      \
+  "setp.ne.b32 p, %2, 0;\n\t"                                                      \
+  "setp.eq.b32 t, %2, %2;\n\t" W4_MMA_N_LINE(KIND, 3, 11, "p")                     \
+      W4_MMA_N_LINE(KIND, 4, 12, "t") W4_MMA_N_LINE(KIND, 5, 13, "t")              \
+      W4_MMA_N_LINE(KIND, 6, 14, "t") W4_MMA_N_LINE(KIND, 7, 15, "t")              \
+      W4_MMA_N_LINE(KIND, 8, 16, "t") W4_MMA_N_LINE(KIND, 9, 17, "t")              \
+      W4_MMA_N_LINE(KIND, 10, 18, "t") "}"
+#define W4_MMA_X8_OPS                                                               \
+  "r"(d_tmem), "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), \
+      "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]),    \
+      "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+template <bool F8 = false>
 __device__ __forceinline__ void mma_ts_8(uint32_t d_tmem, const uint32_t (&a)[8],
                                          const uint64_t (&b)[8], uint32_t idesc,
                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, t;\n\t"
-      "setp.ne.b32 p, %2, 0;\n\t"
-      "setp.eq.b32 t, %2, %2;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %17, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %18, %1, t;\n\t}" ::"r"(d_tmem),
-      "r"(idesc), "r"(accumulate), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
-      "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]),
-      "l"(b[5]), "l"(b[6]), "l"(b[7])
-      : "memory");
+  if constexpr (F8)
+    asm volatile(W4_MMA_X8_STR("f8f6f4")::W4_MMA_X8_OPS : "memory");
+  else
+    asm volatile(W4_MMA_X8_STR("f16")::W4_MMA_X8_OPS : "memory");
 }
 
 // 3-D tiled tensor copy global -> shared.
@@ -406,7 +417,8 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B of the same
-// 16-bit type (0 = f16, 1 = bf16), both K-major, M = 128, N = n.
+// 16-bit type (0 = f16, 1 = bf16), both K-major, M = 128, N = n.  The same
+// fields serve kind::f8f6f4, where type code 0 is E4M3.
 __host__ __device__ __forceinline__ uint32_t idesc_f16(uint32_t ab_format, uint32_t n) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((n >> 3) << 17) |
          ((128u >> 4) << 24);

@@ -6,20 +6,22 @@
 
 namespace w4 {
 
-size_t tc_stage_bytes(int bm, int nsub, int nt) {
+// wblk: prepacked weight bytes of one K block of one 128-column tile (4096
+// for 64-K blocks, 8192 for the 128-K blocks of fp8 activations)
+size_t tc_stage_bytes(int bm, int nsub, int nt, int wblk) {
   return static_cast<size_t>(nsub) *
-         (static_cast<size_t>(bm) * 128 + static_cast<size_t>(nt) * (4096 + 256 + 256));
+         (static_cast<size_t>(bm) * 128 + static_cast<size_t>(nt) * (wblk + 256 + 256));
 }
 
-size_t tc_smem_bytes(int bm, int nsub, int nt, int stages) {
+size_t tc_smem_bytes(int bm, int nsub, int nt, int stages, int wblk) {
   const size_t bars = (2 * kMaxStages + kMaxTmemStages + 3) * 8;
-  return 1024 + tc_stage_bytes(bm, nsub, nt) * stages + bars + 64;  // + slot, abort, tok[2]
+  return 1024 + tc_stage_bytes(bm, nsub, nt, wblk) * stages + bars + 64;  // + slot, abort, tok[2]
 }
 
-int tc_max_stages(int bm, int nsub, int nt) {
+int tc_max_stages(int bm, int nsub, int nt, int wblk) {
   const size_t budget = 225 * 1024;
   int s = kMaxStages;
-  while (s > 2 && tc_smem_bytes(bm, nsub, nt, s) > budget) --s;
+  while (s > 2 && tc_smem_bytes(bm, nsub, nt, s, wblk) > budget) --s;
   return s;
 }
 

@@ -203,6 +203,34 @@ __device__ __forceinline__ void convert_chunk(const uint4& wv, uint32_t s2u, uin
   }
 }
 
+// E4M3 weights for W4A8 with fp8 activations: the 32 K-values of one
+// 16-byte chunk as eight 32-bit tensor-memory columns of four E4M3 bytes in K
+// order.  Each nibble pair becomes the exact fp16 pair (q - bias) by the
+// exponent-bias trick, which one conversion turns into two E4M3 bytes
+// (exact: every value -8..7 is an E4M3 value); two byte pairs make a column.
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+  return r;
+}
+__device__ __forceinline__ void convert_chunk_f8(const uint4& wv, int wbias, uint32_t* v) {
+  const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+  const __half2 off = __half2half2(__int2half_rn(1024 + wbias));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint16_t e[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const __half2 q = __hsub2(as_t2<__half2>(lop_and_or(wd[i] >> (4 * p), 0x000F000Fu,
+                                                          0x64006400u)),
+                                off);
+      e[p] = f16x2_to_e4m3x2(as_u32(q));  // K 2p (low byte), 2p + 1
+    }
+    v[2 * i] = static_cast<uint32_t>(e[0]) | (static_cast<uint32_t>(e[1]) << 16);
+    v[2 * i + 1] = static_cast<uint32_t>(e[2]) | (static_cast<uint32_t>(e[3]) << 16);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ T to_t16(float x);
 template <>
@@ -237,6 +265,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ CUtensorMap zmap, const TcPlan p, const TcArgs args) {
   using T16 = typename std::conditional<MODE == kW4A16_F16, __half, __nv_bfloat16>::type;
+  // W4A8 with fp8 activations: K blocks of 128 E4M3 values (one 128-byte
+  // activation row, 8 KB of nibbles per 128-column tile) on kind::f8f6f4;
+  // otherwise blocks of 64 16-bit values (4 KB of nibbles) on kind::f16
+  constexpr bool F8 = MODE == kW4A8F8;
+  constexpr int BK = F8 ? 128 : kStageK;
+  constexpr uint32_t WB = F8 ? 8192u : 4096u;
+  constexpr int CPB = BK / kChunkK;  // 32-K chunks per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -245,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   Smem sm;
   sm.a = base;
   sm.w = sm.a + static_cast<size_t>(S) * NS * a_sub;             // [S][NT][NS][4096]
-  sm.s = sm.w + static_cast<size_t>(S) * NT * NS * 4096;          // [S][NT][NS * 256]
+  sm.s = sm.w + static_cast<size_t>(S) * NT * NS * WB;            // [S][NT][NS * 256]
   sm.z = sm.s + static_cast<size_t>(S) * NT * NS * 256;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm.z + static_cast<size_t>(S) * NT * NS * 256);
   sm.full = bars;
@@ -300,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int64_t M = args.M, N = args.N, K = args.K;
   const int gsz = static_cast<int>(args.group_size);
-  const int sub_per_group = gsz / kStageK;  // 64-K blocks per scale group
+  const int sub_per_group = gsz / BK;  // K blocks per scale group
   // A stage lies inside one scale group (sub_per_group >= NS) or covers whole
   // groups of 1 or 2 blocks (the plan guarantees one or the other): the group
   // of block qq of a stage is the stage's first group + (qq >> grow_shift).
@@ -342,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ntv > NT) ntv = NT;
         const uint8_t* wsrc =
             args.b_packed +
-            ((static_cast<int64_t>(nt) * NT * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * 2) *
+            ((static_cast<int64_t>(nt) * NT * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * CPB) *
              kTileN) * 16;
         const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
         // scale group of the stage, kept without division per stage
@@ -354,9 +389,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
           const uint32_t fb = full0 + s * 8;
           if (wprod) {
-            mbar_arrive_expect_tx_a(fb, ntv * nv * 4096 + NT * (sc_bytes + zp_bytes));
+            mbar_arrive_expect_tx_a(fb, ntv * nv * WB + NT * (sc_bytes + zp_bytes));
             for (int t = 0; t < ntv; ++t)
-              bulk_g2s_a(w0 + (s * NT + t) * NS * 4096, wsrc + t * tile_stride, nv * 4096, fb);
+              bulk_g2s_a(w0 + (s * NT + t) * NS * WB, wsrc + t * tile_stride, nv * WB, fb);
             if (sc_bytes || zp_bytes) {
               const int g0 = gcur;
               for (int t = 0; t < NT; ++t) {
@@ -366,14 +401,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   tma_load_2d_a(z0 + (s * NT + t) * NS * 256, &zmap, n0 + t * kTileN, g0, fb);
               }
             }
-            wsrc += NS * 4096;
+            wsrc += NS * WB;
           } else if (p.a3d) {
             mbar_arrive_expect_tx_a(fb, NS * a_sub);
             tma_load_3d_a(a0 + s * NS * a_sub, &amap, 0, y, k64_0, fb);
           } else {
             mbar_arrive_expect_tx_a(fb, nv * a_sub);
             for (int j = 0; j < nv; ++j)
-              tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * kStageK, y, fb);
+              tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * BK, y, fb);
           }
           if (stage_in_group) {
             gleft -= NS;
@@ -410,7 +445,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // alone issues every group (the loop right below).
     if constexpr (!MMA2) {
     if (lane == 0 && warp == kMmaWarp) {
-      const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
+      const uint32_t idesc =
+          idesc_f16(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u, static_cast<uint32_t>(BM));
       const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
       const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
       uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0;
@@ -481,11 +517,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               // W4A8: the first stage's shared-memory slot is released as soon
               // as its own four MMAs retire (measured 3% faster at 256-row
               // tiles; W4A16 measured slower with the extra commit)
-              mma_ts_4(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              mma_ts_4<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
               mma_commit(&sm.empty[s1]);
-              mma_ts_4(tmem, a8 + 4, b8 + 4, idesc, 1u);
+              mma_ts_4<F8>(tmem, a8 + 4, b8 + 4, idesc, 1u);
             } else {
-              mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
             }
           } else {
             const int k64_0 = (u.kb0 + j) * NS;
@@ -495,11 +531,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
               const uint64_t dsc = desc0 + s * NS * sub16;
               if (nv == 4) {
-                mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+                mma_ts_stage16<F8>(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
               } else {
-                mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
+                mma_ts_stage<F8>(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
                 for (int q = 1; q < nv; ++q)
-                  mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
+                  mma_ts_stage<F8>(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
               }
             }
           }
@@ -528,7 +564,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
     if (lane == 0) {
       const uint32_t me = warp == kMmaWarp ? 0u : 1u;  // issues the groups g with g % 2 == me
-      const uint32_t idesc = idesc_f16(MODE == kW4A16_F16 ? 0u : 1u, static_cast<uint32_t>(BM));
+      const uint32_t idesc =
+          idesc_f16(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u, static_cast<uint32_t>(BM));
       const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
       const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
       uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0, g = 0, tok_ph = 0;
@@ -605,7 +642,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   b8[i] = desc0 + s1 * 2 * sub16 + half * sub16 + 2 * kk;
                 }
               }
-              mma_ts_8(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
             } else {
               const int k64_0 = (u.kb0 + j) * NS;
               const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
@@ -614,11 +651,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t acol = tmem + p.acol + (ts * NT + t) * NS * 32;
                 const uint64_t dsc = desc0 + s * NS * sub16;
                 if (nv == 4) {
-                  mma_ts_stage16(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
+                  mma_ts_stage16<F8>(dcol, acol, dsc, sub16, idesc, chunk_start ? 0u : 1u);
                 } else {
-                  mma_ts_stage(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
+                  mma_ts_stage<F8>(dcol, acol, dsc, idesc, chunk_start ? 0u : 1u);
                   for (int q = 1; q < nv; ++q)
-                    mma_ts_stage(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
+                    mma_ts_stage<F8>(dcol, acol + q * 32, dsc + q * sub16, idesc, 1u);
                 }
               }
             }
@@ -720,12 +757,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
           for (int t = 0; t < NT; ++t) {
             const size_t st_idx = static_cast<size_t>(s) * NT + t;
-            const uint8_t* wst = sm.w + st_idx * NS * 4096;
+            const uint8_t* wst = sm.w + st_idx * NS * WB;
             const uint8_t* sst = sm.s + st_idx * NS * 256;
             const uint8_t* zst = sm.z + st_idx * NS * 256;
             const uint32_t tcol = tmem + lane_base + p.acol + (ts * NT + t) * NS * 32;
             const bool row_ok = n0 + t * kTileN + r < N;
             for (int qq = 0; qq < nv; ++qq) {
+              if constexpr (F8) {
+                // four 32-K chunks -> 32 columns of E4M3 bytes (no scales)
+                uint32_t v[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  convert_chunk_f8(*reinterpret_cast<const uint4*>(wst + qq * WB + c * 2048 + r * 16),
+                                   args.wbias, v + 8 * c);
+                if (!row_ok) {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) v[i] = 0;
+                }
+                tmem_st32(tcol + qq * 32, v);
+                continue;
+              }
               const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
               const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
               const int grow = stage_in_group ? 0 : qq >> grow_shift;
@@ -943,6 +994,8 @@ cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUten
     fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_F16, MMA2>);
   else if (plan.mode == kW4A16_BF16)
     fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_BF16, MMA2>);
+  else if (plan.mode == kW4A8F8)
+    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A8F8, MMA2>);
   else fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A8, MMA2>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem_bytes));
@@ -955,6 +1008,12 @@ cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUten
   }
   if (plan.mode == kW4A16_BF16) {
     tc_gemm_kernel<kW4A16_BF16, MMA2>
+        <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
+    return cudaGetLastError();
+  }
+  if (plan.mode == kW4A8F8) {
+    // fp8 activations are read by TMA straight from the caller's buffer
+    tc_gemm_kernel<kW4A8F8, MMA2>
         <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
     return cudaGetLastError();
   }

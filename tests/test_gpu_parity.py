@@ -668,3 +668,77 @@ def test_autotune_installs_the_fastest_schedule(gpu_lib):
         assert np.array_equal(acc.cpu().numpy().astype(np.int64), ref)
     finally:
         w4.override_schedule(torch.int8, M, M, N, K, -1, None)
+
+
+
+# ------------------------------------------------- W4A8, fp8 activations ---
+# out = fp16(acc * s_tok * s_ch), acc the fp32 sum of exact E4M3 x int4
+# products: within 4e-3 * sum|terms| * s_tok * s_ch + 1 fp16 ulp.
+
+F8_SCHEDULES = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk",
+                "tc256_dp", "tc128x2_sk", "tc128x2_kp", "tc256_kp", "gv8_cl", "gv16_cl",
+                "gv32_cl"]
+
+
+def run_fp8(w4, e, schedule=-1, bias=None):
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], e["K"], e["N"])
+    a = e["a"].to(DEV).view(torch.float8_e4m3fn)
+    out = w4.gemm(a, b, e["wtype"], e["N"], group_size=-1, token_scales=e["s_tok"].to(DEV),
+                  channel_scales=e["s_ch"].to(DEV), schedule=schedule, bias=bias)
+    torch.cuda.synchronize()
+    return out.cpu().double().numpy()
+
+
+def fp8_ref(e, rows=None, cols=None):
+    ref, absref = oracle.w4a8_fp8(e["a"].numpy(), e["w"], e["layout"], e["wtype"], e["K"], e["N"])
+    sc = np.outer(e["s_tok"].double().numpy(), e["s_ch"].double().numpy())
+    ref, absref = ref * sc, absref * sc
+    if rows is not None:
+        return ref[rows, cols], absref[rows, cols]
+    return ref, absref
+
+
+@pytest.mark.parametrize("name", F8_SCHEDULES)
+def test_w4a8_fp8_every_schedule(gpu_lib, name):
+    w4 = gpu_lib
+    M = min(ROWS.get(name, 40), 40) - 3
+    e = w4synth.gen_w4a8_fp8(M, 384, 2048, seed=M + 5)
+    got = run_fp8(w4, e, sched(w4, name))
+    ref, absref = fp8_ref(e)
+    assert_within(got, ref, absref, "f16", f"fp8 {name}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 128, 1024])
+def test_w4a8_fp8_qqq_shape(gpu_lib, M):
+    """The QQQ sweep shape (N=8192, K=21760) with fp8 activations, default
+    schedule, on sampled elements computed one by one."""
+    w4 = gpu_lib
+    N, K = w4synth.QQQ_N, w4synth.QQQ_K
+    e = w4synth.gen_w4a8_fp8(M, N, K, seed=M)
+    got = run_fp8(w4, e)
+    rows, cols = samples(M, N, count=48, seed=M)
+    a = e["a"][torch.from_numpy(np.unique(rows))]
+    # the oracle on the sampled rows only (full N), then the sampled columns
+    ur = np.unique(rows)
+    sub = dict(e, a=a, M=len(ur), s_tok=e["s_tok"][torch.from_numpy(ur)])
+    ref, absref = fp8_ref(sub)
+    idx = np.searchsorted(ur, rows)
+    assert_within(got[rows, cols], ref[idx, cols], absref[idx, cols], "f16", f"fp8 QQQ M={M}")
+
+
+def test_w4a8_fp8_rejections(gpu_lib):
+    w4 = gpu_lib
+    e = w4synth.gen_w4a8_fp8(4, 256, 512, seed=1)
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], 512, 256)
+    a = e["a"].to(DEV).view(torch.float8_e4m3fn)
+    with pytest.raises(w4.W4Error) as ei:  # raw int32 output: the sum is not an integer
+        w4.gemm(a, b, e["wtype"], 256, group_size=-1, out_dtype=torch.int32)
+    assert ei.value.status == w4.ERR_UNSUPPORTED
+    with pytest.raises(w4.W4Error) as ei:  # per-group scales
+        w4.gemm(a, b, e["wtype"], 256, scales=torch.ones(4, 256, dtype=torch.int8, device=DEV),
+                group_size=128, token_scales=e["s_tok"].to(DEV), channel_scales=e["s_ch"].to(DEV))
+    assert ei.value.status == w4.ERR_UNSUPPORTED
+    with pytest.raises(w4.W4Error) as ei:  # ds cannot run fp8
+        w4.gemm(a, b, e["wtype"], 256, group_size=-1, token_scales=e["s_tok"].to(DEV),
+                channel_scales=e["s_ch"].to(DEV), schedule=sched(w4, "ds8_sk"))
+    assert ei.value.status == w4.ERR_UNSUPPORTED

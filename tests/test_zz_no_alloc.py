@@ -58,13 +58,14 @@ def _call(w4, a, a_code, b, wtype, N, s, s_code, z, gs, tok, ch, out, out_code):
 
 def test_noalloc_w4a16_matches_oracle(gpu_lib):
     w4 = gpu_lib
-    M, N, K = 16, 4096, 4096
+    M, N, K = 16, 4096, 14336
     d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4,
                           layout=w4.NK_EXLLAMA, group_size=128, zeros=True, seed=11)
     a, s, z = d["a"].to(DEV), d["s"].to(DEV), d["z"].to(DEV)
     b = w4.prepack_B(d["w"].to(DEV), d["wtype"], d["layout"], K, N)
-    # this shape runs stream-K, so the scratch holds partial sums
-    assert w4.schedule_names()[w4.default_schedule(M, N, K, torch.bfloat16, 128)].endswith("_sk")
+    # this shape runs the streamed stream-K schedule, so the scratch holds
+    # the staged activations and partial sums
+    assert w4.schedule_names()[w4.default_schedule(M, N, K, torch.bfloat16, 128)] == "ds16_sk"
     ref, absref = oracle.w4a16(d["a"], d["w"], d["layout"], d["wtype"], d["s"], d["z"], 128, K, N)
     with_ws = w4.gemm(a, b, d["wtype"], N, scales=s, zeros=z, group_size=128)
     for call in range(2):

@@ -101,6 +101,22 @@ def gen_w4a8(M: int, N: int, K: int, group_size: int = -1, layout: int = NK_EXLL
                 wtype=INT4, group_size=group_size)
 
 
+def gen_w4a8_fp8(M: int, N: int, K: int, layout: int = NK_EXLLAMA, seed: int = 0) -> dict:
+    """CPU tensors for one W4A8 problem with fp8 activations: a [M,K] E4M3
+    codes (uint8) drawn uniformly from the 254 finite codes (0x7F and 0xFF,
+    the NaNs, are replaced by their neighbours 0x7E, 0xFE); s_tok [M] fp32
+    U[0.01,0.05]; int4 weight words; s_ch [N] fp32 U[0.001,0.01].  Per-channel
+    only."""
+    g = _gen(seed)
+    codes = torch.randint(0, 256, (M, K), generator=g, dtype=torch.int32)
+    codes = torch.where((codes & 0x7F) == 0x7F, codes - 1, codes).to(torch.uint8)
+    s_tok = uniform((M,), 0.01, 0.05, g, torch.float32)
+    w = random_words(packed_shape(layout, K, N), g)
+    s_ch = uniform((N,), 0.001, 0.01, g, torch.float32)
+    return dict(a=codes, s_tok=s_tok, w=w, s_ch=s_ch, M=M, N=N, K=K, layout=layout, wtype=INT4,
+                group_size=-1)
+
+
 def gen_act16(M: int, K: int, dtype=torch.float16, seed: int = 0) -> torch.Tensor:
     """Activations [M, K] ~ N(0, 1) in fp16 / bf16 (the W4A16 activation
     distribution): the input of the per-token int8 quantization."""
