@@ -89,12 +89,13 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
-def roofline_entry(us, fl, nbytes, pk):
+def roofline_entry(us, fl, nbytes, pk, tc_ratio=1.0):
     """Roofline of one isolated launch: the larger of the HBM time of its
-    algorithmic bytes and the tensor time of its flops (burst bf16 peak),
-    over the measured time."""
+    algorithmic bytes and the tensor time of its flops (burst bf16 peak,
+    times tc_ratio for other MMA kinds: 2 for fp8, the nominal 4.5 / 2.25
+    PFLOP/s ratio), over the measured time."""
     t_hbm = nbytes / (pk["hbm"] * 1e9)
-    t_tc = fl / (pk["bf16"] * 1e12)
+    t_tc = fl / (pk["bf16"] * tc_ratio * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     return {"us": round(us, 2), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
             "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bound": bound,
@@ -332,6 +333,31 @@ def extra_workloads(w4, dev, stream, pk, reps, eager=False):
         del cp, fns
     del b, sg, s_ch
 
+    # W4A8 with fp8 (E4M3) activations, per-channel, at the QQQ sweep shape
+    out["w4a8_fp8_n8192_k21760"] = []
+    e = w4synth.gen_w4a8_fp8(1, N, K, seed=250)
+    b = w4.prepack_B(e["w"].to(dev), e["wtype"], e["layout"], K, N)
+    s_ch = e["s_ch"].to(dev)
+    for M in M_SWEEP:
+        x = w4synth.gen_w4a8_fp8(M, 8, K, seed=260 + M)
+        nb = algo_bytes(M)
+        R = copies_for(nb)
+        cp = [(b, x["a"].to(dev).view(torch.float8_e4m3fn), x["s_tok"].to(dev))]
+        cp += [tuple(t.clone() for t in cp[0]) for _ in range(R - 1)]
+        o = torch.empty((M, N), dtype=torch.float16, device=dev)
+        ws = w4.workspace(dev, w4.workspace_size(M, N, K, torch.float8_e4m3fn, -1))
+        fns = [lambda c=c: w4.gemm(c[1], c[0], e["wtype"], N, group_size=-1, token_scales=c[2],
+                                   channel_scales=s_ch, out=o, ws=ws) for c in cp]
+        us = time_isolated(fns, reps, stream, eager)
+        sch = names[w4.default_schedule(M, N, K, torch.float8_e4m3fn, -1)]
+        # kind::f8f6f4 on the tensor-core schedule; the clustered decode
+        # schedule runs fp16 mma.sync
+        ent = roofline_entry(us, flops(M), nb, pk, tc_ratio=2.0 if sch.startswith("tc") else 1.0)
+        ent.update(M=M, schedule=sch)
+        out["w4a8_fp8_n8192_k21760"].append(ent)
+        del cp, fns
+    del b, s_ch
+
     # W4A16 decode, Llama-3-8B shapes (uint4 + pre-scaled bf16 zero-points, g128)
     for (n, k) in w4synth.DECODE_SHAPES:
         d = w4synth.gen_w4a16(max(w4synth.DECODE_M), n, k, act_dtype=torch.bfloat16,
@@ -441,7 +467,40 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     quant_us = e0.elapsed_time(e1) * 1e3 / 20
     quant_gbs = (3 * qm * K + 4 * qm) / (quant_us * 1e-6) / 1e9
-    del qa, qo
+    # the same for E4M3 codes
+    qo8 = [(torch.empty(qm, K, dtype=torch.float8_e4m3fn, device=dev), qo[r][1]) for r in range(4)]
+    for r in range(3):
+        w4.quantize_per_token_fp8(qa[r % 4], out=qo8[r % 4][0], scales=qo8[r % 4][1])
+    e0.record(stream)
+    for r in range(20):
+        w4.quantize_per_token_fp8(qa[r % 4], out=qo8[r % 4][0], scales=qo8[r % 4][1])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    quant8_us = e0.elapsed_time(e1) * 1e3 / 20
+    # W4A8 with the per-token quantization inside the call (fp16 activations
+    # in), against quantize + gemm, at the largest sweep M
+    dyn = {}
+    b0, sch0 = sets[0]["b"], sets[0]["s_ch"]
+    o_d = torch.empty((qm, N), dtype=torch.float16, device=dev)
+    ws_d = w4.workspace(dev, int(w4.load().w4_gemm_dynamic_workspace_size(qm, N, K, w4.S8, -1)))
+    for name, fn in (
+            ("fused", lambda r: w4.gemm_dynamic(qa[r % 4], sets[r % ROTATE]["b"], sets[0]["wtype"],
+                                                N, torch.int8, group_size=-1,
+                                                channel_scales=sch0, out=o_d, ws=ws_d)),
+            ("two_step", lambda r: w4.gemm(*w4.quantize_per_token(qa[r % 4], out=qo[r % 4][0],
+                                                                  scales=qo[r % 4][1])[:1],
+                                           sets[r % ROTATE]["b"], sets[0]["wtype"], N,
+                                           group_size=-1, token_scales=qo[r % 4][1],
+                                           channel_scales=sch0, out=o_d, ws=ws_d))):
+        for r in range(3):
+            fn(r)
+        e0.record(stream)
+        for r in range(10):
+            fn(r)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dyn[name] = round(e0.elapsed_time(e1) * 1e3 / 10, 1)
+    del qa, qo, qo8, o_d
 
     # eager warm-up (sets kernel attributes), then one graph per step of the
     # rotation pattern
@@ -623,9 +682,12 @@ def run_gpu(args):
         "sweep": sweep, "roofline": roofline, "e2e": e2e, "extra": extra,
         "prepack": {"us": round(prepack_us, 1),
                     "gbs": round(2 * K * N // 2 / (prepack_us * 1e-6) / 1e9, 1)},
-        "quantize": {"kernel": "quant_per_token_kernel<fp16>", "M": qm, "K": K,
+        "quantize": {"kernel": "quant2_kernel<fp16, int8>", "M": qm, "K": K,
                      "us": round(quant_us, 2), "gbs": round(quant_gbs, 1), "bound": "hbm",
-                     "frac": round(quant_gbs / pk["hbm"], 3)},
+                     "frac": round(quant_gbs / pk["hbm"], 3),
+                     "fp8_us": round(quant8_us, 2),
+                     "fp8_frac": round((3 * qm * K + 4 * qm) / (quant8_us * 1e-6) / 1e9 / pk["hbm"], 3)},
+        "dynamic_w4a8_m1024_us": dyn,
         "gpu_launches": launches_per_step(w4) * args.steps * len(rep_ms),
         "clocks": clk,
     }

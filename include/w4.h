@@ -265,6 +265,45 @@ w4_status w4_gemm_noalloc(const void* a, int a_type, int64_t M, int64_t K, const
 w4_status w4_quantize_per_token(const void* a, int a_type, int64_t M, int64_t K, int8_t* a_q,
                                 float* s_tok, void* stream);
 
+/* Dynamic per-token fp8 quantization of activations for W4A8 with E4M3
+ * activations (a_type W4_E4M3 of the GEMM calls): the same step as
+ * w4_quantize_per_token with E4M3 codes ([PT]: one scale per token from its
+ * own values; [PR9855]: fp8 activations).  For every row m:
+ *   s_tok[m]  = max_k |a[m][k]| / 448, in fp32 (one rounding);
+ *   a_q[m][k] = the E4M3 value nearest to a[m][k] / s_tok[m] rounded once
+ *               to fp32, ties to the even mantissa, magnitudes beyond 448
+ *               saturated to 448 (never NaN).
+ * A row of zeros gets s_tok 0 and codes 0.  Arguments, alignment and errors
+ * as w4_quantize_per_token (a_q: [M,K] bytes). */
+w4_status w4_quantize_per_token_fp8(const void* a, int a_type, int64_t M, int64_t K,
+                                    uint8_t* a_q, float* s_tok, void* stream);
+
+/* W4A8 with dynamic per-token quantization inside the call ([PT]: the
+ * activation scale of each token computed at run time from that token and
+ * applied in the epilogue; [QQQ] / [PR9855]: int8 or fp8 activations).
+ * Computes, from fp16 / bf16 activations a [M,K] (a_type W4_F16 / W4_BF16):
+ *   (a_q, s_tok) = w4_quantize_per_token (act_type W4_S8) or
+ *                  w4_quantize_per_token_fp8 (act_type W4_E4M3) of a;
+ *   out [M,N] fp16 = the W4A8 product of a_q with the weights, exactly as
+ *                  w4_gemm_bias would compute it with a_token_scales = s_tok
+ *                  (and the same schedule).
+ * The codes and scales live in the workspace (token_scales_out, when not
+ * NULL, receives s_tok [M] instead); on the tensor-core schedule the int8
+ * codes are written straight in the form that schedule reads, which saves
+ * a pass over the activations.  b_scales / scale_type / group_size / wtype /
+ * ch_scales / bias as in w4_gemm_bias; out_type is fp16.
+ * workspace: at least w4_gemm_dynamic_workspace_size(M, N, K, act_type,
+ * group_size) bytes, 16-byte aligned, zero-filled before its first use.
+ * Errors as w4_gemm_bias and w4_quantize_per_token; K must be a positive
+ * multiple of 64 (128 for fp8), else UNSUPPORTED. */
+size_t w4_gemm_dynamic_workspace_size(int64_t M, int64_t N, int64_t K, int act_type,
+                                      int64_t group_size);
+w4_status w4_gemm_dynamic(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                          int wtype, int64_t N, const void* b_scales, int scale_type,
+                          int64_t group_size, const float* ch_scales, int act_type,
+                          const void* bias, void* out, float* token_scales_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static text for a status code; message of the last failed call on this
  * host thread ("" when none). */
 const char* w4_status_string(int status);

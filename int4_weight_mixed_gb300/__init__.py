@@ -89,6 +89,13 @@ def load():
         lib.w4_override_schedule.restype = i32
         lib.w4_quantize_per_token.argtypes = [p, i32, i64, i64, p, p, p]
         lib.w4_quantize_per_token.restype = i32
+        lib.w4_gemm_dynamic_workspace_size.argtypes = [i64, i64, i64, i32, i64]
+        lib.w4_gemm_dynamic_workspace_size.restype = sz
+        lib.w4_gemm_dynamic.argtypes = [p, i32, i64, i64, p, i32, i64, p, i32, i64, p, i32, p,
+                                        p, p, p, sz, p]
+        lib.w4_gemm_dynamic.restype = i32
+        lib.w4_quantize_per_token_fp8.argtypes = [p, i32, i64, i64, p, p, p]
+        lib.w4_quantize_per_token_fp8.restype = i32
         lib.w4_check_status.argtypes = [p, sz, p]
         lib.w4_check_status.restype = i32
         lib.w4_status_string.argtypes = [i32]
@@ -292,6 +299,33 @@ def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
     return out
 
 
+def gemm_dynamic(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
+                 act_dtype: torch.dtype = torch.int8, scales: torch.Tensor | None = None,
+                 group_size: int = -1, channel_scales: torch.Tensor | None = None,
+                 bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                 token_scales_out: torch.Tensor | None = None,
+                 ws: torch.Tensor | None = None) -> torch.Tensor:
+    """w4_gemm_dynamic: fp16/bf16 activations quantized per token to int8
+    (act_dtype torch.int8) or E4M3 (torch.float8_e4m3fn) inside the call,
+    then the W4A8 product; fp16 out [M, N]."""
+    lib = load()
+    _dense_on(a.device, a=a, b_packed=b_packed, scales=scales, channel_scales=channel_scales,
+              bias=bias, out=out, token_scales_out=token_scales_out, ws=ws)
+    M, K = a.shape
+    act = _DTYPE_CODE[act_dtype]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    nbytes = int(lib.w4_gemm_dynamic_workspace_size(M, N, K, act, group_size))
+    if ws is None:
+        ws = workspace(a.device, nbytes)
+    scale_code = _DTYPE_CODE[scales.dtype] if scales is not None else S8
+    _check(lib.w4_gemm_dynamic(_ptr(a), _DTYPE_CODE[a.dtype], M, K, _ptr(b_packed), wtype, N,
+                               _ptr(scales), scale_code, group_size, _ptr(channel_scales), act,
+                               _ptr(bias), _ptr(out), _ptr(token_scales_out), _ptr(ws),
+                               ws.numel(), _stream(a.device)), "w4_gemm_dynamic")
+    return out
+
+
 def quantize_per_token(a: torch.Tensor, out: torch.Tensor | None = None,
                        scales: torch.Tensor | None = None):
     """w4_quantize_per_token: fp16/bf16 activations [M, K] -> (int8 codes
@@ -308,6 +342,27 @@ def quantize_per_token(a: torch.Tensor, out: torch.Tensor | None = None,
     assert scales.dtype == torch.float32 and scales.is_contiguous() and scales.numel() == M
     _check(lib.w4_quantize_per_token(_ptr(a), _DTYPE_CODE[a.dtype], M, K, _ptr(out), _ptr(scales),
                                      _stream(a.device)), "w4_quantize_per_token")
+    return out, scales
+
+
+def quantize_per_token_fp8(a: torch.Tensor, out: torch.Tensor | None = None,
+                           scales: torch.Tensor | None = None):
+    """w4_quantize_per_token_fp8: fp16/bf16 activations [M, K] -> (E4M3
+    codes [M, K] as torch.float8_e4m3fn, fp32 per-token scales [M]), the `a`
+    and `token_scales` of a W4A8 gemm with fp8 activations."""
+    lib = load()
+    assert a.dim() == 2 and a.is_cuda and a.is_contiguous()
+    M, K = a.shape
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device=a.device)
+    if scales is None:
+        scales = torch.empty(M, dtype=torch.float32, device=a.device)
+    assert out.dtype in (torch.float8_e4m3fn, torch.uint8) and out.is_contiguous()
+    assert out.shape == (M, K)
+    assert scales.dtype == torch.float32 and scales.is_contiguous() and scales.numel() == M
+    _check(lib.w4_quantize_per_token_fp8(_ptr(a), _DTYPE_CODE[a.dtype], M, K, _ptr(out),
+                                         _ptr(scales), _stream(a.device)),
+           "w4_quantize_per_token_fp8")
     return out, scales
 
 

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdlib>
 #include <cstdio>
@@ -643,11 +644,14 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
 }  // extern "C"
 
 namespace {
+// prestaged: W4A8 on the tensor-core schedule with its bf16 activation copy
+// already in the workspace (the dynamic-quantization entry point writes it)
 w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
                     int wtype, int64_t N, const void* b_scales, int scale_type,
                     const void* b_zeros, int64_t group_size, const float* a_token_scales,
                     const float* ch_scales, const void* bias, void* out, int out_type,
-                    void* workspace, size_t workspace_bytes, void* stream, int schedule) {
+                    void* workspace, size_t workspace_bytes, void* stream, int schedule,
+                    bool prestaged = false) {
   Problem pr{};
   w4_status st = validate(a, a_type, M, K, b_packed, wtype, N, b_scales, scale_type, b_zeros,
                           group_size, a_token_scales, ch_scales, out, out_type, pr);
@@ -866,7 +870,7 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
             plan.nsub, plan.stages, plan.tstages, plan.icol, plan.gicopy, plan.acol, plan.gps, plan.a3d,
             tc_mma2(plan) ? 1 : 0, plan.tiles, plan.kb_total, plan.grid, plan.decomp, plan.ksplit,
             plan.max_segs, plan.smem_bytes);
-  if (pr.mode == kW4A8) {
+  if (pr.mode == kW4A8 && !prestaged) {
     cudaError_t e = launch_a8_to_bf16(static_cast<const int8_t*>(a), M * K, ws + plan.ws_act, s);
     if (e != cudaSuccess) return cuda_fail(e, "int8->bf16 launch");
   }
@@ -874,9 +878,106 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "tc launch");
 }
 
+// Workspace of the dynamic-quantization call: the W4A8 GEMM's own, then the
+// codes [M][K] and the token scales [M].
+struct DynLayout {
+  int si;           // schedule of the W4A8 GEMM
+  bool prestage;    // tensor-core int8: the quantizer writes the bf16 copy
+  size_t gemm_ws, codes, stok, total;
+};
+DynLayout dyn_layout(int act_type, int64_t M, int64_t N, int64_t K, int64_t gs) {
+  DynLayout d{};
+  Problem pr{};
+  pr.mode = mode_of(act_type);
+  pr.M = M;
+  pr.N = N;
+  pr.K = K;
+  pr.gs = gs;
+  pr.has_sg = gs != K;
+  d.si = default_schedule_impl(pr.mode, M, N, K, gs, pr.has_sg);
+  d.prestage = pr.mode == kW4A8 && kSchedules[d.si].engine == kEngineTc && K % 8 == 0 &&
+               K <= 32768;
+  // the GEMM part always spans the status word and the split-K counters
+  // (which every call expects to find zero), whatever its schedule needs
+  d.gemm_ws = align256(std::max(ws_needed(d.si, pr), kWsHeader + kCounterBytes));
+  d.codes = d.gemm_ws;
+  d.stok = align256(d.codes + static_cast<size_t>(M) * K);
+  d.total = align256(d.stok + static_cast<size_t>(M) * 4);
+  return d;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t w4_gemm_dynamic_workspace_size(int64_t M, int64_t N, int64_t K, int act_type,
+                                      int64_t group_size) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % kStageK != 0) return kWsHeader;
+  if (act_type != W4_S8 && act_type != W4_E4M3) return kWsHeader;
+  const int64_t gs = group_size == -1 ? K : group_size;
+  if (gs <= 0 || K % gs != 0) return kWsHeader;
+  if (act_type == W4_E4M3 && K % 128 != 0) return kWsHeader;
+  // the largest over the schedules the call may take (the default one),
+  // with room for any schedule an override may name
+  const DynLayout d = dyn_layout(act_type, M, N, K, gs);
+  const size_t any = w4_gemm_workspace_size(M, N, K, act_type, group_size);
+  const size_t extra = d.total - d.gemm_ws;
+  return (any > d.gemm_ws ? align256(any) : d.gemm_ws) + extra;
+}
+
+w4_status w4_gemm_dynamic(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
+                          int wtype, int64_t N, const void* b_scales, int scale_type,
+                          int64_t group_size, const float* ch_scales, int act_type,
+                          const void* bias, void* out, float* token_scales_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return fail(W4_ERR_INVALID_ARGUMENT, "negative size");
+  if (a_type != W4_F16 && a_type != W4_BF16)
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16 or W4_BF16");
+  if (act_type != W4_S8 && act_type != W4_E4M3)
+    return fail(W4_ERR_INVALID_ARGUMENT, "act_type must be W4_S8 or W4_E4M3");
+  if (M == 0 || N == 0) return W4_OK;
+  if (K > 0 && !a) return fail(W4_ERR_INVALID_ARGUMENT, "a is null");
+  if (!aligned_to(a, 2) || !aligned_to(token_scales_out, 4))
+    return fail(W4_ERR_INVALID_ARGUMENT, "a pointer is not aligned to its element size");
+  if (K % 8 != 0) return fail(W4_ERR_INVALID_ARGUMENT, "K must be a multiple of 8");
+  const int64_t gs = group_size == -1 ? K : group_size;
+  if (K > 0 && (gs <= 0 || K % gs != 0))
+    return fail(W4_ERR_INVALID_ARGUMENT, "group_size must be -1 or a positive divisor of K");
+  if (K == 0 || K % kStageK != 0 || (act_type == W4_E4M3 && K % 128 != 0))
+    return fail(W4_ERR_UNSUPPORTED, "K must be a positive multiple of 64 (128 for fp8)");
+  if (!workspace || !aligned16(workspace)) return fail(W4_ERR_WORKSPACE, "workspace is null or not 16-byte aligned");
+  const DynLayout d = dyn_layout(act_type, M, N, K, gs);
+  if (workspace_bytes < d.total)
+    return fail(W4_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, d.total);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* stok = token_scales_out ? token_scales_out : reinterpret_cast<float*>(ws + d.stok);
+  void* codes = ws + d.codes;
+  // Check the GEMM's arguments before anything is enqueued (the codes and
+  // scales it will read are in the workspace).
+  {
+    Problem pr{};
+    w4_status st = validate(codes, act_type, M, K, b_packed, wtype, N, b_scales, scale_type,
+                            nullptr, group_size, stok, ch_scales, out, W4_F16, pr);
+    if (st != W4_OK) return st;
+    if (bias && !aligned_to(bias, 2))
+      return fail(W4_ERR_INVALID_ARGUMENT, "bias is not aligned to its element size");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* qdst = codes;
+  int qout = act_type == W4_E4M3 ? 2 : 0;
+  // the bf16 form is written from rows held in registers (16-byte loads)
+  const bool prestage = d.prestage && aligned16(a);
+  if (prestage) {
+    const TcPlan plan = make_plan(d.si, kW4A8, M, N, K, gs);
+    qdst = ws + plan.ws_act;
+    qout = 1;
+  }
+  cudaError_t e = launch_quant_per_token(a_type == W4_BF16, a, M, K, qdst, stok, qout, s);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return gemm_impl(codes, act_type, M, K, b_packed, wtype, N, b_scales, scale_type, nullptr,
+                   group_size, stok, ch_scales, bias, out, W4_F16, workspace, d.gemm_ws, stream,
+                   prestage ? d.si : -1, prestage);
+}
 
 w4_status w4_gemm_ex(const void* a, int a_type, int64_t M, int64_t K, const void* b_packed,
                      int wtype, int64_t N, const void* b_scales, int scale_type,
@@ -918,7 +1019,22 @@ w4_status w4_quantize_per_token(const void* a, int a_type, int64_t M, int64_t K,
   if (!aligned_to(a, 2) || !aligned_to(s_tok, 4))
     return fail(W4_ERR_INVALID_ARGUMENT, "a and s_tok must be aligned to their element size");
   if (M > 0x7fffffff) return fail(W4_ERR_UNSUPPORTED, "M above 2^31 - 1");
-  cudaError_t e = launch_quant_per_token(a_type == W4_BF16, a, M, K, a_q, s_tok,
+  cudaError_t e = launch_quant_per_token(a_type == W4_BF16, a, M, K, a_q, s_tok, 0,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4_OK : cuda_fail(e, "quantize launch");
+}
+
+w4_status w4_quantize_per_token_fp8(const void* a, int a_type, int64_t M, int64_t K,
+                                    uint8_t* a_q, float* s_tok, void* stream) {
+  if (M < 0 || K < 0) return fail(W4_ERR_INVALID_ARGUMENT, "negative size");
+  if (a_type != W4_F16 && a_type != W4_BF16)
+    return fail(W4_ERR_INVALID_ARGUMENT, "a_type must be W4_F16 or W4_BF16");
+  if (M == 0) return W4_OK;
+  if (!s_tok || (K > 0 && (!a || !a_q))) return fail(W4_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned_to(a, 2) || !aligned_to(s_tok, 4))
+    return fail(W4_ERR_INVALID_ARGUMENT, "a and s_tok must be aligned to their element size");
+  if (M > 0x7fffffff) return fail(W4_ERR_UNSUPPORTED, "M above 2^31 - 1");
+  cudaError_t e = launch_quant_per_token(a_type == W4_BF16, a, M, K, a_q, s_tok, 2,
                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4_OK : cuda_fail(e, "quantize launch");
 }

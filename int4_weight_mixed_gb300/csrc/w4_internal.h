@@ -171,8 +171,9 @@ cudaError_t launch_simt(int mode, const void* a, const TcArgs& args, cudaStream_
 cudaError_t launch_bias_rows(int mode, int64_t M, int64_t N, const void* bias, bool w4a8,
                              void* out, cudaStream_t s);
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s);
-cudaError_t launch_quant_per_token(bool bf16, const void* a, int64_t M, int64_t K, int8_t* q,
-                                   float* s_tok, cudaStream_t s);
+// out: 0 int8 codes, 1 int8 codes as bf16 values, 2 E4M3 codes
+cudaError_t launch_quant_per_token(bool bf16, const void* a, int64_t M, int64_t K, void* q,
+                                   float* s_tok, int out, cudaStream_t s);
 cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                       const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
 cudaError_t launch_dk(const DkPlan& plan, const void* a, const TcArgs& args, cudaStream_t s);

@@ -9,11 +9,15 @@
 //              integer (ties to even); a row of zeros gets s_tok 0, codes 0.
 //
 // One CTA per row; the work is HBM-bound (2 bytes read and 1 written per
-// element).  The first pass streams the row with 16-byte loads, four in
-// flight per thread, and reduces |a| to the row maximum; the second pass
-// reads the row again — from L2, where the first pass just left it — and
-// writes eight codes per 8-byte store.  Rows whose length or addresses do
-// not allow 16-byte loads take the same two passes one element at a time.
+// element).  The first pass streams the row with 16-byte loads and reduces
+// |a| to the row maximum; the second pass reads the row again — from L2,
+// where the first pass just left it, so DRAM sees it once — and writes eight
+// codes per store.  Rows whose length or addresses do not allow 16-byte
+// loads take the same two passes one element at a time.
+//
+// The same kernels make E4M3 codes for fp8 activations (vLLM PR #9855:
+// W4A8 "including fp8 activations"): s_tok = amax / 448 and each code the
+// E4M3 value nearest to fl32(a / s_tok), ties to even, saturated at 448.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -53,36 +57,47 @@ __device__ __forceinline__ float max8(const uint4& v) {
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-// The int8 code of x as a byte: the correctly rounded fp32 quotient x / s,
-// rounded to the nearest integer with ties to even.  |x| <= amax keeps the
-// quotient within 127 * (1 + 2^-23); the clamp only guards that bound.
-__device__ __forceinline__ uint32_t code(float x, float s) {
-  float r = rintf(__fdiv_rn(x, s));
-  r = fminf(fmaxf(r, -127.f), 127.f);
-  return static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu;
+// ---------------------------------------------------------------------------
+// Codes of all three kinds (int8, int8 as bf16 values — the operand the
+// tensor-core W4A8 schedule reads — and E4M3) from the same two passes: the
+// row maximum, then the codes from a second read of the row (from L2, where
+// the first pass left it).
+//
+// int8 codes without a division per element: with r = 1/s rounded once to
+// fp32, the product p = fl(x * r) differs from fl(x / s) by at most
+// |x / s| * (2^-23 + 2^-24 + 2^-47) < 2.3e-5 for |x / s| <= 127 + 2^-16; so
+// when p is farther than 2^-15 from every half-integer, both round to the
+// same integer (ties to even only matter exactly at a half-integer), and
+// only the few quotients that close are divided exactly.  (s below 2^-128
+// makes r infinite: then every code takes the division.)
+enum QuantOut { kOutS8 = 0, kOutBf16 = 1, kOutE4M3 = 2 };
+
+__device__ __forceinline__ float code_s8_fast(float x, float s, float r, bool fast) {
+  const float p = x * r;
+  const float d = fabsf(p - truncf(p));  // distance above the integer toward zero
+  float q = (!fast || fabsf(d - 0.5f) <= 0x1p-15f) ? rintf(__fdiv_rn(x, s)) : rintf(p);
+  return fminf(fmaxf(q, -127.f), 127.f);
 }
 
-// Eight codes of the 16-bit values in v, element j in byte j.
-template <typename T>
-__device__ __forceinline__ uint2 codes8(const uint4& v, float s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[2] = {0u, 0u};
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const float2 f = pair_f32<T>(w[p]);
-    out[p >> 1] |= (code(f.x, s) | (code(f.y, s) << 8)) << (16 * (p & 1));
-  }
-  return make_uint2(out[0], out[1]);
+// E4M3 byte of the correctly rounded quotient x / s: nearest-even,
+// saturated at 448
+__device__ __forceinline__ uint32_t code_e4m3(float x, float s) {
+  uint16_t e2;
+  const float v = __fdiv_rn(x, s);
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(e2) : "f"(0.f), "f"(v));
+  return e2 & 0xFFu;
 }
 
-template <typename T>
+template <typename T, int OUT>
 __global__ void __launch_bounds__(kQuantThreads)
-    quant_per_token_kernel(const T* __restrict__ a, int64_t K, int8_t* __restrict__ q,
-                           float* __restrict__ s_tok, int vec) {
+    quant2_kernel(const T* __restrict__ a, int64_t K, void* __restrict__ q,
+                  float* __restrict__ s_tok, int vec) {
+  // a GEMM launched after this one may start its weight stream now: it reads
+  // the codes and scales only after this grid is complete
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float red[kQuantThreads / 32];
   const int64_t m = blockIdx.x;
   const T* row = a + m * K;
-  int8_t* qrow = q + m * K;
 
   // pass 1: the row maximum of |a|
   float amax = 0.f;
@@ -102,39 +117,93 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
   for (int i = 1; i < kQuantThreads / 32; ++i) amax = fmaxf(amax, red[i]);
 
-  const float s = __fdiv_rn(amax, 127.f);
+  const float s = __fdiv_rn(amax, OUT == kOutE4M3 ? 448.f : 127.f);
   if (threadIdx.x == 0) s_tok[m] = s;
   const bool live = amax > 0.f;
+  const float r = __frcp_rn(s);
+  const bool fast = isfinite(r);
 
   // pass 2: the codes
   if (vec) {
     const uint4* r8 = reinterpret_cast<const uint4*>(row);
-    uint2* q8 = reinterpret_cast<uint2*>(qrow);
     const int64_t n8 = K >> 3;
-#pragma unroll 4
-    for (int64_t i = threadIdx.x; i < n8; i += kQuantThreads)
-      q8[i] = live ? codes8<T>(__ldg(r8 + i), s) : make_uint2(0u, 0u);
+#pragma unroll 2
+    for (int64_t i = threadIdx.x; i < n8; i += kQuantThreads) {
+      const uint4 v = __ldg(r8 + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 fp = pair_f32<T>(w[pp]);
+        f[2 * pp] = fp.x;
+        f[2 * pp + 1] = fp.y;
+      }
+      if constexpr (OUT == kOutE4M3) {
+        uint32_t o[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          o[e >> 2] |= (live ? code_e4m3(f[e], s) : 0u) << (8 * (e & 3));
+        reinterpret_cast<uint2*>(static_cast<uint8_t*>(q) + m * K)[i] = make_uint2(o[0], o[1]);
+      } else {
+        float c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = live ? code_s8_fast(f[e], s, r, fast) : 0.f;
+        if constexpr (OUT == kOutBf16) {
+          uint32_t o[4];
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(c[2 * pp], c[2 * pp + 1]);  // exact
+            o[pp] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(q) + m * K)[i] =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          uint32_t o[2] = {0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(c[e])) & 0xFFu) << (8 * (e & 3));
+          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + m * K)[i] = make_uint2(o[0], o[1]);
+        }
+      }
+    }
   } else {
-    for (int64_t k = threadIdx.x; k < K; k += kQuantThreads)
-      qrow[k] = static_cast<int8_t>(live ? code(one_f32(row[k]), s) : 0u);
+    for (int64_t k = threadIdx.x; k < K; k += kQuantThreads) {
+      const float x = one_f32(row[k]);
+      if constexpr (OUT == kOutE4M3) {
+        static_cast<uint8_t*>(q)[m * K + k] = static_cast<uint8_t>(live ? code_e4m3(x, s) : 0u);
+      } else {
+        const float c = live ? code_s8_fast(x, s, r, fast) : 0.f;
+        if constexpr (OUT == kOutBf16)
+          static_cast<__nv_bfloat16*>(q)[m * K + k] = __float2bfloat16_rn(c);
+        else
+          static_cast<int8_t*>(q)[m * K + k] = static_cast<int8_t>(static_cast<int>(c));
+      }
+    }
   }
+}
+
+template <typename T>
+cudaError_t launch_quant_t(int out, const void* a, int64_t M, int64_t K, void* q, float* s_tok,
+                           cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(M));
+  const int vec = K % 8 == 0 && reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(q) % (out == kOutBf16 ? 16 : 8) == 0;
+  const T* at = static_cast<const T*>(a);
+  if (out == kOutS8) quant2_kernel<T, kOutS8><<<grid, kQuantThreads, 0, s>>>(at, K, q, s_tok, vec);
+  else if (out == kOutBf16)
+    quant2_kernel<T, kOutBf16><<<grid, kQuantThreads, 0, s>>>(at, K, q, s_tok, vec);
+  else quant2_kernel<T, kOutE4M3><<<grid, kQuantThreads, 0, s>>>(at, K, q, s_tok, vec);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_quant_per_token(bool bf16, const void* a, int64_t M, int64_t K, int8_t* q,
-                                   float* s_tok, cudaStream_t s) {
+// out: 0 int8 codes, 1 int8 codes stored as bf16 values, 2 E4M3 codes
+cudaError_t launch_quant_per_token(bool bf16, const void* a, int64_t M, int64_t K, void* q,
+                                   float* s_tok, int out, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  const int vec = K % 8 == 0 && reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
-                  reinterpret_cast<uintptr_t>(q) % 8 == 0;
-  const dim3 grid(static_cast<unsigned>(M));
-  if (bf16)
-    quant_per_token_kernel<__nv_bfloat16><<<grid, kQuantThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a), K, q, s_tok, vec);
-  else
-    quant_per_token_kernel<__half><<<grid, kQuantThreads, 0, s>>>(static_cast<const __half*>(a),
-                                                                   K, q, s_tok, vec);
-  return cudaGetLastError();
+  return bf16 ? launch_quant_t<__nv_bfloat16>(out, a, M, K, q, s_tok, s)
+              : launch_quant_t<__half>(out, a, M, K, q, s_tok, s);
 }
 
 }  // namespace w4

@@ -316,3 +316,47 @@ def test_override_table(lib):
     assert lib.w4_override_schedule(1, 1, 2, 8, 72, -1, 1) == E      # K % 64
     assert lib.w4_override_schedule(1, 1, 2, 8, 256, 96, 1) == E     # group size
     assert lib.w4_override_schedule(1, 1, 2, 8, 64, -1, 99) == E     # schedule index
+
+
+
+def test_dynamic_and_fp8_argument_checks(lib):
+    """The dynamic-quantization call and fp8 activations reject bad arguments
+    on the host; the dynamic workspace covers the GEMM's plus the codes."""
+    E, U = w4.ERR_INVALID_ARGUMENT, w4.ERR_UNSUPPORTED
+    f = lib.w4_gemm_dynamic
+    base = dict(a=256, at=0, M=4, K=256, b=256, wt=2, N=128, s=None, st=2, gs=-1, ch=256, act=2,
+                bias=None, out=256, tok=None, ws=256, wsb=1 << 24, stream=None)
+
+    def call(**kw):
+        d = dict(base, **kw)
+        return f(d["a"], d["at"], d["M"], d["K"], d["b"], d["wt"], d["N"], d["s"], d["st"],
+                 d["gs"], d["ch"], d["act"], d["bias"], d["out"], d["tok"], d["ws"], d["wsb"],
+                 d["stream"])
+    assert call(at=2) == E                      # int8 input
+    assert call(act=1) == E                     # act_type must be int8 or E4M3
+    assert call(a=None) == E
+    assert call(K=100) == E                     # K % 8
+    assert call(K=320, act=4) == U              # fp8 wants K % 128
+    assert call(ws=None) == w4.ERR_WORKSPACE
+    assert call(wsb=16) == w4.ERR_WORKSPACE
+    assert call(M=0, a=None) == w4.OK
+    # the codes never overlap the header + split-K counters, even when the
+    # GEMM part itself (the clustered schedule) needs only the header
+    for M in (1, 7, 16):
+        nd = lib.w4_gemm_dynamic_workspace_size(M, 1024, 4096, 2, -1)
+        assert nd >= 256 + 64 * 1024 + M * 4096 + M * 4
+    nd = lib.w4_gemm_dynamic_workspace_size(300, 1024, 4096, 2, -1)
+    assert nd >= lib.w4_gemm_workspace_size(300, 1024, 4096, 2, -1) + 300 * 4096 + 300 * 4
+    # fp8 activations through the plain GEMM call: per-channel, fp16 out, K % 128
+    assert _gemm(lib, a_type=4, wtype=2, s=None, gs=-1, ot=0, tok=256, ch=256, K=192) == U
+    assert _gemm(lib, a_type=4, wtype=2, s=256, st=2, gs=128, ot=0, tok=256, ch=256) == U
+    assert _gemm(lib, a_type=4, wtype=2, s=None, gs=-1, ot=3) == U
+    assert _gemm(lib, a_type=4, wtype=1, s=None, gs=-1, ot=0, tok=256, ch=256) == U
+    names = w4.schedule_names()
+    pick = lambda M, N, K: names[lib.w4_default_schedule(M, N, K, 4, -1)]
+    assert pick(1, 8192, 21760) == "gv8_cl" and pick(16, 8192, 21760) == "gv16_cl"
+    assert pick(1024, 8192, 21760).startswith("tc")
+    q = lib.w4_quantize_per_token_fp8
+    assert q(1, 2, 4, 64, 1, 1, None) == E      # int8 input
+    assert q(1, 0, -1, 64, 1, 1, None) == E
+    assert q(None, 0, 0, 64, None, None, None) == w4.OK

@@ -742,3 +742,102 @@ def test_w4a8_fp8_rejections(gpu_lib):
         w4.gemm(a, b, e["wtype"], 256, group_size=-1, token_scales=e["s_tok"].to(DEV),
                 channel_scales=e["s_ch"].to(DEV), schedule=sched(w4, "ds8_sk"))
     assert ei.value.status == w4.ERR_UNSUPPORTED
+
+
+
+# ------------------------------------------- per-token fp8 quantization ---
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,K", [(1, 21760), (16, 21760), (37, 4096), (5, 72), (3, 13),
+                                 (1024, 21760), (2, 40000)])
+def test_quantize_per_token_fp8_bit_exact(gpu_lib, M, K, dt):
+    w4 = gpu_lib
+    a = w4synth.gen_act16(M, K, dt, seed=M + 3 * K)
+    q, s = w4.quantize_per_token_fp8(a.to(DEV))
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token_fp8(a)
+    assert np.array_equal(s.cpu().numpy().view(np.int32), rs.view(np.int32)), "scales"
+    bad = np.argwhere(q.cpu().view(torch.uint8).numpy() != rq)
+    assert bad.size == 0, f"{len(bad)} codes differ, first {bad[:3].tolist()}"
+
+
+@pytest.mark.parametrize("aligned", [True, False])
+def test_quantize_fp8_special_rows(gpu_lib, aligned):
+    """Zero rows, an outlier, ties between E4M3 values, the subnormal range,
+    the largest and the smallest bf16 magnitudes."""
+    w4 = gpu_lib
+    K = 264
+    dt = torch.bfloat16
+    a = w4synth.gen_act16(8, K, dt, seed=31).float()
+    a[0] = 0.0
+    a[1] = 0.0
+    a[1, 7] = -448.0
+    a[2, :6] = torch.tensor([448.0, 9.0, 11.0, 13.0, -15.0, 0.0068359375])  # ties / subnormal step
+    a[3] *= 3.0e38 / a[3].abs().max()
+    a[4] *= 1.0e-38 / a[4].abs().max()
+    a[5, ::3] = 1000.0
+    a = a.to(dt)
+    if aligned:
+        a_dev = a.to(DEV)
+    else:
+        buf = torch.zeros(a.numel() + 1, dtype=dt, device=DEV)
+        buf[1:] = a.reshape(-1).to(DEV)
+        a_dev = buf[1:].view(a.shape)
+    q, s = w4.quantize_per_token_fp8(a_dev)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token_fp8(a)
+    assert np.array_equal(s.cpu().numpy().view(np.int32), rs.view(np.int32))
+    assert np.array_equal(q.cpu().view(torch.uint8).numpy(), rq)
+    assert s[0].item() == 0 and int(q[0].view(torch.uint8).sum()) == 0
+
+
+# --------------------------- W4A8 with dynamic per-token quantization ---
+
+@pytest.mark.parametrize("M", [1, 7, 24, 40, 300, 1024])
+@pytest.mark.parametrize("gs", [-1, 128])
+def test_gemm_dynamic_int8_equals_two_steps(gpu_lib, M, gs):
+    """The fused call gives exactly what quantize_per_token followed by the
+    W4A8 gemm gives (same codes, same schedule), and its codes / scales are
+    the oracle's (through token_scales_out and the product)."""
+    w4 = gpu_lib
+    N, K = 1024, 4096
+    e = w4synth.gen_w4a8(M, N, K, group_size=gs, seed=M + 2)
+    a16 = w4synth.gen_act16(M, K, torch.float16, seed=M + 9).to(DEV)
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], K, N)
+    sg = None if e["sg"] is None else e["sg"].to(DEV)
+    sch = e["s_ch"].to(DEV)
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(3)).half().to(DEV)
+    stok = torch.empty(M, dtype=torch.float32, device=DEV)
+    out = w4.gemm_dynamic(a16, b, e["wtype"], N, torch.int8, scales=sg, group_size=gs,
+                          channel_scales=sch, bias=bias, token_scales_out=stok)
+    q, s = w4.quantize_per_token(a16)
+    ref2 = w4.gemm(q, b, e["wtype"], N, scales=sg, group_size=gs, token_scales=s,
+                   channel_scales=sch, bias=bias)
+    torch.cuda.synchronize()
+    assert torch.equal(stok, s)
+    assert torch.equal(out, ref2)
+    rq, rs = oracle.quant_per_token(a16.cpu())
+    assert np.array_equal(s.cpu().numpy().view(np.int32), rs.view(np.int32))
+    rows, cols = samples(M, N, count=64, seed=M)
+    acc = oracle.w4a8_elems(rq, e["w"], e["layout"], e["wtype"], e["sg"], gs, K, N, rows, cols)
+    prod = oracle.w4a8_scale(acc, rows, cols, rs.astype(np.float64), e["s_ch"])
+    assert_fp16_near(out.cpu().double().numpy()[rows, cols], oracle.add_bias(prod, cols, bias.cpu()),
+                     np.abs(prod) + np.abs(bias.cpu().double().numpy()[cols]), f"dynamic M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 24, 300])
+def test_gemm_dynamic_fp8(gpu_lib, M):
+    """fp8 activations quantized inside the call: the oracle's E4M3 codes and
+    scales through the oracle's W4A8-fp8 product, within the float bound."""
+    w4 = gpu_lib
+    N, K = 512, 2048
+    e = w4synth.gen_w4a8(M, N, K, group_size=-1, seed=M + 4)
+    a16 = w4synth.gen_act16(M, K, torch.bfloat16, seed=M + 5)
+    b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], K, N)
+    out = w4.gemm_dynamic(a16.to(DEV), b, e["wtype"], N, torch.float8_e4m3fn, group_size=-1,
+                          channel_scales=e["s_ch"].to(DEV))
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token_fp8(a16)
+    ref, absref = oracle.w4a8_fp8(rq, e["w"], e["layout"], e["wtype"], K, N)
+    sc = np.outer(rs.astype(np.float64), e["s_ch"].double().numpy())
+    assert_within(out.cpu().double().numpy(), ref * sc, absref * sc, "f16", f"dynamic fp8 M={M}")
