@@ -700,28 +700,66 @@ def run_gpu(args):
 
 
 def run_single(args):
-    """One GEMM of the sweep (M = args.single), eager launches: the small
-    case for ncu captures (one weight copy, ~0.2 GB on the device)."""
+    """One GEMM (M = args.single) of the sweep shape or of --shape N,K, eager
+    launches: the small case for ncu captures (one weight copy).  --act
+    int8: W4A8 (per-channel, or --group-size); fp8: W4A8 with E4M3
+    activations; bf16: W4A16 uint4 with bf16 zero-points, group 128."""
     import int4_weight_mixed_gb300 as w4
 
     dev = torch.device("cuda", 0)
     M = args.single
+    n, k = (int(x) for x in args.shape.split(","))
     gs = args.group_size
-    e = w4synth.gen_w4a8(M, N, K, group_size=gs, seed=0)
-    b = w4.prepack_B(e["w"].to(dev), e["wtype"], e["layout"], K, N)
-    a, s_tok, s_ch = e["a"].to(dev), e["s_tok"].to(dev), e["s_ch"].to(dev)
-    sg = None if e["sg"] is None else e["sg"].to(dev)
-    ws = w4.workspace(dev, w4.workspace_size(M, N, K, torch.int8, gs))
-    out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    if args.act == "bf16":
+        d = w4synth.gen_w4a16(M, n, k, act_dtype=torch.bfloat16, wtype=w4synth.UINT4,
+                              group_size=128, zeros=True, seed=0)
+        b = w4.prepack_B(d["w"].to(dev), d["wtype"], d["layout"], k, n)
+        a, s, z = d["a"].to(dev), d["s"].to(dev), d["z"].to(dev)
+        ws = w4.workspace(dev, w4.workspace_size(M, n, k, torch.bfloat16, 128))
+        out = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        call = lambda: w4.gemm(a, b, d["wtype"], n, scales=s, zeros=z, group_size=128, out=out,
+                               ws=ws, schedule=args.schedule)
+    else:
+        fp8 = args.act == "fp8"
+        e = (w4synth.gen_w4a8_fp8(M, n, k, seed=0) if fp8
+             else w4synth.gen_w4a8(M, n, k, group_size=gs, seed=0))
+        b = w4.prepack_B(e["w"].to(dev), e["wtype"], e["layout"], k, n)
+        a = e["a"].to(dev).view(torch.float8_e4m3fn) if fp8 else e["a"].to(dev)
+        s_tok, s_ch = e["s_tok"].to(dev), e["s_ch"].to(dev)
+        sg = None if fp8 or e["sg"] is None else e["sg"].to(dev)
+        ws = w4.workspace(dev, w4.workspace_size(M, n, k, a.dtype, gs))
+        out = torch.empty((M, n), dtype=torch.float16, device=dev)
+        call = lambda: w4.gemm(a, b, e["wtype"], n, scales=sg, group_size=gs, token_scales=s_tok,
+                               channel_scales=s_ch, out=out, ws=ws, schedule=args.schedule)
     for _ in range(args.warmup + args.steps):
-        w4.gemm(a, b, e["wtype"], N, scales=sg, group_size=gs, token_scales=s_tok,
-                channel_scales=s_ch, out=out, ws=ws, schedule=args.schedule)
+        call()
     torch.cuda.synchronize()
     st = w4.check_status(ws)
-    print(json.dumps({"single_M": M, "group_size": gs, "launches": args.warmup + args.steps,
-                      "status": st}))
+    print(json.dumps({"single_M": M, "N": n, "K": k, "act": args.act, "group_size": gs,
+                      "launches": args.warmup + args.steps, "status": st}))
     if st != w4.OK:
         sys.exit(1)
+
+
+def run_launch_list(args):
+    """Only the step: W warm-up then K steps of the sweep, eager launches
+    (for an ncu launch list: 15 launches of this library per step)."""
+    import int4_weight_mixed_gb300 as w4
+
+    dev = torch.device("cuda", 0)
+    w4.load()
+    sets = make_inputs(dev)
+    outs = {M: torch.empty((M, N), dtype=torch.float16, device=dev) for M in M_SWEEP}
+    ws = w4.workspace(dev, w4.workspace_size(max(M_SWEEP), N, K, torch.int8, -1))
+    for i in range(args.warmup + args.steps):
+        for j, M in enumerate(M_SWEEP):
+            st = sets[rotation(i, j)]
+            a, s_tok = st["acts"][M]
+            w4.gemm(a, st["b"], st["wtype"], N, scales=None, group_size=-1, token_scales=s_tok,
+                    channel_scales=st["s_ch"], out=outs[M], ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"launch_list_steps": args.steps, "warmup": args.warmup,
+                      "launches_per_step": launches_per_step(w4)}))
 
 
 def run_quant_single(args):
@@ -821,6 +859,11 @@ def main():
                     help="leave out the other workloads (shorter launch lists)")
     ap.add_argument("--single", type=int, default=0, help="run only the GEMM with this M")
     ap.add_argument("--group-size", type=int, default=-1, help="group size of --single")
+    ap.add_argument("--act", default="int8", choices=["int8", "fp8", "bf16"],
+                    help="activations of --single")
+    ap.add_argument("--shape", default=f"{N},{K}", help="N,K of --single")
+    ap.add_argument("--launch-list", action="store_true",
+                    help="run only warm-up + K eager steps (ncu launch lists)")
     ap.add_argument("--schedule", type=int, default=-1)
     ap.add_argument("--quant-single", type=int, default=0,
                     help="run only the per-token quantization of this many rows")
@@ -831,6 +874,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.launch_list:
+        run_launch_list(args)
     elif args.single:
         run_single(args)
     elif args.quant_single:
