@@ -72,11 +72,44 @@ __device__ __forceinline__ float max8(const uint4& v) {
 // makes r infinite: then every code takes the division.)
 enum QuantOut { kOutS8 = 0, kOutBf16 = 1, kOutE4M3 = 2 };
 
+// fast: r = 1/s is finite (s below 2^-128 takes the division everywhere)
 __device__ __forceinline__ float code_s8_fast(float x, float s, float r, bool fast) {
   const float p = x * r;
   const float d = fabsf(p - truncf(p));  // distance above the integer toward zero
   float q = (!fast || fabsf(d - 0.5f) <= 0x1p-15f) ? rintf(__fdiv_rn(x, s)) : rintf(p);
   return fminf(fmaxf(q, -127.f), 127.f);
+}
+
+// The eight int8 codes of f[] (|f| <= amax, so every code is within
+// [-127, 127]) as integers, rounded to nearest even: from the products with
+// r, and, in a branch taken only when some product lies within 2^-15 of a
+// half-integer (or r is not finite), from the exact quotients for those.
+__device__ __forceinline__ void codes8_s8(const float (&f)[8], float s, float r, bool fast,
+                                          int (&c)[8]) {
+  bool redo = !fast;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float p = f[e] * r;
+    c[e] = __float2int_rn(p);
+    redo |= fabsf(fabsf(p - truncf(p)) - 0.5f) <= 0x1p-15f;
+  }
+  if (redo) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float p = f[e] * r;
+      if (!fast || fabsf(fabsf(p - truncf(p)) - 0.5f) <= 0x1p-15f)
+        c[e] = __float2int_rn(__fdiv_rn(f[e], s));
+    }
+  }
+}
+
+// Low bytes of four ints, in order, in one word.
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+  uint32_t lo, hi, r;
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(lo) : "r"(a), "r"(b));
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(hi) : "r"(c), "r"(d));
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r) : "r"(lo), "r"(hi));
+  return r;
 }
 
 // E4M3 byte of the correctly rounded quotient x / s: nearest-even,
@@ -145,24 +178,21 @@ __global__ void __launch_bounds__(kQuantThreads)
           o[e >> 2] |= (live ? code_e4m3(f[e], s) : 0u) << (8 * (e & 3));
         reinterpret_cast<uint2*>(static_cast<uint8_t*>(q) + m * K)[i] = make_uint2(o[0], o[1]);
       } else {
-        float c[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) c[e] = live ? code_s8_fast(f[e], s, r, fast) : 0.f;
+        int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (live) codes8_s8(f, s, r, fast, c);
         if constexpr (OUT == kOutBf16) {
           uint32_t o[4];
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(c[2 * pp], c[2 * pp + 1]);  // exact
-            o[pp] = *reinterpret_cast<const uint32_t*>(&b2);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(static_cast<float>(c[2 * pp]),
+                                                            static_cast<float>(c[2 * pp + 1]));
+            o[pp] = *reinterpret_cast<const uint32_t*>(&b2);  // exact
           }
           reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(q) + m * K)[i] =
               make_uint4(o[0], o[1], o[2], o[3]);
         } else {
-          uint32_t o[2] = {0u, 0u};
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(c[e])) & 0xFFu) << (8 * (e & 3));
-          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + m * K)[i] = make_uint2(o[0], o[1]);
+          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + m * K)[i] =
+              make_uint2(pack4_s8(c[0], c[1], c[2], c[3]), pack4_s8(c[4], c[5], c[6], c[7]));
         }
       }
     }

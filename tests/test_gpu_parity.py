@@ -507,7 +507,8 @@ def _assert_quant_equal(q, s, rq, rs, what):
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("M,K", [(1, 21760), (16, 21760), (37, 4096), (5, 72), (3, 13), (2, 8),
-                                 (0, 64), (4, 0), (1024, 21760)])
+                                 (0, 64), (4, 0), (1024, 21760), (3, 65536), (2, 65600),
+                                 (7, 2048)])
 def test_quantize_per_token_bit_exact(gpu_lib, M, K, dt):
     w4 = gpu_lib
     a = w4synth.gen_act16(M, K, dt, seed=M + K)
@@ -749,7 +750,7 @@ def test_w4a8_fp8_rejections(gpu_lib):
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("M,K", [(1, 21760), (16, 21760), (37, 4096), (5, 72), (3, 13),
-                                 (1024, 21760), (2, 40000)])
+                                 (1024, 21760), (2, 40000), (3, 65536), (2, 65600)])
 def test_quantize_per_token_fp8_bit_exact(gpu_lib, M, K, dt):
     w4 = gpu_lib
     a = w4synth.gen_act16(M, K, dt, seed=M + 3 * K)
