@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libw4.so")
-SOURCES = ["w4_api.cu", "w4_kernels.cu", "w4_tc.cu", "w4_tc2.cu", "w4_dk.cu", "w4_noalloc.cu",
+SOURCES = ["w4_api.cu", "w4_kernels.cu", "w4_tc.cu", "w4_tc2.cu", "w4_tc3.cu", "w4_dk.cu", "w4_noalloc.cu",
            "w4_ds.cu", "w4_quant.cu", "w4_gv.cu"]
 HEADERS = ["w4_internal.h", "w4_ptx.cuh", "w4_tc_kernel.cuh", "w4_epilogue.cuh", os.path.join("..", "..", "include", "w4.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -51,6 +51,9 @@ const Schedule kSchedules[] = {
     {"ds32_sk", kEngineDs, 32, kStreamK, 1},
     {"gv8_cl", kEngineGv, 8, kSplitK, 1},             {"gv16_cl", kEngineGv, 16, kSplitK, 1},
     {"gv32_cl", kEngineGv, 32, kSplitK, 1},
+    // two CTAs of a cluster share each MMA (cta_group::2): 256 weight columns
+    // x 256 activation rows per tile, 128 activation rows per CTA
+    {"tc256p_sk", kEngineTc, 256, kStreamK, 1, 1},    {"tc256p_dp", kEngineTc, 256, kDataParallel, 1, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 
@@ -109,6 +112,9 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   p.mode = mode;
   p.bm = sc.bm;
   p.nt = sc.nt;
+  p.pair = sc.pair;
+  const int ncta = p.pair ? 2 : 1;
+  const int bmc = p.bm / ncta;  // activation rows in each CTA's shared memory
   // K block: 64 16-bit values (4 KB of nibbles per tile), or 128 E4M3 values
   // (8 KB) for fp8 activations
   const int bk = mode == kW4A8F8 ? 128 : kStageK;
@@ -120,24 +126,48 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   int nsub = p.bm <= 64 ? 4 : (p.bm <= 128 ? 2 : 1);
   nsub = nsub / p.nt > 0 ? nsub / p.nt : 1;
   const int64_t G = K / gs;
-  if (G > 1)  // a stage must cover whole groups or lie inside one group
-    while (nsub > 1 && (nsub * kStageK) % gs != 0 && gs % (nsub * kStageK) != 0) nsub /= 2;
+  auto group_ok = [&](int ns) {  // a stage covers whole groups or lies inside one
+    return G <= 1 || (ns * kStageK) % gs == 0 || gs % (ns * kStageK) == 0;
+  };
+  while (nsub > 1 && !group_ok(nsub)) nsub /= 2;
+  // The converter groups need at least kConvGroups stages in shared memory
+  // (the order of their barrier waits relies on it): shallower stages when
+  // the deep ones do not fit that many times.
+  while (nsub > 1 && tc_max_stages(bmc, nsub, p.nt, wblk) < kConvGroups) {
+    nsub /= 2;
+    while (nsub > 1 && !group_ok(nsub)) nsub /= 2;
+  }
   p.nsub = nsub;
   p.gps = (G > 1 && gs < nsub * kStageK) ? static_cast<int>(nsub * kStageK / gs) : 1;
-  p.stages = tc_max_stages(p.bm, nsub, p.nt, wblk);
-  p.smem_bytes = tc_smem_bytes(p.bm, nsub, p.nt, p.stages, wblk);
+  p.stages = tc_max_stages(bmc, nsub, p.nt, wblk);
+  p.smem_bytes = tc_smem_bytes(bmc, nsub, p.nt, p.stages, wblk);
   p.m_tiles = static_cast<int>((M + p.bm - 1) / p.bm);
   p.n128 = static_cast<int>((N + kTileN - 1) / kTileN);
-  p.n_tiles = (p.n128 + p.nt - 1) / p.nt;
+  p.n_tiles = (p.n128 + p.nt * ncta - 1) / (p.nt * ncta);
   p.tiles = p.m_tiles * p.n_tiles;
   p.k64 = static_cast<int>(K / bk);
   p.kb_total = (p.k64 + nsub - 1) / nsub;
   // W4A8 exactness: |a| <= 128 and |v*sg| <= 128 (group) or |v| <= 8
   // (per-channel) keep every fp32 partial sum of a chunk within 2^24.
   p.chunk_stages = static_cast<int>(((gs < K) ? 1024 : 16384) / (kStageK * nsub));
-  const int sms = sm_count();
+  // units of work distribution: CTAs, or the two-CTA clusters that can be
+  // resident at once
+  int sms = sm_count();
+  if (p.pair) {
+    // queried once per mode (a pair plan's shared memory depends on the mode
+    // only); without a device, one pair per two SMs
+    static std::mutex mu;
+    static int cache[4];  // resident clusters + 1 (0: not yet queried)
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[mode] == 0) {
+      const int c = tc_pair_clusters(mode, p.smem_bytes);
+      cache[mode] = (c > 0 ? c : sms / 2) + 1;
+    }
+    sms = cache[mode] - 1;
+  }
   p.decomp = sc.decomp;
-  if (p.tiles * static_cast<size_t>(kConvWarps) * 4 > kCounterBytes) p.decomp = kDataParallel;
+  if (p.tiles * static_cast<size_t>(kConvWarps) * 4 * ncta > kCounterBytes)
+    p.decomp = kDataParallel;
   p.ws_counters = kWsHeader;
   p.ws_partials = p.ws_counters + kCounterBytes;
   p.ksplit = 1;
@@ -145,7 +175,7 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   size_t part = 0;
   const size_t slot_bytes = static_cast<size_t>(p.nt) * kTileN * p.bm * 4;
   if (p.decomp == kDataParallel) {
-    p.grid = p.tiles < sms ? p.tiles : sms;
+    p.grid = (p.tiles < sms ? p.tiles : sms) * ncta;
   } else if (p.decomp == kSplitK) {
     // K splits: W4A8 splits at least until no unit is longer than one exact
     // chunk; then the split count minimizes waves x stages per unit, with a
@@ -167,14 +197,14 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
     }
     p.ksplit = best_ks;
     const int64_t units = static_cast<int64_t>(p.tiles) * p.ksplit;
-    p.grid = static_cast<int>(units < sms ? units : sms);
-    if (p.ksplit > 1) part = static_cast<size_t>(p.tiles) * p.ksplit * slot_bytes;
+    p.grid = static_cast<int>(units < sms ? units : sms) * ncta;
+    if (p.ksplit > 1) part = static_cast<size_t>(p.tiles) * p.ksplit * slot_bytes * ncta;
   } else {
     const int64_t T = static_cast<int64_t>(p.tiles) * p.kb_total;
-    int64_t g = T / 2;  // at least 2 stages per CTA
+    int64_t g = T / 2;  // at least 2 stages per CTA (pair)
     if (g > sms) g = sms;
     if (g < 1) g = 1;
-    p.grid = static_cast<int>(g);
+    p.grid = static_cast<int>(g) * ncta;
     int ms = 1;
     for (int64_t c = 0; c < g; ++c) {
       int64_t b = c * T / g, e = (c + 1) * T / g;
@@ -183,7 +213,7 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
       if (segs > ms) ms = segs;
     }
     p.max_segs = ms;
-    part = static_cast<size_t>(p.grid) * p.max_segs * slot_bytes;
+    part = static_cast<size_t>(p.grid) * p.max_segs * slot_bytes;  // one slot set per CTA
   }
   // Tensor memory: accumulators (NT x BM columns), the W4A8 int32 copies
   // when a unit can span several exact chunks, then the converted-weight
@@ -205,6 +235,7 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   if (p.ksplit > 16) ts = 0;  // too many partial sums to be worth it: not offered
   if (ts > kMaxTmemStages) ts = kMaxTmemStages;
   if (ts > p.stages - 1) ts = p.stages - 1;
+  if (p.stages < kConvGroups) ts = 0;  // not offered (see above)
   p.tstages = ts;
   p.ws_act = align256(p.ws_partials + part);
   size_t act = mode == kW4A8 ? static_cast<size_t>(M) * K * 2 : 0;
@@ -802,7 +833,7 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
     // E4M3 [M][K]: one 2-D box of 128 K x BM rows per K block (128-byte rows)
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(plan.bm)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(plan.bm / (plan.pair ? 2 : 1))};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(act), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -817,7 +848,7 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
                                  static_cast<cuuint64_t>(K / kStageK)};
     const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(K) * 2, 128};
     const cuuint32_t box3[3] = {static_cast<cuuint32_t>(kStageK),
-                                static_cast<cuuint32_t>(plan.bm),
+                                static_cast<cuuint32_t>(plan.bm / (plan.pair ? 2 : 1)),
                                 static_cast<cuuint32_t>(plan.nsub)};
     const cuuint32_t estr3[3] = {1, 1, 1};
     CUresult r = enc(&amap, t16, 3, const_cast<void*>(act), dims3, strides3, box3, estr3,
@@ -828,7 +859,7 @@ w4_status gemm_impl(const void* a, int a_type, int64_t M, int64_t K, const void*
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
       const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
       const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK),
-                                 static_cast<cuuint32_t>(plan.bm)};
+                                 static_cast<cuuint32_t>(plan.bm / (plan.pair ? 2 : 1))};
       const cuuint32_t estr[2] = {1, 1};
       r = enc(&amap, t16, 2, const_cast<void*>(act), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -58,6 +58,7 @@ struct Schedule {
   int bm;      // activation rows per tile (UMMA N)
   int decomp;  // kDataParallel / kStreamK / kSplitK
   int nt;      // 128-column weight tiles per CTA (tc): 1, or 2 to share each activation tile
+  int pair;    // tc: 1 = two CTAs of a cluster share each MMA (tile of 256 weight columns)
 };
 
 // Everything a tc launch needs, computed on the host.
@@ -65,6 +66,8 @@ struct TcPlan {
   int mode;
   int bm;
   int nt;              // 128-column weight tiles per CTA tile (1 or 2)
+  int pair;            // CTA pairs (cta_group::2): tile = 2 x nt x 128 weight columns,
+                       // each CTA holding bm / 2 activation rows; grid = 2 x pairs
   int n128;            // ceil(N / 128): prepacked weight tiles that exist
   int ksplit;          // kSplitK: K splits per tile
   int icol;            // W4A8: first tensor-memory column of the int32 copies (0 = none)
@@ -92,7 +95,7 @@ struct TcPlan {
 
 // MMA groups issued by two alternating threads (else one): where a group's
 // MMAs are short (N <= 128 activation rows)
-inline bool tc_mma2(const TcPlan& p) { return p.bm <= 128; }
+inline bool tc_mma2(const TcPlan& p) { return p.bm <= 128 && !p.pair; }
 
 struct TcArgs {
   const uint8_t* b_packed;
@@ -189,5 +192,7 @@ cudaError_t launch_gv(const GvPlan& plan, const CUtensorMap& amap, const TcArgs&
 size_t tc_stage_bytes(int bm, int nsub, int nt, int wblk);
 size_t tc_smem_bytes(int bm, int nsub, int nt, int stages, int wblk);
 int tc_max_stages(int bm, int nsub, int nt, int wblk);
+// Most co-resident two-CTA clusters of the pair kernel (-1 without a device).
+int tc_pair_clusters(int mode, size_t smem);
 
 }  // namespace w4

@@ -424,6 +424,132 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(uint32_t ab_format, uint3
          ((128u >> 4) << 24);
 }
 
+// --------------------------------------------- CTA pairs (cta_group::2)
+// A cluster of two CTAs on two SMs shares each tcgen05.mma: rank 0 issues
+// it, each CTA holds its half of the A rows (tensor memory) and of the B
+// columns (shared memory), and each CTA's tensor memory receives its half of
+// D.  Every tcgen05 instruction of such a kernel takes cta_group::2.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes
+// (barrier initialisation included) before the other CTAs' later accesses.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Shared::cluster address of the same object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Arrive (release, cluster scope) on an mbarrier given by its
+// shared::cluster address, which may lie in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for a barrier that threads of the other CTA arrive on (acquire at
+// cluster scope); bounded the same way.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, int* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > W4_WAIT_TIMEOUT_NS) {
+        *abort = 1;
+        if (status) atomicExch(status, 5 /* W4_ERR_TIMEOUT */);
+        return false;
+      }
+    }
+  }
+}
+// Tensor memory of a CTA pair: one warp of each of the two CTAs issues these.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Arrive once on the barrier at the same shared-memory offset in both CTAs of
+// the pair when every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+// Four / eight pair MMAs (M = 256 across the two CTAs), operands as mma_ts_4
+// / mma_ts_8.
+#define W4_MMA2_LINE(KIND, A, B, P) \
+  "tcgen05.mma.cta_group::2.kind::" KIND " [%0], [%" #A "], %" #B ", %1, " P ";\n\t"
+#define W4_MMA2_X4_STR(KIND)                                                        \
+  "{\n\t.reg .pred p, t;\n\t"                                                      \
+  "setp.ne.b32 p, %2, 0;\n\t"                                                      \
+  "setp.eq.b32 t, %2, %2;\n\t" W4_MMA2_LINE(KIND, 3, 7, "p")                       \
+      W4_MMA2_LINE(KIND, 4, 8, "t") W4_MMA2_LINE(KIND, 5, 9, "t")                  \
+      W4_MMA2_LINE(KIND, 6, 10, "t") "}"
+template <bool F8 = false>
+__device__ __forceinline__ void mma_pair_4(uint32_t d_tmem, const uint32_t* a, const uint64_t* b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  if constexpr (F8)
+    asm volatile(W4_MMA2_X4_STR("f8f6f4")::W4_MMA_X4_OPS : "memory");
+  else
+    asm volatile(W4_MMA2_X4_STR("f16")::W4_MMA_X4_OPS : "memory");
+}
+#define W4_MMA2_X8_STR(KIND)                                                        \
+  "{\n\t.reg .pred p, t;\n\t"                                                      \
+  "setp.ne.b32 p, %2, 0;\n\t"                                                      \
+  "setp.eq.b32 t, %2, %2;\n\t" W4_MMA2_LINE(KIND, 3, 11, "p")                      \
+      W4_MMA2_LINE(KIND, 4, 12, "t") W4_MMA2_LINE(KIND, 5, 13, "t")                \
+      W4_MMA2_LINE(KIND, 6, 14, "t") W4_MMA2_LINE(KIND, 7, 15, "t")                \
+      W4_MMA2_LINE(KIND, 8, 16, "t") W4_MMA2_LINE(KIND, 9, 17, "t")                \
+      W4_MMA2_LINE(KIND, 10, 18, "t") "}"
+template <bool F8 = false>
+__device__ __forceinline__ void mma_pair_8(uint32_t d_tmem, const uint32_t (&a)[8],
+                                           const uint64_t (&b)[8], uint32_t idesc,
+                                           uint32_t accumulate) {
+  if constexpr (F8)
+    asm volatile(W4_MMA2_X8_STR("f8f6f4")::W4_MMA_X8_OPS : "memory");
+  else
+    asm volatile(W4_MMA2_X8_STR("f16")::W4_MMA_X8_OPS : "memory");
+}
+// Instruction descriptor with an explicit M (128, or 256 for a CTA pair).
+__host__ __device__ __forceinline__ uint32_t idesc_f16_m(uint32_t ab_format, uint32_t n,
+                                                        uint32_t m) {
+  return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -1,7 +1,7 @@
 // w4_tc.cu — the tensor-core schedule of the 4-bit-weight GEMM for sm_103a:
 // shared-memory sizing, the one-issuer kernel instantiations and the launch
 // dispatch (the kernel itself is in w4_tc_kernel.cuh; the two-issuer variant
-// is compiled in w4_tc2.cu).
+// is compiled in w4_tc2.cu, the CTA-pair variant in w4_tc3.cu).
 #include "w4_tc_kernel.cuh"
 
 namespace w4 {
@@ -18,18 +18,22 @@ size_t tc_smem_bytes(int bm, int nsub, int nt, int stages, int wblk) {
   return 1024 + tc_stage_bytes(bm, nsub, nt, wblk) * stages + bars + 64;  // + slot, abort, tok[2]
 }
 
+// Most pipeline stages that fit in shared memory (0 when none does).
 int tc_max_stages(int bm, int nsub, int nt, int wblk) {
   const size_t budget = 225 * 1024;
   int s = kMaxStages;
-  while (s > 2 && tc_smem_bytes(bm, nsub, nt, s, wblk) > budget) --s;
+  while (s > 0 && tc_smem_bytes(bm, nsub, nt, s, wblk) > budget) --s;
   return s;
 }
 
 cudaError_t launch_tc_mma2(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                            const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
+cudaError_t launch_tc_pair(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                           const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s);
 
 cudaError_t launch_tc(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                       const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  if (plan.pair) return launch_tc_pair(plan, amap, smap, zmap, args, s);
   if (!tc_mma2(plan)) return launch_tc_t<false>(plan, amap, smap, zmap, args, s);
   return launch_tc_mma2(plan, amap, smap, zmap, args, s);
 }

@@ -1,0 +1,22 @@
+// w4_tc3.cu — the CTA-pair variant of the tensor-core kernel (two CTAs of a
+// cluster share each tcgen05.mma, cta_group::2; see w4_tc_kernel.cuh),
+// compiled apart from the other variants.
+#include "w4_tc_kernel.cuh"
+
+namespace w4 {
+
+cudaError_t launch_tc_pair(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                           const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  return launch_tc_t<false, true>(plan, amap, smap, zmap, args, s);
+}
+
+int tc_pair_clusters(int mode, size_t smem) {
+  switch (mode) {
+    case kW4A16_F16: return tc_pair_clusters_mode<kW4A16_F16>(smem);
+    case kW4A16_BF16: return tc_pair_clusters_mode<kW4A16_BF16>(smem);
+    case kW4A8F8: return tc_pair_clusters_mode<kW4A8F8>(smem);
+    default: return tc_pair_clusters_mode<kW4A8>(smem);
+  }
+}
+
+}  // namespace w4

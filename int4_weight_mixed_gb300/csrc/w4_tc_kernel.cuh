@@ -65,8 +65,9 @@ struct Unit {
 };
 
 struct Work {
-  int64_t T, G, kb;
-  int64_t begin, end;  // stream-K range of this CTA
+  int64_t T, G, kb;    // G: CTAs, or CTA pairs (the unit of work distribution)
+  int64_t me;          // this CTA's (or pair's) index among the G
+  int64_t begin, end;  // stream-K range of this CTA (pair)
   int64_t first_tile;
 };
 
@@ -82,7 +83,7 @@ __device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
   if (p.decomp == kSplitK) {
     // units (tile, split), c, c+G, ...: split j covers stages
     // [j*kb/ks, (j+1)*kb/ks) of its tile
-    const int64_t v = blockIdx.x + static_cast<int64_t>(u) * p.grid;
+    const int64_t v = w.me + static_cast<int64_t>(u) * w.G;
     if (v >= static_cast<int64_t>(p.tiles) * p.ksplit) return false;
     const int t = static_cast<int>(div_nn(v, p.ksplit)), j = static_cast<int>(v - static_cast<int64_t>(t) * p.ksplit);
     out.tile = t;
@@ -95,13 +96,13 @@ __device__ bool next_unit(const TcPlan& p, const Work& w, int u, Unit& out) {
     return true;
   }
   if (p.decomp == kDataParallel) {
-    int64_t t = blockIdx.x + static_cast<int64_t>(u) * p.grid;
+    int64_t t = w.me + static_cast<int64_t>(u) * w.G;
     if (t >= p.tiles) return false;
     out.tile = static_cast<int>(t);
     out.kb0 = 0;
     out.kb1 = p.kb_total;
     out.nslots = 1;
-    out.cfirst = blockIdx.x;
+    out.cfirst = static_cast<int>(w.me);
     out.seg = 0;
     out.split = 0;
     return true;
@@ -131,9 +132,9 @@ __device__ __forceinline__ size_t slot_index(const TcPlan& p, const Work& w, con
   const int64_t seg = u.tile - div_nn(sk_start(cpr, w.T, w.G), w.kb);
   return static_cast<size_t>(cpr) * p.max_segs + seg;
 }
-__device__ __forceinline__ size_t own_slot(const TcPlan& p, const Unit& u) {
+__device__ __forceinline__ size_t own_slot(const TcPlan& p, const Work& w, const Unit& u) {
   if (p.decomp == kSplitK) return static_cast<size_t>(u.tile) * p.ksplit + u.split;
-  return static_cast<size_t>(blockIdx.x) * p.max_segs + u.seg;
+  return static_cast<size_t>(w.me) * p.max_segs + u.seg;
 }
 
 // Tile -> (m_tile, n_tile), grouped raster: runs of up to 8 m-tiles share
@@ -259,7 +260,15 @@ struct Smem {
 }  // namespace
 
 // MMA2: two alternating MMA-issuing threads; a separate instantiation.
-template <int MODE, bool MMA2>
+// PAIR: a cluster of two CTAs shares every MMA (cta_group::2, M = 256): CTA
+// rank r converts weight columns [n0 + 128r, n0 + 128r + 128) of the pair's
+// 256-column tile into its own tensor memory and loads activation rows
+// [y + BM/2 r, y + BM/2 (r + 1)) of the BM-row tile into its own shared
+// memory; rank 0 issues the MMAs, which give each CTA the sums of its 128
+// weight columns against all BM rows.  Per SM the MMA work of a stage is
+// that of a single CTA, but the activation bytes per stage halve, so twice
+// as many stages fit in shared memory.
+template <int MODE, bool MMA2, bool PAIR = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap amap,
                    const __grid_constant__ CUtensorMap smap,
@@ -272,11 +281,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int BK = F8 ? 128 : kStageK;
   constexpr uint32_t WB = F8 ? 8192u : 4096u;
   constexpr int CPB = BK / kChunkK;  // 32-K chunks per block
+  static_assert(!(PAIR && MMA2), "a CTA pair has one MMA issuer");
+  constexpr int NCTA = PAIR ? 2 : 1;
+  if constexpr (PAIR) {
+    // launched without its two-CTA clusters: nothing may run
+    if (cluster_size() != 2) {
+      if (threadIdx.x == 0) atomicExch(args.status, 4 /* W4_ERR_CUDA */);
+      return;
+    }
+  }
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages, NT = p.nt;
-  const uint32_t a_sub = static_cast<uint32_t>(BM) * 128;  // bytes of one 64-K activation tile
+  const int BMc = BM / NCTA;  // activation rows held by this CTA
+  const uint32_t a_sub = static_cast<uint32_t>(BMc) * 128;  // bytes of one 64-K activation tile
   Smem sm;
   sm.a = base;
   sm.w = sm.a + static_cast<size_t>(S) * NS * a_sub;             // [S][NT][NS][4096]
@@ -301,9 +321,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sm.full[i], 2);  // weight producer + activation producer
       mbar_init(&sm.empty[i], 4 + 1);  // one converter group + the MMA commit
     }
-    for (int i = 0; i < TS; ++i) mbar_init(&sm.tfull[i], 4);
+    // tfull / dempty: the converter warps of both CTAs of a pair arrive on
+    // rank 0's (the other CTA's copies stay unused)
+    for (int i = 0; i < TS; ++i) mbar_init(&sm.tfull[i], 4 * NCTA);
     mbar_init(sm.dfull, 1);
-    mbar_init(sm.dempty, kConvWarps);
+    mbar_init(sm.dempty, kConvWarps * NCTA);
     mbar_init(sm.fin, MMA2 ? 2 : 1);  // one commit per MMA issuing thread
     if constexpr (MMA2) {
       mbar_init(&sm.tok[0], 1);
@@ -316,21 +338,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (args.zeros) prefetch_tensormap(&zmap);
   }
   if (warp == kProdWarp) {
-    tmem_alloc(sm.tmem_slot, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(sm.tmem_slot, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(sm.tmem_slot, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers initialised
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
+  // rank 0's tfull / dempty, as seen from this CTA
+  const uint32_t tfull_c = PAIR ? peer_addr(smem_addr(sm.tfull), 0) : smem_addr(sm.tfull);
+  const uint32_t dempty_c = PAIR ? peer_addr(smem_addr(sm.dempty), 0) : smem_addr(sm.dempty);
 
 
   Work wk;
   wk.kb = p.kb_total;
   wk.T = static_cast<int64_t>(p.tiles) * p.kb_total;
-  wk.G = p.grid;
-  wk.begin = sk_start(blockIdx.x, wk.T, wk.G);
-  wk.end = sk_start(blockIdx.x + 1, wk.T, wk.G);
+  wk.G = p.grid / NCTA;
+  wk.me = blockIdx.x / NCTA;
+  wk.begin = sk_start(wk.me, wk.T, wk.G);
+  wk.end = sk_start(wk.me + 1, wk.T, wk.G);
   wk.first_tile = div_nn(wk.begin, wk.kb);
 
   const int64_t M = args.M, N = args.N, K = args.K;
@@ -371,13 +403,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         int mt, nt;
         tile_coords(p, u.tile, mt, nt);
-        const int32_t n0 = nt * NT * kTileN;       // first weight column of the CTA tile
-        const int32_t y = mt * BM;
-        int ntv = p.n128 - nt * NT;                 // weight tiles that exist (ragged N)
+        const int wt0 = (nt * NCTA + static_cast<int>(rank)) * NT;  // first weight tile of this CTA
+        const int32_t n0 = wt0 * kTileN;           // first weight column of the CTA tile
+        const int32_t y = mt * BM + static_cast<int>(rank) * BMc;
+        int ntv = p.n128 - wt0;                     // weight tiles that exist (ragged N)
         if (ntv > NT) ntv = NT;
+        if (ntv < 0) ntv = 0;
         const uint8_t* wsrc =
             args.b_packed +
-            ((static_cast<int64_t>(nt) * NT * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * CPB) *
+            ((static_cast<int64_t>(wt0) * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * CPB) *
              kTileN) * 16;
         const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
         // scale group of the stage, kept without division per stage
@@ -444,14 +478,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // MMAs accumulate after all earlier ones.  Without MMA2, the MMA warp
     // alone issues every group (the loop right below).
     if constexpr (!MMA2) {
-    if (lane == 0 && warp == kMmaWarp) {
-      const uint32_t idesc =
-          idesc_f16(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u, static_cast<uint32_t>(BM));
+    if (lane == 0 && warp == kMmaWarp && rank != 0) {
+      // a pair's MMAs are issued by rank 0: wait for their last commit, so
+      // that this CTA's tensor and shared memory outlive them
+      volatile int no_abort = 0;
+      mbar_wait(sm.fin, 0, &no_abort, args.status);
+    } else if (lane == 0 && warp == kMmaWarp) {
+      const uint32_t idesc = idesc_f16_m(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u,
+                                         static_cast<uint32_t>(BM), PAIR ? 256u : 128u);
       const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
       const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
       uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0;
       bool ok = true;
       Unit u;
+      // barriers the other CTA of a pair arrives on are read at cluster scope
+      auto wait_x = [&](uint64_t* bar, uint32_t par) {
+        if constexpr (PAIR) return mbar_wait_cluster(bar, par, abort, args.status);
+        else return mbar_wait(bar, par, abort, args.status);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (PAIR) mma_commit_pair(bar);
+        else mma_commit(bar);
+      };
       for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
         bool chunk_start = true;
         const int nkb = u.kb1 - u.kb0;
@@ -470,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         for (int j = 0; j < nkb;) {
           if (chunk_start) {
-            if (ev > 0 && !mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) {
+            if (ev > 0 && !wait_x(sm.dempty, (ev - 1) & 1)) {
               ok = false;
               break;
             }
@@ -480,8 +528,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // per group) when both belong to the same exact chunk.
           const bool pair = NS == 1 && NT == 1 && TS >= 2 && left >= 2;
           // The converter group arrives on tfull only after it observed the
-          // stage's full barrier, so tfull also orders the activation tile.
-          if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
+          // stage's full barrier, so tfull also orders the activation tile
+          // (of both CTAs of a pair).
+          if (!wait_x(&sm.tfull[ts], tph)) {
             ok = false;
             break;
           }
@@ -492,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ts2 = 0;
             tph2 ^= 1;
           }
-          if (pair && !mbar_wait(&sm.tfull[ts2], tph2, abort, args.status)) {
+          if (pair && !wait_x(&sm.tfull[ts2], tph2)) {
             ok = false;
             break;
           }
@@ -517,12 +566,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               // W4A8: the first stage's shared-memory slot is released as soon
               // as its own four MMAs retire (measured 3% faster at 256-row
               // tiles; W4A16 measured slower with the extra commit)
-              mma_ts_4<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
-              mma_commit(&sm.empty[s1]);
-              mma_ts_4<F8>(tmem, a8 + 4, b8 + 4, idesc, 1u);
+              if constexpr (PAIR) {
+                mma_pair_4<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+                commit(&sm.empty[s1]);
+                mma_pair_4<F8>(tmem, a8 + 4, b8 + 4, idesc, 1u);
+              } else {
+                mma_ts_4<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+                commit(&sm.empty[s1]);
+                mma_ts_4<F8>(tmem, a8 + 4, b8 + 4, idesc, 1u);
+              }
             } else {
-              mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              if constexpr (PAIR) mma_pair_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              else mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
             }
+          } else if constexpr (PAIR) {
+            // one stage of one 64-K block (the pair kernel has NS = NT = 1)
+            uint32_t a4[4];
+            uint64_t b4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              a4[i] = tmem + p.acol + ts * 32 + 8 * i;
+              b4[i] = desc0 + s * sub16 + 2 * i;
+            }
+            mma_pair_4<F8>(tmem, a4, b4, idesc, chunk_start ? 0u : 1u);
           } else {
             const int k64_0 = (u.kb0 + j) * NS;
             const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
@@ -539,10 +605,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
           }
-          if (!(MODE == kW4A8 && pair)) mma_commit(&sm.empty[s1]);
+          if (!(MODE == kW4A8 && pair)) commit(&sm.empty[s1]);
           advance();
           if (pair) {
-            mma_commit(&sm.empty[s2]);
+            commit(&sm.empty[s2]);
             advance();
           }
           const int used = pair ? 2 : 1;
@@ -550,14 +616,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           left -= used;
           chunk_start = false;
           if (left == 0) {
-            mma_commit(sm.dfull);
+            commit(sm.dfull);
             ++ev;
             chunk_start = true;
           }
         }
       }
       // All issued MMAs complete before tensor memory is released.
-      mma_commit(sm.fin);
+      commit(sm.fin);
       volatile int no_abort = 0;
       mbar_wait(sm.fin, 0, &no_abort, args.status);
     }
@@ -718,7 +784,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
       int mt, nt;
       tile_coords(p, u.tile, mt, nt);
-      const int64_t n0 = static_cast<int64_t>(nt) * NT * kTileN;  // first weight column
+      // first weight column of this CTA's tile; the accumulator covers all BM
+      // rows of the (pair's) tile
+      const int64_t n0 = (static_cast<int64_t>(nt) * NCTA + rank) * NT * kTileN;
       const int64_t m0 = static_cast<int64_t>(mt) * BM;
       const int nkb = u.kb1 - u.kb0;
       const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
@@ -741,16 +809,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (cleft == 0) cleft = chunk_len < nkb - j ? chunk_len : nkb - j;
         if (static_cast<int>(it % kConvGroups) == grp) {
           const uint32_t s = cs, ts = cts;
-          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], cph, abort, args.status))) {
-            ok = false;
-            break;
-          }
+          // The tensor-memory slot first: it is free once the MMA of stage
+          // it-TS retired.  MMAs retire in order, so stage it-S (TS < S),
+          // the previous user of shared-memory slot s, has then been converted
+          // and its copies have landed; only after that is the parity wait on
+          // full[s] unambiguous.  (A group converts every kConvGroups-th stage:
+          // nothing else orders this group's wait after the landing of stage
+          // it-S, which another group converted; were that phase still
+          // pending, the parity wait would pass at once.)  The slot wait itself
+          // is unambiguous for S >= kConvGroups: this group's previous slot
+          // wait (stage it-kConvGroups-TS) already covers stage it-TS-S.
           if (it >= static_cast<uint32_t>(TS)) {
-            // the tensor-memory slot is free once the MMA of stage it-TS retired
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.empty[ps], pph, abort, args.status))) {
               ok = false;
               break;
             }
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], cph, abort, args.status))) {
+            ok = false;
+            break;
           }
           tc_fence_after();
           const int k64_0 = (u.kb0 + j) * NS;
@@ -814,8 +891,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&sm.tfull[ts]);
+            // empty first: once the MMA thread sees tfull, this group's share
+            // of the stage's release has been counted
             mbar_arrive(&sm.empty[s]);
+            if constexpr (PAIR) mbar_arrive_cluster(tfull_c + ts * 8);
+            else mbar_arrive(&sm.tfull[ts]);
           }
         }
         const bool chunk_end = --cleft == 0;
@@ -830,7 +910,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // The last to arrive adds the others' partial sums to its own
         // accumulator; the others write theirs and then count themselves as
         // written (high half), which the last one waits for.
-        int* ctr = args.counters + static_cast<size_t>(u.tile) * kConvWarps + cw;
+        int* ctr = args.counters + (static_cast<size_t>(u.tile) * NCTA + rank) * kConvWarps + cw;
         bool reducer = false;
         if (split) {
           int prev_count = 0;
@@ -840,9 +920,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // position of this unit among the tile's contributors (K order), and
         // the slot of contributor sl held by lane sl (<= 32 contributors)
-        const int my_sl = p.decomp == kSplitK ? u.split : static_cast<int>(blockIdx.x) - u.cfirst;
+        // (a pair's two CTAs keep separate slots: pair slot * NCTA + rank)
+        const int my_sl = p.decomp == kSplitK ? u.split : static_cast<int>(wk.me) - u.cfirst;
         const size_t lane_slot =
-            reducer && lane < u.nslots ? slot_index(p, wk, u, lane) * slot_elems : 0;
+            reducer && lane < u.nslots ? (slot_index(p, wk, u, lane) * NCTA + rank) * slot_elems : 0;
         // Pull what this drain will read toward L2 while the last MMAs run:
         // the other contributors' partial sums (reducer) and the int32
         // running sum of the earlier chunks (W4A8 with the global copy).
@@ -858,7 +939,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   u.nslots <= 32
                       ? static_cast<size_t>(__shfl_sync(
                             0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
-                      : slot_index(p, wk, u, sl) * slot_elems;
+                      : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
               prefetch_l2(part + sbase + coff);
             }
           }
@@ -879,7 +960,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           __threadfence();
         }
-        const size_t my_slot = split && !reducer ? own_slot(p, u) * slot_elems : 0;
+        const size_t my_slot =
+            split && !reducer ? (own_slot(p, wk, u) * NCTA + rank) * slot_elems : 0;
         // Blocks of 8 accumulator columns over all weight tiles, round-robin
         // over the converter groups.  Global layout of partial sums and of
         // the int32 running sum: block (t, cc) is 128 rows x 8 columns, row r
@@ -936,7 +1018,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     u.nslots <= 32
                         ? static_cast<size_t>(__shfl_sync(
                               0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
-                        : slot_index(p, wk, u, sl) * slot_elems;
+                        : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
                 ld_cg_v8(part + sbase + coff, x);
               }
 #pragma unroll
@@ -962,7 +1044,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sm.dempty);
+        if (lane == 0) {
+          if constexpr (PAIR) mbar_arrive_cluster(dempty_c);
+          else mbar_arrive(sm.dempty);
+        }
         first_chunk = false;
         if (split && !reducer) {
           // partial sums visible device-wide, then counted as written
@@ -977,60 +1062,95 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // a pair: neither CTA frees its tensor memory or exits while the other may
+  // still arrive on its barriers or the MMAs may read its shared memory
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   if (warp == kProdWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
 
 namespace {
-template <bool MMA2>
-cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
-                        const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
-  const void* fn;
-  if (plan.mode == kW4A16_F16)
-    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_F16, MMA2>);
-  else if (plan.mode == kW4A16_BF16)
-    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A16_BF16, MMA2>);
-  else if (plan.mode == kW4A8F8)
-    fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A8F8, MMA2>);
-  else fn = reinterpret_cast<const void*>(&tc_gemm_kernel<kW4A8, MMA2>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int MODE, bool MMA2, bool PAIR>
+cudaError_t launch_tc_mode(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                           const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  auto* fn = &tc_gemm_kernel<MODE, MMA2, PAIR>;
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem_bytes));
   if (e != cudaSuccess) return e;
-  const int threads = kTcThreads;
-  if (plan.mode == kW4A16_F16) {
-    tc_gemm_kernel<kW4A16_F16, MMA2>
-        <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
-    return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (MODE == kW4A8) {
+    // W4A8: a programmatic dependent of its int8 -> bf16 staging launch; only
+    // the activation producer waits for that grid (weights and scales are not
+    // written by it), so the weight stream starts at once
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
-  if (plan.mode == kW4A16_BF16) {
-    tc_gemm_kernel<kW4A16_BF16, MMA2>
-        <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
-    return cudaGetLastError();
+  if (PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
-  if (plan.mode == kW4A8F8) {
-    // fp8 activations are read by TMA straight from the caller's buffer
-    tc_gemm_kernel<kW4A8F8, MMA2>
-        <<<plan.grid, threads, plan.smem_bytes, s>>>(amap, smap, zmap, plan, args);
-    return cudaGetLastError();
-  }
-  // W4A8: a programmatic dependent of its int8 -> bf16 staging launch; only
-  // the activation producer waits for that grid (weights and scales are not
-  // written by it), so the weight stream starts at once
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
-  cfg.blockDim = dim3(threads);
+  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = s;
   cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, fn, amap, smap, zmap, plan, args);
+}
+
+// fp8 activations are read by TMA straight from the caller's buffer; W4A8
+// int8 from the workspace's bf16 copy; W4A16 from the caller's buffer.
+template <bool MMA2, bool PAIR = false>
+cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
+                        const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  switch (plan.mode) {
+    case kW4A16_F16: return launch_tc_mode<kW4A16_F16, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
+    case kW4A16_BF16: return launch_tc_mode<kW4A16_BF16, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
+    case kW4A8F8: return launch_tc_mode<kW4A8F8, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
+    default: return launch_tc_mode<kW4A8, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
+  }
+}
+
+// Most two-CTA clusters of the pair kernel of this mode that can be resident
+// at once with `smem` bytes of shared memory per CTA (-1 when unknown).
+template <int MODE>
+int tc_pair_clusters_mode(size_t smem) {
+  auto* fn = &tc_gemm_kernel<MODE, false, true>;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, &tc_gemm_kernel<kW4A8, MMA2>, amap, smap, zmap, plan, args);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return n;
 }
 }  // namespace
 

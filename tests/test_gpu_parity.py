@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp",
-       "tc128x2_sk", "tc128x2_dp", "tc128x2_kp"]
+       "tc128x2_sk", "tc128x2_dp", "tc128x2_kp", "tc256p_sk", "tc256p_dp"]
 DK = ["dk8_sk", "dk16_sk"]
 DS = ["ds8_sk", "ds16_sk", "ds32_sk"]
 GV = ["gv8_cl", "gv16_cl", "gv32_cl"]
@@ -57,6 +57,20 @@ def samples(M, N, count=384, seed=0):
     rows = np.concatenate([[0, M - 1, M // 2], tail_r, rng.integers(0, M, count)])
     cols = np.concatenate([[0, N - 1, min(127, N - 1)], tail_c, rng.integers(0, N, count)])
     return rows.astype(np.int64), cols.astype(np.int64)
+
+
+# --------------------------------------------------------------- CTA pairs ---
+@pytest.mark.parametrize("name", ["tc256p_sk", "tc256p_dp"])
+@pytest.mark.parametrize("M,N", [(256, 256), (100, 384), (300, 640)])
+def test_pair_w4a8_int32_exact(gpu_lib, name, M, N):
+    """Two CTAs of a cluster share each MMA: int32 accumulators bit-exact,
+    with a pair tile whose second CTA has no weight columns (N = 384, 640:
+    odd 128-column tile counts) or no activation rows (M = 100)."""
+    w4 = gpu_lib
+    e = w4synth.gen_w4a8(M, N, 1024, group_size=-1, seed=M + N)
+    acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
+    ref = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], None, -1, e["K"], e["N"])
+    assert np.array_equal(acc.numpy().astype(np.int64), ref)
 
 
 # ----------------------------------------------------------------- prepack ---
@@ -123,7 +137,8 @@ def test_w4a16_several_tiles(gpu_lib, name, zeros, dt):
 
 
 @pytest.mark.parametrize("M", [256, 1000])
-@pytest.mark.parametrize("name", ["tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp"])
+@pytest.mark.parametrize("name", ["tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp", "tc256p_sk",
+                                  "tc256p_dp"])
 def test_w4a16_f16_zero_points_large_m(gpu_lib, name, M):
     """fp16 activations with uint4 + pre-scaled zero-points on the wide
     tensor-core tiles (the large-M path), ragged N, several K groups."""
@@ -189,7 +204,7 @@ def test_ds_ragged(gpu_lib, name, M, N, K, gs, dt):
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("name", ["default", "ds8_sk", "ds16_sk", "ds32_sk", "dk16_sk", "tc16_sk",
-                                  "tc64_sk", "simt", "gv8_cl", "gv16_cl", "gv32_cl"])
+                                  "tc64_sk", "simt", "gv8_cl", "gv16_cl", "gv32_cl", "tc256p_sk"])
 def test_w4a16_power_of_two_scales_exact(gpu_lib, dt, name):
     # exact products and sums: the GPU output must equal the exact result
     # rounded once (to nearest even) to the output type.  The activations are
@@ -278,7 +293,7 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
                                   "tc128x2_kp", "tc256_kp", "tc256_sk", "tc256_dp", "dk8_sk",
                                   "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk", "gv8_cl", "gv16_cl",
-                                  "gv32_cl"])
+                                  "gv32_cl", "tc256p_sk", "tc256p_dp"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
@@ -328,7 +343,7 @@ def test_w4a8_qqq_per_channel(gpu_lib, M):
     assert_fp16_within_ulp(out[rows, cols], ref, f"qqq per-channel M={M}")
 
 
-@pytest.mark.parametrize("name", ["tc128x2_kp", "tc256_kp"])
+@pytest.mark.parametrize("name", ["tc128x2_kp", "tc256_kp", "tc256p_sk"])
 @pytest.mark.parametrize("M", [128, 1024])
 def test_w4a8_qqq_per_channel_split_k(gpu_lib, M, name):
     """Two weight tiles per CTA, K split so that no unit passes one exact
@@ -586,7 +601,7 @@ def test_quantize_feeds_w4a8(gpu_lib, M):
 
 BIAS_SCHEDULES = ["simt", "tc16_sk", "tc64_sk", "tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp",
                   "dk8_sk", "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk", "gv8_cl", "gv16_cl",
-                  "gv32_cl"]
+                  "gv32_cl", "tc256p_sk"]
 
 
 @pytest.mark.parametrize("name", BIAS_SCHEDULES)
@@ -678,7 +693,7 @@ def test_autotune_installs_the_fastest_schedule(gpu_lib):
 
 F8_SCHEDULES = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk",
                 "tc256_dp", "tc128x2_sk", "tc128x2_kp", "tc256_kp", "gv8_cl", "gv16_cl",
-                "gv32_cl"]
+                "gv32_cl", "tc256p_sk", "tc256p_dp"]
 
 
 def run_fp8(w4, e, schedule=-1, bias=None):
@@ -725,6 +740,56 @@ def test_w4a8_fp8_qqq_shape(gpu_lib, M):
     ref, absref = fp8_ref(sub)
     idx = np.searchsorted(ur, rows)
     assert_within(got[rows, cols], ref[idx, cols], absref[idx, cols], "f16", f"fp8 QQQ M={M}")
+
+
+# ----------------------------------------- stage slots reused many times ---
+# N=8192 and a long K give every CTA of a forced tensor-core schedule dozens
+# of pipeline stages, so each shared-memory stage slot is refilled many
+# times and each converter group waits on slots whose previous stage another
+# group converted (a wait that passed on the previous stage's phase would
+# convert stale bytes).
+
+SLOT_SCHEDULES = ["tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128x2_sk", "tc256_sk",
+                  "tc256p_sk"]
+SLOT_BM = {"tc16_sk": 16, "tc32_sk": 32, "tc64_sk": 64, "tc128_sk": 128, "tc128x2_sk": 128,
+           "tc256_sk": 256, "tc256p_sk": 256}
+
+
+@pytest.mark.parametrize("name", SLOT_SCHEDULES)
+def test_w4a8_int32_stage_slots_cycle(gpu_lib, name):
+    w4 = gpu_lib
+    M, N, K = SLOT_BM[name] - 3, 8192, 16384
+    e = w4synth.gen_w4a8(M, N, K, group_size=-1, seed=61)
+    acc = run_w4a8(w4, e, torch.int32, sched(w4, name)).numpy().astype(np.int64)
+    rows, cols = samples(M, N, count=256, seed=62)
+    ref = oracle.w4a8_elems(e["a"], e["w"], e["layout"], e["wtype"], None, -1, K, N, rows, cols)
+    assert np.array_equal(acc[rows, cols], ref), name
+
+
+@pytest.mark.parametrize("name", SLOT_SCHEDULES)
+def test_w4a8_fp8_stage_slots_cycle(gpu_lib, name):
+    w4 = gpu_lib
+    M, N, K = SLOT_BM[name] - 3, 8192, 16384
+    e = w4synth.gen_w4a8_fp8(M, N, K, seed=63)
+    got = run_fp8(w4, e, sched(w4, name))
+    ur = np.unique(np.array([0, M // 2, M - 1]))
+    sub = dict(e, a=e["a"][torch.from_numpy(ur)], M=len(ur),
+               s_tok=e["s_tok"][torch.from_numpy(ur)])
+    ref, absref = fp8_ref(sub)
+    assert_within(got[ur], ref, absref, "f16", f"fp8 slots {name}")
+
+
+@pytest.mark.parametrize("name", SLOT_SCHEDULES)
+def test_w4a16_stage_slots_cycle(gpu_lib, name):
+    w4 = gpu_lib
+    M, N, K = SLOT_BM[name] - 3, 8192, 16384
+    d = w4synth.gen_w4a16(M, N, K, act_dtype=torch.bfloat16, wtype=w4.UINT4,
+                          layout=w4.NK_EXLLAMA, group_size=128, zeros=True, seed=64)
+    got = run_w4a16(w4, d, sched(w4, name)).double().numpy()
+    rows, cols = samples(M, N, count=256, seed=65)
+    ref, absref = oracle.w4a16_elems(d["a"], d["w"], d["layout"], d["wtype"], d["s"], d["z"], 128,
+                                     K, N, rows, cols)
+    assert_within(got[rows, cols], ref, absref, "bf16", f"w4a16 slots {name}")
 
 
 def test_w4a8_fp8_rejections(gpu_lib):
