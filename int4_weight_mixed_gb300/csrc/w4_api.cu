@@ -54,6 +54,9 @@ const Schedule kSchedules[] = {
     // two CTAs of a cluster share each MMA (cta_group::2): 256 weight columns
     // x 256 activation rows per tile, 128 activation rows per CTA
     {"tc256p_sk", kEngineTc, 256, kStreamK, 1, 1},    {"tc256p_dp", kEngineTc, 256, kDataParallel, 1, 1},
+    // the same with 128 activation rows (64 per CTA): the accumulator is half
+    // as wide, so the W4A8 int32 running sum stays in tensor memory beside it
+    {"tc128p_sk", kEngineTc, 128, kStreamK, 1, 1},
 };
 constexpr int kNumSchedules = sizeof(kSchedules) / sizeof(kSchedules[0]);
 
@@ -440,12 +443,18 @@ int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs,
   // stream-K balances fewer than four waves of wide tiles; data-parallel beyond
   const int64_t tiles = ((M + bm - 1) / bm) * ((N + kTileN - 1) / kTileN);
   const bool dp = tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128;
-  for (int si = 1; si < kNumSchedules; ++si) {
-    const Schedule& sc = kSchedules[si];
-    if (sc.engine == kEngineTc && sc.bm == bm && (sc.decomp == kDataParallel) == dp &&
-        schedule_fits(si, mode, M, N, K, gs, has_sg))
-      return si;
-  }
+  // 256-row W4A8 tiles (int8 or fp8 activations) on CTA pairs: measured 2-5%
+  // faster (int8) and 25% (fp8) than one CTA per tile; W4A16 on single CTAs
+  // (within 1% either way)
+  const bool pair = bm == 256 && (mode == kW4A8 || mode == kW4A8F8);
+  for (int pass = 0; pass < 2; ++pass)
+    for (int si = 1; si < kNumSchedules; ++si) {
+      const Schedule& sc = kSchedules[si];
+      if (sc.engine == kEngineTc && sc.bm == bm && (sc.pair != 0) == pair &&
+          (pass == 1 || (sc.decomp == kDataParallel) == dp) &&
+          schedule_fits(si, mode, M, N, K, gs, has_sg))
+        return si;
+    }
   for (int si = 1; si < kNumSchedules; ++si)
     if (kSchedules[si].engine == kEngineTc && kSchedules[si].bm == bm &&
         schedule_fits(si, mode, M, N, K, gs, has_sg))

@@ -48,15 +48,35 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// With SLEEP, a waiting thread is suspended in hardware until the phase
+// completes or W4_WAIT_HINT_NS has passed (then the caller checks its abort
+// flag and the time limit and waits again) instead of returning to a polling
+// loop: in the tensor-core kernel the idle converter warps otherwise spend a
+// large share of an SM's issue slots polling, next to the warps doing the
+// work (all its waits sleep: measured 3% faster).  The decode and
+// quantization kernels poll (measured 0.5% slower with the hint).
+#ifndef W4_WAIT_HINT_NS
+#define W4_WAIT_HINT_NS 100000u  // 100 us
+#endif
+template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
+  if (SLEEP && W4_WAIT_HINT_NS != 0u)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(static_cast<uint32_t>(W4_WAIT_HINT_NS))
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
@@ -76,13 +96,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed.  Gives up when
 // *abort is set by another thread of the CTA, or after the time limit (then
 // it sets *abort and the status word).  Returns true on success.
+template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* status) {
   if (mbar_test_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_try_wait<SLEEP>(bar, parity)) return true;
+    if ((SLEEP && W4_WAIT_HINT_NS != 0u) || (it & 63u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > W4_WAIT_TIMEOUT_NS) {
         *abort = 1;
@@ -451,40 +472,16 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// Arrive (release, cluster scope) on an mbarrier given by its
-// shared::cluster address, which may lie in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// mbar_wait for a barrier that threads of the other CTA arrive on (acquire at
-// cluster scope); bounded the same way.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort, int* status) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > W4_WAIT_TIMEOUT_NS) {
-        *abort = 1;
-        if (status) atomicExch(status, 5 /* W4_ERR_TIMEOUT */);
-        return false;
-      }
-    }
-  }
+// Arrive on an mbarrier given by its shared::cluster address, which may lie
+// in the other CTA of the pair.  What the arrival publishes there is tensor
+// memory written with tcgen05.st (completed by tcgen05.wait::st and ordered by
+// tcgen05.fence::before_thread_sync before the arrival) and shared memory
+// filled by TMA (complete once the arriving thread observed its barrier), both
+// read by the other CTA's MMAs after tcgen05.fence::after_thread_sync; the
+// default (CTA-scope) release suffices for that, and the cluster-scope form
+// made the pair kernel 18-26% slower.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 // Tensor memory of a CTA pair: one warp of each of the two CTAs issues these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {

@@ -3,10 +3,15 @@
 // compiled apart from the other variants.
 #include "w4_tc_kernel.cuh"
 
+#ifndef W4_PAIR_MMA2
+#define W4_PAIR_MMA2 1  // two alternating MMA issuers in rank 0
+#endif
+
 namespace w4 {
 
 cudaError_t launch_tc_pair(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                            const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  if (W4_PAIR_MMA2) return launch_tc_t<true, true>(plan, amap, smap, zmap, args, s);
   return launch_tc_t<false, true>(plan, amap, smap, zmap, args, s);
 }
 

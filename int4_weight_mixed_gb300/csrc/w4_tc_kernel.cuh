@@ -281,7 +281,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int BK = F8 ? 128 : kStageK;
   constexpr uint32_t WB = F8 ? 8192u : 4096u;
   constexpr int CPB = BK / kChunkK;  // 32-K chunks per block
-  static_assert(!(PAIR && MMA2), "a CTA pair has one MMA issuer");
   constexpr int NCTA = PAIR ? 2 : 1;
   if constexpr (PAIR) {
     // launched without its two-CTA clusters: nothing may run
@@ -418,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int gcur = u.kb0 * NS / sub_per_group;
         int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-          if (!mbar_wait(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
+          if (!mbar_wait<true>(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
           const int k64_0 = kb * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
           const uint32_t fb = full0 + s * 8;
@@ -463,7 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t issued = it;
       for (uint32_t j = (issued > static_cast<uint32_t>(S) ? issued - S : 0); j < issued; ++j) {
         volatile int no_abort = 0;
-        mbar_wait(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
+        mbar_wait<true>(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
       }
     }
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
@@ -482,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // a pair's MMAs are issued by rank 0: wait for their last commit, so
       // that this CTA's tensor and shared memory outlive them
       volatile int no_abort = 0;
-      mbar_wait(sm.fin, 0, &no_abort, args.status);
+      mbar_wait<true>(sm.fin, 0, &no_abort, args.status);
     } else if (lane == 0 && warp == kMmaWarp) {
       const uint32_t idesc = idesc_f16_m(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u,
                                          static_cast<uint32_t>(BM), PAIR ? 256u : 128u);
@@ -491,10 +490,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0;
       bool ok = true;
       Unit u;
-      // barriers the other CTA of a pair arrives on are read at cluster scope
       auto wait_x = [&](uint64_t* bar, uint32_t par) {
-        if constexpr (PAIR) return mbar_wait_cluster(bar, par, abort, args.status);
-        else return mbar_wait(bar, par, abort, args.status);
+        return mbar_wait<true>(bar, par, abort, args.status);
       };
       auto commit = [&](uint64_t* bar) {
         if constexpr (PAIR) mma_commit_pair(bar);
@@ -580,13 +577,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               else mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
             }
           } else if constexpr (PAIR) {
-            // one stage of one 64-K block (the pair kernel has NS = NT = 1)
+            // a stage of one K block (NS = 1, or the last, one-block stage of
+            // NS = 2; the pair kernel has NT = 1)
             uint32_t a4[4];
             uint64_t b4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              a4[i] = tmem + p.acol + ts * 32 + 8 * i;
-              b4[i] = desc0 + s * sub16 + 2 * i;
+              a4[i] = tmem + p.acol + ts * NS * 32 + 8 * i;
+              b4[i] = desc0 + s * NS * sub16 + 2 * i;
             }
             mma_pair_4<F8>(tmem, a4, b4, idesc, chunk_start ? 0u : 1u);
           } else {
@@ -625,13 +623,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // All issued MMAs complete before tensor memory is released.
       commit(sm.fin);
       volatile int no_abort = 0;
-      mbar_wait(sm.fin, 0, &no_abort, args.status);
+      mbar_wait<true>(sm.fin, 0, &no_abort, args.status);
     }
     } else {
-    if (lane == 0) {
+    if (lane == 0 && rank != 0) {
+      // a pair's MMAs are issued by rank 0: wait for their last commits
+      if (warp == kMmaWarp) {
+        volatile int no_abort = 0;
+        mbar_wait<true>(sm.fin, 0, &no_abort, args.status);
+      }
+    } else if (lane == 0) {
       const uint32_t me = warp == kMmaWarp ? 0u : 1u;  // issues the groups g with g % 2 == me
-      const uint32_t idesc =
-          idesc_f16(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u, static_cast<uint32_t>(BM));
+      const uint32_t idesc = idesc_f16_m(MODE == kW4A16_BF16 || MODE == kW4A8 ? 1u : 0u,
+                                         static_cast<uint32_t>(BM), PAIR ? 256u : 128u);
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (PAIR) mma_commit_pair(bar);
+        else mma_commit(bar);
+      };
       const uint64_t desc0 = sw128_kmajor_desc(smem_addr(sm.a));
       const uint32_t sub16 = a_sub / 16;  // descriptor address units per activation tile
       uint32_t s = 0, ph = 0, ts = 0, tph = 0, ev = 0, g = 0, tok_ph = 0;
@@ -661,13 +669,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int used = pair ? 2 : 1;
           const bool chunk_end = left == used;
           if ((g & 1u) == me) {
-            if (chunk_start && ev > 0 && !mbar_wait(sm.dempty, (ev - 1) & 1, abort, args.status)) {
+            if (chunk_start && ev > 0 && !mbar_wait<true>(sm.dempty, (ev - 1) & 1, abort, args.status)) {
               ok = false;
               break;
             }
             // The converter group arrives on tfull only after it observed the
             // stage's full barrier, so tfull also orders the activation tile.
-            if (!mbar_wait(&sm.tfull[ts], tph, abort, args.status)) {
+            if (!mbar_wait<true>(&sm.tfull[ts], tph, abort, args.status)) {
               ok = false;
               break;
             }
@@ -678,14 +686,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               ts2 = 0;
               tph2 ^= 1;
             }
-            if (pair && !mbar_wait(&sm.tfull[ts2], tph2, abort, args.status)) {
+            if (pair && !mbar_wait<true>(&sm.tfull[ts2], tph2, abort, args.status)) {
               ok = false;
               break;
             }
             // the other thread has issued the previous group (waited last,
             // so that the pipe changes hands with the least delay)
             if (g > 0) {
-              if (!mbar_wait(&sm.tok[me], tok_ph, abort, args.status)) {
+              if (!mbar_wait<true>(&sm.tok[me], tok_ph, abort, args.status)) {
                 ok = false;
                 break;
               }
@@ -708,7 +716,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   b8[i] = desc0 + s1 * 2 * sub16 + half * sub16 + 2 * kk;
                 }
               }
-              mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              if constexpr (PAIR) mma_pair_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+              else mma_ts_8<F8>(tmem, a8, b8, idesc, chunk_start ? 0u : 1u);
+            } else if constexpr (PAIR) {
+              // a stage of one K block (NS = 1, or the last, one-block stage
+              // of NS = 2; the pair kernel has NT = 1)
+              uint32_t a4[4];
+              uint64_t b4[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                a4[i] = tmem + p.acol + ts * NS * 32 + 8 * i;
+                b4[i] = desc0 + s * NS * sub16 + 2 * i;
+              }
+              mma_pair_4<F8>(tmem, a4, b4, idesc, chunk_start ? 0u : 1u);
             } else {
               const int k64_0 = (u.kb0 + j) * NS;
               const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
@@ -729,9 +749,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // this thread's own MMAs)
             tc_fence_before();
             mbar_arrive(&sm.tok[me ^ 1u]);
-            mma_commit(&sm.empty[s1]);
-            if (pair) mma_commit(&sm.empty[s2]);
-            if (chunk_end) mma_commit(sm.dfull);
+            commit(&sm.empty[s1]);
+            if (pair) commit(&sm.empty[s2]);
+            if (chunk_end) commit(sm.dfull);
             issued = true;
           }
           advance();
@@ -746,11 +766,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // All issued MMAs complete before tensor memory is released (a thread
-      // that issued none arrives directly).
-      if (issued) mma_commit(sm.fin);
+      // that issued none arrives directly; in a pair it commits all the
+      // same, which reaches both CTAs' barriers at once).
+      if (PAIR || issued) commit(sm.fin);
       else mbar_arrive(sm.fin);
       volatile int no_abort = 0;
-      mbar_wait(sm.fin, 0, &no_abort, args.status);
+      mbar_wait<true>(sm.fin, 0, &no_abort, args.status);
     }
     }
   }
@@ -820,12 +841,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // is unambiguous for S >= kConvGroups: this group's previous slot
           // wait (stage it-kConvGroups-TS) already covers stage it-TS-S.
           if (it >= static_cast<uint32_t>(TS)) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.empty[ps], pph, abort, args.status))) {
+            if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.empty[ps], pph, abort, args.status))) {
               ok = false;
               break;
             }
           }
-          if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], cph, abort, args.status))) {
+          if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.full[s], cph, abort, args.status))) {
             ok = false;
             break;
           }
@@ -894,7 +915,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // empty first: once the MMA thread sees tfull, this group's share
             // of the stage's release has been counted
             mbar_arrive(&sm.empty[s]);
-            if constexpr (PAIR) mbar_arrive_cluster(tfull_c + ts * 8);
+            if constexpr (PAIR) mbar_arrive_remote(tfull_c + ts * 8);
             else mbar_arrive(&sm.tfull[ts]);
           }
         }
@@ -944,7 +965,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(sm.dfull, ev & 1, abort, args.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait<true>(sm.dfull, ev & 1, abort, args.status))) {
           ok = false;
           break;
         }
@@ -1045,7 +1066,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) mbar_arrive_cluster(dempty_c);
+          if constexpr (PAIR) mbar_arrive_remote(dempty_c);
           else mbar_arrive(sm.dempty);
         }
         first_chunk = false;

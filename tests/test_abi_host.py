@@ -52,7 +52,9 @@ def test_default_heuristic(lib):
     assert name(16, 4096, 4096, torch.bfloat16, 64) == "tc16_sk"   # group 64 splits a K block
     assert name(32, 8192, 21760, torch.int8, -1) == "ds32_sk"
     assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
-    assert name(1024, 8192, 21760, torch.int8, -1) == "tc256_sk"  # 256 tiles < 4 waves
+    # W4A8 at 256-row tiles on CTA pairs (stream-K: 256 tiles < 4 waves); W4A16 on single CTAs
+    assert name(1024, 8192, 21760, torch.int8, -1) == "tc256p_sk"
+    assert name(1024, 8192, 21760, torch.bfloat16, 128) == "tc256_sk"
     assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"
     assert name(4, 13, 512, torch.float16, 128) == "dk8_sk"  # any N (streamed needs N % 8 == 0)
     assert name(20, 13, 512, torch.float16, 128) == "simt"  # N % 8 != 0 beyond 16 rows

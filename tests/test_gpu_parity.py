@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 ALL = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk", "tc256_dp",
-       "tc128x2_sk", "tc128x2_dp", "tc128x2_kp", "tc256p_sk", "tc256p_dp"]
+       "tc128x2_sk", "tc128x2_dp", "tc128x2_kp", "tc256p_sk", "tc256p_dp", "tc128p_sk"]
 DK = ["dk8_sk", "dk16_sk"]
 DS = ["ds8_sk", "ds16_sk", "ds32_sk"]
 GV = ["gv8_cl", "gv16_cl", "gv32_cl"]
@@ -60,7 +60,7 @@ def samples(M, N, count=384, seed=0):
 
 
 # --------------------------------------------------------------- CTA pairs ---
-@pytest.mark.parametrize("name", ["tc256p_sk", "tc256p_dp"])
+@pytest.mark.parametrize("name", ["tc256p_sk", "tc256p_dp", "tc128p_sk"])
 @pytest.mark.parametrize("M,N", [(256, 256), (100, 384), (300, 640)])
 def test_pair_w4a8_int32_exact(gpu_lib, name, M, N):
     """Two CTAs of a cluster share each MMA: int32 accumulators bit-exact,
@@ -293,7 +293,7 @@ def run_w4a8(w4, e, out_dtype, schedule=-1):
 @pytest.mark.parametrize("name", ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp",
                                   "tc128x2_kp", "tc256_kp", "tc256_sk", "tc256_dp", "dk8_sk",
                                   "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk", "gv8_cl", "gv16_cl",
-                                  "gv32_cl", "tc256p_sk", "tc256p_dp"])
+                                  "gv32_cl", "tc256p_sk", "tc256p_dp", "tc128p_sk"])
 @pytest.mark.parametrize("gs", [-1, 128])
 def test_w4a8_int32_bit_exact(gpu_lib, name, gs):
     w4 = gpu_lib
@@ -343,7 +343,7 @@ def test_w4a8_qqq_per_channel(gpu_lib, M):
     assert_fp16_within_ulp(out[rows, cols], ref, f"qqq per-channel M={M}")
 
 
-@pytest.mark.parametrize("name", ["tc128x2_kp", "tc256_kp", "tc256p_sk"])
+@pytest.mark.parametrize("name", ["tc128x2_kp", "tc256_kp", "tc256p_sk", "tc128p_sk"])
 @pytest.mark.parametrize("M", [128, 1024])
 def test_w4a8_qqq_per_channel_split_k(gpu_lib, M, name):
     """Two weight tiles per CTA, K split so that no unit passes one exact
@@ -523,7 +523,7 @@ def _assert_quant_equal(q, s, rq, rs, what):
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("M,K", [(1, 21760), (16, 21760), (37, 4096), (5, 72), (3, 13), (2, 8),
                                  (0, 64), (4, 0), (1024, 21760), (3, 65536), (2, 65600),
-                                 (7, 2048)])
+                                 (7, 2048), (2000, 4096), (400, 8)])
 def test_quantize_per_token_bit_exact(gpu_lib, M, K, dt):
     w4 = gpu_lib
     a = w4synth.gen_act16(M, K, dt, seed=M + K)
@@ -693,7 +693,7 @@ def test_autotune_installs_the_fastest_schedule(gpu_lib):
 
 F8_SCHEDULES = ["simt", "tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128_dp", "tc256_sk",
                 "tc256_dp", "tc128x2_sk", "tc128x2_kp", "tc256_kp", "gv8_cl", "gv16_cl",
-                "gv32_cl", "tc256p_sk", "tc256p_dp"]
+                "gv32_cl", "tc256p_sk", "tc256p_dp", "tc128p_sk"]
 
 
 def run_fp8(w4, e, schedule=-1, bias=None):
@@ -750,9 +750,9 @@ def test_w4a8_fp8_qqq_shape(gpu_lib, M):
 # convert stale bytes).
 
 SLOT_SCHEDULES = ["tc16_sk", "tc32_sk", "tc64_sk", "tc128_sk", "tc128x2_sk", "tc256_sk",
-                  "tc256p_sk"]
+                  "tc256p_sk", "tc128p_sk"]
 SLOT_BM = {"tc16_sk": 16, "tc32_sk": 32, "tc64_sk": 64, "tc128_sk": 128, "tc128x2_sk": 128,
-           "tc256_sk": 256, "tc256p_sk": 256}
+           "tc256_sk": 256, "tc256p_sk": 256, "tc128p_sk": 128}
 
 
 @pytest.mark.parametrize("name", SLOT_SCHEDULES)
@@ -815,7 +815,8 @@ def test_w4a8_fp8_rejections(gpu_lib):
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("M,K", [(1, 21760), (16, 21760), (37, 4096), (5, 72), (3, 13),
-                                 (1024, 21760), (2, 40000), (3, 65536), (2, 65600)])
+                                 (1024, 21760), (2, 40000), (3, 65536), (2, 65600),
+                                 (2000, 4096)])
 def test_quantize_per_token_fp8_bit_exact(gpu_lib, M, K, dt):
     w4 = gpu_lib
     a = w4synth.gen_act16(M, K, dt, seed=M + 3 * K)
