@@ -652,7 +652,9 @@ def run_gpu(args):
     dom = max(M_SWEEP, key=lambda M: per_m[M])
     dom_us = per_m[dom]
     dom_ent = next(e for e in sweep if e["M"] == dom)
-    kname = ("tc_gemm_kernel<W4A8> (+ its int8->bf16 staging launch)"
+    pair = dom_ent["schedule"].startswith("tc") and "p_" in dom_ent["schedule"]
+    kname = (f"tc_gemm_kernel<W4A8{', CTA pairs' if pair else ''}> ({dom_ent['schedule']}, "
+             "+ its int8->bf16 staging launch)"
              if dom_ent["schedule"].startswith("tc") else f"{dom_ent['schedule']} launches")
     if dom_ent["bound"] == "tensor":
         roofline = {"kernel": kname, "M": dom, "bound": "tensor",
@@ -664,7 +666,8 @@ def run_gpu(args):
         roofline = {"kernel": kname, "M": dom, "bound": "hbm",
                     "achieved": round(algo_bytes(dom) / (dom_us * 1e-6) / 1e9, 1),
                     "peak": pk["hbm"], "unit": "GB/s", "peak_source": f"{pk['src']} HBM copy"}
-    roofline["traffic"] = measured_traffic("tc_gemm_kernel<W4A8>", dom)
+    roofline["traffic"] = measured_traffic(
+        "tc_gemm_kernel<W4A8, CTA pairs>" if pair else "tc_gemm_kernel<W4A8>", dom)
     roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 3)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
