@@ -47,14 +47,39 @@ __device__ __forceinline__ float one_f32<__nv_bfloat16>(__nv_bfloat16 x) {
   return __bfloat162float(x);
 }
 
-// Largest |x| of the eight 16-bit values in v.
+// Running maximum of |x| over pairs of 16-bit values, kept packed: the
+// maximum is exact in the input type, so it is taken there (one instruction
+// per pair) and converted to fp32 once per thread.
 template <typename T>
-__device__ __forceinline__ float max8(const uint4& v) {
-  const float2 a = pair_f32<T>(v.x), b = pair_f32<T>(v.y), c = pair_f32<T>(v.z),
-               d = pair_f32<T>(v.w);
-  const float m0 = fmaxf(fabsf(a.x), fabsf(a.y)), m1 = fmaxf(fabsf(b.x), fabsf(b.y));
-  const float m2 = fmaxf(fabsf(c.x), fabsf(c.y)), m3 = fmaxf(fabsf(d.x), fabsf(d.y));
-  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+struct Pair16;
+template <>
+struct Pair16<__half> {
+  using P = __half2;
+  static __device__ __forceinline__ P zero() { return __float2half2_rn(0.f); }
+  static __device__ __forceinline__ P amax(P m, uint32_t v) {
+    return __hmax2(m, __habs2(*reinterpret_cast<const __half2*>(&v)));
+  }
+  static __device__ __forceinline__ float to_f32(P m) {
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+};
+template <>
+struct Pair16<__nv_bfloat16> {
+  using P = __nv_bfloat162;
+  static __device__ __forceinline__ P zero() { return __float2bfloat162_rn(0.f); }
+  static __device__ __forceinline__ P amax(P m, uint32_t v) {
+    return __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&v)));
+  }
+  static __device__ __forceinline__ float to_f32(P m) {
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+};
+template <typename T>
+__device__ __forceinline__ typename Pair16<T>::P amax8(typename Pair16<T>::P m, const uint4& v) {
+  m = Pair16<T>::amax(m, v.x);
+  m = Pair16<T>::amax(m, v.y);
+  m = Pair16<T>::amax(m, v.z);
+  return Pair16<T>::amax(m, v.w);
 }
 
 // ---------------------------------------------------------------------------
@@ -81,24 +106,31 @@ __device__ __forceinline__ float code_s8_fast(float x, float s, float r, bool fa
 }
 
 // The eight int8 codes of f[] (|f| <= amax, so every code is within
-// [-127, 127]) as integers, rounded to nearest even: from the products with
-// r, and, in a branch taken only when some product lies within 2^-15 of a
-// half-integer (or r is not finite), from the exact quotients for those.
+// [-127, 127]), rounded to nearest even, as t[e] = code + 1.5 * 2^23: adding
+// that constant to a value of magnitude below 2^22 rounds it to an integer
+// (nearest even, the FADD's own rounding) held in the low mantissa bits, so
+// the low byte of t's bit pattern is the two's-complement code and t - 1.5 *
+// 2^23 its exact value.  Codes come from the products p with r; a product
+// whose distance to the nearest integer is 0.5 - 2^-15 or more (within
+// 2^-15 of a half-integer), or any product when r is not finite, is replaced
+// by the code of the exact quotient, in a branch taken for few vectors.
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
 __device__ __forceinline__ void codes8_s8(const float (&f)[8], float s, float r, bool fast,
-                                          int (&c)[8]) {
-  bool redo = !fast;
+                                          float (&t)[8]) {
+  // explicitly rounded operations: none may be fused or reassociated
+  float dmax = 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const float p = f[e] * r;
-    c[e] = __float2int_rn(p);
-    redo |= fabsf(fabsf(p - truncf(p)) - 0.5f) <= 0x1p-15f;
+    const float p = __fmul_rn(f[e], r);
+    t[e] = __fadd_rn(p, kRoundMagic);
+    dmax = fmaxf(dmax, fabsf(__fsub_rn(p, __fsub_rn(t[e], kRoundMagic))));
   }
-  if (redo) {
+  if (!fast || dmax >= 0.5f - 0x1p-15f) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float p = f[e] * r;
-      if (!fast || fabsf(fabsf(p - truncf(p)) - 0.5f) <= 0x1p-15f)
-        c[e] = __float2int_rn(__fdiv_rn(f[e], s));
+      const float p = __fmul_rn(f[e], r);
+      if (!fast || fabsf(__fsub_rn(p, __fsub_rn(t[e], kRoundMagic))) >= 0.5f - 0x1p-15f)
+        t[e] = __fadd_rn(__fdiv_rn(f[e], s), kRoundMagic);
     }
   }
 }
@@ -137,8 +169,10 @@ __global__ void __launch_bounds__(kQuantThreads)
   if (vec) {
     const uint4* r8 = reinterpret_cast<const uint4*>(row);
     const int64_t n8 = K >> 3;
+    typename Pair16<T>::P m2 = Pair16<T>::zero();
 #pragma unroll 4
-    for (int64_t i = threadIdx.x; i < n8; i += kQuantThreads) amax = fmaxf(amax, max8<T>(__ldg(r8 + i)));
+    for (int64_t i = threadIdx.x; i < n8; i += kQuantThreads) m2 = amax8<T>(m2, __ldg(r8 + i));
+    amax = Pair16<T>::to_f32(m2);
   } else {
     for (int64_t k = threadIdx.x; k < K; k += kQuantThreads) amax = fmaxf(amax, fabsf(one_f32(row[k])));
   }
@@ -178,21 +212,26 @@ __global__ void __launch_bounds__(kQuantThreads)
           o[e >> 2] |= (live ? code_e4m3(f[e], s) : 0u) << (8 * (e & 3));
         reinterpret_cast<uint2*>(static_cast<uint8_t*>(q) + m * K)[i] = make_uint2(o[0], o[1]);
       } else {
-        int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (live) codes8_s8(f, s, r, fast, c);
+        float t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = kRoundMagic;  // code 0
+        if (live) codes8_s8(f, s, r, fast, t);
         if constexpr (OUT == kOutBf16) {
           uint32_t o[4];
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(static_cast<float>(c[2 * pp]),
-                                                            static_cast<float>(c[2 * pp + 1]));
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fsub_rn(t[2 * pp], kRoundMagic),
+                                                            __fsub_rn(t[2 * pp + 1], kRoundMagic));
             o[pp] = *reinterpret_cast<const uint32_t*>(&b2);  // exact
           }
           reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(q) + m * K)[i] =
               make_uint4(o[0], o[1], o[2], o[3]);
         } else {
-          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + m * K)[i] =
-              make_uint2(pack4_s8(c[0], c[1], c[2], c[3]), pack4_s8(c[4], c[5], c[6], c[7]));
+          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + m * K)[i] = make_uint2(
+              pack4_s8(__float_as_int(t[0]), __float_as_int(t[1]), __float_as_int(t[2]),
+                       __float_as_int(t[3])),
+              pack4_s8(__float_as_int(t[4]), __float_as_int(t[5]), __float_as_int(t[6]),
+                       __float_as_int(t[7])));
         }
       }
     }
