@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&sm.full[i], 2);  // weight producer + activation producer
+      mbar_init(&sm.full[i], 1);  // the producer thread of the stage's parity
       mbar_init(&sm.empty[i], 4 + 1);  // one converter group + the MMA commit
     }
     // tfull / dempty: the converter warps of both CTAs of a pair arrive on
@@ -382,16 +382,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcOtherRegs));
   if (warp == kProdWarp || warp == kActWarp) {
     // ----------------------------------------------------------- producers
-    // Two single-thread producers fill each stage in parallel, each with its
-    // own expect-tx on the stage's full barrier: the weight producer the bulk
-    // copy of the stage's nibbles and the scale / zero-point boxes, the
-    // activation producer the activation tile(s).
+    // Two single-thread producers take alternate stages; for each of its
+    // stages a producer issues the bulk copy of the stage's nibbles, the
+    // scale / zero-point boxes and the activation tile(s), with one expect-tx
+    // on the stage's full barrier.
     if (lane == 0) {
       const bool wprod = warp == kProdWarp;
       // W4A8: the activations come from the staging grid this one may have
       // been launched beside (programmatic dependent launch); wait for it
-      if (!wprod) asm volatile("griddepcontrol.wait;" ::: "memory");
-      uint32_t it = 0, s = 0, ph = 0;
+      // Each of the two threads issues every copy of alternate stages (stage
+      // it goes to the thread with it % 2 == pid), stepping two stages at a
+      // time: one thread issuing the weights of every stage was the stage
+      // rate's limit (its dependent instruction chain per stage, on a
+      // sub-partition shared with four converter warps, took as long as the
+      // stage's MMAs).
+      const uint32_t pid = wprod ? 0u : 1u;
+      bool waited = false;  // W4A8: the staging grid this one may overlap
+      uint32_t n_issued = 0, last_it = 0;  // stages this thread issued, the last one
+      uint32_t it_u = 0;    // stage index of the unit's first stage
       bool ok = true;
       Unit u;
       const uint32_t a0 = smem_addr(sm.a), w0 = smem_addr(sm.w);
@@ -408,62 +416,81 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int ntv = p.n128 - wt0;                     // weight tiles that exist (ragged N)
         if (ntv > NT) ntv = NT;
         if (ntv < 0) ntv = 0;
+        const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
+        // this thread's first stage of the unit, and its ring slot / phase
+        const int kbf = u.kb0 + static_cast<int>((pid + 2u - (it_u & 1u)) & 1u);
+        uint32_t it = it_u + static_cast<uint32_t>(kbf - u.kb0);
+        uint32_t s = it % S, ph = (it / S) & 1u;
         const uint8_t* wsrc =
             args.b_packed +
-            ((static_cast<int64_t>(wt0) * (K / kChunkK) + static_cast<int64_t>(u.kb0) * NS * CPB) *
+            ((static_cast<int64_t>(wt0) * (K / kChunkK) + static_cast<int64_t>(kbf) * NS * CPB) *
              kTileN) * 16;
-        const int64_t tile_stride = (K / kChunkK) * kTileN * 16;  // bytes between weight tiles
         // scale group of the stage, kept without division per stage
-        int gcur = u.kb0 * NS / sub_per_group;
-        int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
-        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+        int gcur = kbf * NS / sub_per_group;
+        int gleft = sub_per_group - (kbf * NS) % sub_per_group;
+        for (int kb = kbf; kb < u.kb1; kb += 2, it += 2) {
           if (!mbar_wait<true>(&sm.empty[s], ph ^ 1, abort, args.status)) { ok = false; break; }
           const int k64_0 = kb * NS;
           const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;  // valid 64-K blocks
           const uint32_t fb = full0 + s * 8;
-          if (wprod) {
-            mbar_arrive_expect_tx_a(fb, ntv * nv * WB + NT * (sc_bytes + zp_bytes));
-            for (int t = 0; t < ntv; ++t)
-              bulk_g2s_a(w0 + (s * NT + t) * NS * WB, wsrc + t * tile_stride, nv * WB, fb);
-            if (sc_bytes || zp_bytes) {
-              const int g0 = gcur;
-              for (int t = 0; t < NT; ++t) {
-                if (sc_bytes)
-                  tma_load_2d_a(s0 + (s * NT + t) * NS * 256, &smap, n0 + t * kTileN, g0, fb);
-                if (zp_bytes)
-                  tma_load_2d_a(z0 + (s * NT + t) * NS * 256, &zmap, n0 + t * kTileN, g0, fb);
-              }
+          const uint32_t abytes = p.a3d ? NS * a_sub : nv * a_sub;
+          mbar_arrive_expect_tx_a(fb, ntv * nv * WB + NT * (sc_bytes + zp_bytes) + abytes);
+          for (int t = 0; t < ntv; ++t)
+            bulk_g2s_a(w0 + (s * NT + t) * NS * WB, wsrc + t * tile_stride, nv * WB, fb);
+          if (sc_bytes || zp_bytes) {
+            const int g0 = gcur;
+            for (int t = 0; t < NT; ++t) {
+              if (sc_bytes)
+                tma_load_2d_a(s0 + (s * NT + t) * NS * 256, &smap, n0 + t * kTileN, g0, fb);
+              if (zp_bytes)
+                tma_load_2d_a(z0 + (s * NT + t) * NS * 256, &zmap, n0 + t * kTileN, g0, fb);
             }
-            wsrc += NS * WB;
-          } else if (p.a3d) {
-            mbar_arrive_expect_tx_a(fb, NS * a_sub);
+          }
+          // W4A8: the activations come from the staging grid this one may
+          // have been launched beside (programmatic dependent launch); the
+          // weights of the first stage are already on their way
+          if (!waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            waited = true;
+          }
+          if (p.a3d) {
             tma_load_3d_a(a0 + s * NS * a_sub, &amap, 0, y, k64_0, fb);
           } else {
-            mbar_arrive_expect_tx_a(fb, nv * a_sub);
             for (int j = 0; j < nv; ++j)
               tma_load_2d_a(a0 + (s * NS + j) * a_sub, &amap, (k64_0 + j) * BK, y, fb);
           }
+          ++n_issued;
+          last_it = it;
+          wsrc += 2 * NS * WB;
           if (stage_in_group) {
-            gleft -= NS;
-            if (gleft == 0) {
+            gleft -= 2 * NS;
+            while (gleft <= 0) {
               ++gcur;
-              gleft = sub_per_group;
+              gleft += sub_per_group;
             }
           } else {
-            gcur += p.gps;
+            gcur += 2 * p.gps;
           }
-          if (++s == static_cast<uint32_t>(S)) {
-            s = 0;
+          s += 2;
+          if (s >= static_cast<uint32_t>(S)) {
+            s -= S;
             ph ^= 1;
           }
         }
+        it_u += static_cast<uint32_t>(u.kb1 - u.kb0);
       }
-      // Let every copy issued land before the CTA can exit.
-      const uint32_t issued = it;
-      for (uint32_t j = (issued > static_cast<uint32_t>(S) ? issued - S : 0); j < issued; ++j) {
-        volatile int no_abort = 0;
-        mbar_wait<true>(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
-      }
+      // Let every copy this thread issued land before the CTA can exit: its
+      // stages among the last S of the whole sequence, the final users of
+      // their slots (an earlier stage's slot may have been refilled, and with
+      // an odd S by the other thread, so a parity wait on it would be
+      // ambiguous).  After an abort: its own last S stages.
+      const uint32_t end = ok ? it_u : last_it + 1;
+      if (n_issued > 0)
+        for (uint32_t j = (end > static_cast<uint32_t>(S) ? end - S : 0); j < end; ++j) {
+          if ((j & 1u) != pid || j > last_it) continue;
+          volatile int no_abort = 0;
+          mbar_wait<true>(&sm.full[j % S], (j / S) & 1, &no_abort, args.status);
+        }
     }
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     // ----------------------------------------------------------------- MMA
