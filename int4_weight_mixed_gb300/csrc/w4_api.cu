@@ -384,13 +384,13 @@ struct Override {
   int64_t m_lo, m_hi, N, K, gs;
   int schedule;
 };
-const char* const kBuiltinOverrideNames[] = {"tc256_sk", "tc256_sk"};
+const char* const kBuiltinOverrideNames[] = {"tc256p_dp", "tc256p_dp"};
 const Override kBuiltinOverrides[] = {
-    // W4A16 bf16, Llama-3-70B MLP down projection (N=8192, K=28672):
-    // tc256_sk 1619 us vs tc256_dp 1674 us at M=4096, 3296 vs 3316 at 8192
+    // W4A16 bf16, Llama-3-70B MLP down projection (N=8192, K=28672), M=4096:
+    // tc256p_dp 1252 us, tc256p_sk 1349, tc256_sk 1598
     {kW4A16_BF16, 4096, 8192, 8192, 28672, 128, -1},
-    // W4A16 bf16, Llama-3-70B MLP gate/up (N=57344, K=8192):
-    // tc256_sk 3447.5 vs 3448.4 us at M=4096, 6815.6 vs 6820.9 at 8192
+    // W4A16 bf16, Llama-3-70B MLP gate/up (N=57344, K=8192), M=4096:
+    // tc256p_dp 2585 us, tc256p_sk 2594, tc256_sk 3341
     {kW4A16_BF16, 4096, 8192, 57344, 8192, 128, -1},
 };
 constexpr int kMaxOverrides = 256;
@@ -443,10 +443,11 @@ int default_schedule_impl(int mode, int64_t M, int64_t N, int64_t K, int64_t gs,
   // stream-K balances fewer than four waves of wide tiles; data-parallel beyond
   const int64_t tiles = ((M + bm - 1) / bm) * ((N + kTileN - 1) / kTileN);
   const bool dp = tiles >= 4 * static_cast<int64_t>(sm_count()) && bm >= 128;
-  // 256-row W4A8 tiles (int8 or fp8 activations) on CTA pairs: measured 2-5%
-  // faster (int8) and 25% (fp8) than one CTA per tile; W4A16 on single CTAs
-  // (within 1% either way)
-  const bool pair = bm == 256 && (mode == kW4A8 || mode == kW4A8F8);
+  // 256-row tiles on CTA pairs (W4A8 N=8192 K=21760 M=1024: 241 us against
+  // 406 for 128-row single-CTA tiles; fp8 M=1024 153 against 221 for
+  // single-CTA 256-row tiles; W4A16 prefill 20-23% faster), and 128-row W4A8
+  // tiles (M=128: 66.2 against 67.6 us)
+  const bool pair = bm == 256 || (bm == 128 && mode == kW4A8);
   for (int pass = 0; pass < 2; ++pass)
     for (int si = 1; si < kNumSchedules; ++si) {
       const Schedule& sc = kSchedules[si];

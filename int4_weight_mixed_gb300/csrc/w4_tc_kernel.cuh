@@ -51,6 +51,12 @@
 #include "w4_internal.h"
 #include "w4_ptx.cuh"
 
+// Converter warpgroups at kTcConvRegs registers and the fifth warpgroup at
+// kTcOtherRegs (setmaxnreg at kernel start), or the launch's even split.
+#ifndef W4_TC_REGSPLIT
+#define W4_TC_REGSPLIT (PAIR || (MODE != kW4A8 && !MMA2))
+#endif
+
 namespace w4 {
 
 namespace {
@@ -290,6 +296,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  // converter groups visit only their own stages (see the converter loop)
+  constexpr bool kOwnStages = PAIR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // W4A16 with one MMA issuer: the fifth warpgroup (producers, MMA) gives
   // registers to the converters, whose scale / zero-point FMAs otherwise
   // spill (the other kernels keep the even split: measured faster)
-  if constexpr (MODE != kW4A8 && !MMA2)
+  if constexpr (W4_TC_REGSPLIT)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcOtherRegs));
   if (warp == kProdWarp || warp == kActWarp) {
     // ----------------------------------------------------------- producers
@@ -803,7 +811,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   } else {
-    if constexpr (MODE != kW4A8 && !MMA2)
+    if constexpr (W4_TC_REGSPLIT)
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcConvRegs));
     // ----------------------------------------------- converters + epilogue
     const int cw = warp;               // converter warp index 0..kConvWarps-1
@@ -812,21 +820,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = q * 32 + lane;       // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int nblk = BM / 8;           // 8-column blocks of the accumulator
-    uint32_t it = 0, ev = 0;
-    // stage counters kept incrementally (no division in the loop): it % S and
-    // its phase, it % TS, and (it - TS) % S and its phase once it >= TS
-    uint32_t cs = 0, cph = 0, cts = 0, ps = 0, pph = 0;
-    auto adv = [&]() {
-      if (++cs == static_cast<uint32_t>(S)) {
-        cs = 0;
-        cph ^= 1;
-      }
-      if (++cts == static_cast<uint32_t>(TS)) cts = 0;
-      if (it > static_cast<uint32_t>(TS) && ++ps == static_cast<uint32_t>(S)) {
-        ps = 0;
-        pph ^= 1;
-      }
-    };
+    uint32_t it_u = 0, ev = 0;  // it_u: the unit's first stage in this CTA's stage sequence
     bool ok = true;
     Unit u;
     for (int ui = 0; ok && next_unit(p, wk, ui, u); ++ui) {
@@ -838,274 +832,343 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int64_t m0 = static_cast<int64_t>(mt) * BM;
       const int nkb = u.kb1 - u.kb0;
       const int chunk_len = MODE == kW4A8 ? p.chunk_stages : nkb;
-      int cleft = 0;  // stages left in the current exact chunk
       bool first_chunk = true;
-      int gcur = u.kb0 * NS / sub_per_group;  // scale group of stage j
-      int gleft = sub_per_group - (u.kb0 * NS) % sub_per_group;
-      auto gadv = [&]() {
-        if (stage_in_group) {
-          gleft -= NS;
-          if (gleft == 0) {
-            ++gcur;
-            gleft = sub_per_group;
+      // one stage of this group (stage it of the sequence, j of the unit, in
+      // shared-memory slot s with phase cph and tensor-memory slot ts; stage
+      // it - TS in slot ps with phase pph); false when a wait gave up
+      auto conv_stage = [&](int j, uint32_t it, uint32_t s, uint32_t cph, uint32_t ts,
+                            uint32_t ps, uint32_t pph) -> bool {
+        // The tensor-memory slot first: it is free once the MMA of stage
+        // it-TS retired.  MMAs retire in order, so stage it-S (TS < S),
+        // the previous user of shared-memory slot s, has then been converted
+        // and its copies have landed; only after that is the parity wait on
+        // full[s] unambiguous.  (A group converts every kConvGroups-th stage:
+        // nothing else orders this group's wait after the landing of stage
+        // it-S, which another group converted; were that phase still
+        // pending, the parity wait would pass at once.)  The slot wait itself
+        // is unambiguous for S >= kConvGroups: this group's previous slot
+        // wait (stage it-kConvGroups-TS) already covers stage it-TS-S.
+        if (it >= static_cast<uint32_t>(TS)) {
+          if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.empty[ps], pph, abort, args.status))) {
+            return false;
           }
-        } else {
-          gcur += p.gps;
         }
-      };
-      for (int j = 0; j < nkb; ++j, ++it, adv(), gadv()) {
-        if (cleft == 0) cleft = chunk_len < nkb - j ? chunk_len : nkb - j;
-        if (static_cast<int>(it % kConvGroups) == grp) {
-          const uint32_t s = cs, ts = cts;
-          // The tensor-memory slot first: it is free once the MMA of stage
-          // it-TS retired.  MMAs retire in order, so stage it-S (TS < S),
-          // the previous user of shared-memory slot s, has then been converted
-          // and its copies have landed; only after that is the parity wait on
-          // full[s] unambiguous.  (A group converts every kConvGroups-th stage:
-          // nothing else orders this group's wait after the landing of stage
-          // it-S, which another group converted; were that phase still
-          // pending, the parity wait would pass at once.)  The slot wait itself
-          // is unambiguous for S >= kConvGroups: this group's previous slot
-          // wait (stage it-kConvGroups-TS) already covers stage it-TS-S.
-          if (it >= static_cast<uint32_t>(TS)) {
-            if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.empty[ps], pph, abort, args.status))) {
-              ok = false;
-              break;
-            }
-          }
-          if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.full[s], cph, abort, args.status))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int k64_0 = (u.kb0 + j) * NS;
-          const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
-          for (int t = 0; t < NT; ++t) {
-            const size_t st_idx = static_cast<size_t>(s) * NT + t;
-            const uint8_t* wst = sm.w + st_idx * NS * WB;
-            const uint8_t* sst = sm.s + st_idx * NS * 256;
-            const uint8_t* zst = sm.z + st_idx * NS * 256;
-            const uint32_t tcol = tmem + lane_base + p.acol + (ts * NT + t) * NS * 32;
-            const bool row_ok = n0 + t * kTileN + r < N;
-            for (int qq = 0; qq < nv; ++qq) {
-              if constexpr (F8) {
-                // four 32-K chunks -> 32 columns of E4M3 bytes (no scales)
-                uint32_t v[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                  convert_chunk_f8(*reinterpret_cast<const uint4*>(wst + qq * WB + c * 2048 + r * 16),
-                                   args.wbias, v + 8 * c);
-                if (!row_ok) {
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) v[i] = 0;
-                }
-                tmem_st32(tcol + qq * 32, v);
-                continue;
-              }
-              const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
-              const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
-              const int grow = stage_in_group ? 0 : qq >> grow_shift;
-              uint32_t s2 = 0, nz2 = 0;
-              bool has_s = true;
-              if (MODE == kW4A8) {
-                has_s = args.scales != nullptr;
-                if (has_s) {
-                  const float sg = static_cast<float>(
-                      reinterpret_cast<const int8_t*>(sst + grow * 128)[r]);
-                  s2 = as_u32(__float2bfloat162_rn(sg));
-                }
-              } else {
-                const uint16_t sv = reinterpret_cast<const uint16_t*>(sst + grow * 256)[r];
-                s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
-                if (args.zeros) {
-                  const uint16_t zv =
-                      reinterpret_cast<const uint16_t*>(zst + grow * 256)[r] ^ 0x8000u;
-                  nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
-                }
-              }
+        if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.full[s], cph, abort, args.status))) {
+          return false;
+        }
+        tc_fence_after();
+        const int k64_0 = (u.kb0 + j) * NS;
+        const int nv = p.k64 - k64_0 < NS ? p.k64 - k64_0 : NS;
+        for (int t = 0; t < NT; ++t) {
+          const size_t st_idx = static_cast<size_t>(s) * NT + t;
+          const uint8_t* wst = sm.w + st_idx * NS * WB;
+          const uint8_t* sst = sm.s + st_idx * NS * 256;
+          const uint8_t* zst = sm.z + st_idx * NS * 256;
+          const uint32_t tcol = tmem + lane_base + p.acol + (ts * NT + t) * NS * 32;
+          const bool row_ok = n0 + t * kTileN + r < N;
+          for (int qq = 0; qq < nv; ++qq) {
+            if constexpr (F8) {
+              // four 32-K chunks -> 32 columns of E4M3 bytes (no scales)
               uint32_t v[32];
-              uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
-              uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
-              convert_chunk<MODE>(w0, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v0);
-              convert_chunk<MODE>(w1, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v1);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                convert_chunk_f8(*reinterpret_cast<const uint4*>(wst + qq * WB + c * 2048 + r * 16),
+                                 args.wbias, v + 8 * c);
               if (!row_ok) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0;
               }
               tmem_st32(tcol + qq * 32, v);
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            // empty first: once the MMA thread sees tfull, this group's share
-            // of the stage's release has been counted
-            mbar_arrive(&sm.empty[s]);
-            if constexpr (PAIR) mbar_arrive_remote(tfull_c + ts * 8);
-            else mbar_arrive(&sm.tfull[ts]);
-          }
-        }
-        const bool chunk_end = --cleft == 0;
-        if (!chunk_end) continue;
-        // ------------------------------------------------ drain an event
-        const bool final_ev = (j == nkb - 1);
-        const bool split = final_ev && u.nslots > 1;
-        const size_t slot_elems = static_cast<size_t>(NT) * kTileN * BM;
-        const uint32_t* part = reinterpret_cast<const uint32_t*>(args.partials);
-        // Split tile: each warp takes its place in the arrival order of the
-        // tile's contributors for its sub-tile (low half of the counter).
-        // The last to arrive adds the others' partial sums to its own
-        // accumulator; the others write theirs and then count themselves as
-        // written (high half), which the last one waits for.
-        int* ctr = args.counters + (static_cast<size_t>(u.tile) * NCTA + rank) * kConvWarps + cw;
-        bool reducer = false;
-        if (split) {
-          int prev_count = 0;
-          if (lane == 0) prev_count = atomicAdd(ctr, 1);
-          prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
-          reducer = (prev_count & 0xffff) == u.nslots - 1;
-        }
-        // position of this unit among the tile's contributors (K order), and
-        // the slot of contributor sl held by lane sl (<= 32 contributors)
-        // (a pair's two CTAs keep separate slots: pair slot * NCTA + rank)
-        const int my_sl = p.decomp == kSplitK ? u.split : static_cast<int>(wk.me) - u.cfirst;
-        const size_t lane_slot =
-            reducer && lane < u.nslots ? (slot_index(p, wk, u, lane) * NCTA + rank) * slot_elems : 0;
-        // Pull what this drain will read toward L2 while the last MMAs run:
-        // the other contributors' partial sums (reducer) and the int32
-        // running sum of the earlier chunks (W4A8 with the global copy).
-        int32_t* gi_base = args.icopy + static_cast<size_t>(blockIdx.x) * NT * BM * kTileN;
-        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
-          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
-          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
-          if (MODE == kW4A8 && p.gicopy && !first_chunk) prefetch_l2(gi_base + coff);
-          if (reducer) {
-            for (int sl = 0; sl < u.nslots; ++sl) {
-              if (sl == my_sl) continue;
-              const size_t sbase =
-                  u.nslots <= 32
-                      ? static_cast<size_t>(__shfl_sync(
-                            0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
-                      : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
-              prefetch_l2(part + sbase + coff);
-            }
-          }
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait<true>(sm.dfull, ev & 1, abort, args.status))) {
-          ok = false;
-          break;
-        }
-        ++ev;
-        tc_fence_after();
-        if (reducer) {
-          // every other contributor has written its partial sums
-          bool done = true;
-          if (lane == 0) done = wait_count_hi(ctr, u.nslots - 1, abort, args.status);
-          if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, done, 0))) {
-            ok = false;
-            break;
-          }
-          __threadfence();
-        }
-        const size_t my_slot =
-            split && !reducer ? (own_slot(p, wk, u) * NCTA + rank) * slot_elems : 0;
-        // Blocks of 8 accumulator columns over all weight tiles, round-robin
-        // over the converter groups.  Global layout of partial sums and of
-        // the int32 running sum: block (t, cc) is 128 rows x 8 columns, row r
-        // holding its 8 columns contiguously.
-        for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
-          const int t = bb / nblk, cc = (bb - t * nblk) * 8;
-          const uint32_t dcol = tmem + lane_base + t * BM + cc;
-          const int64_t nrow = n0 + t * kTileN + r;  // output column
-          const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
-          uint32_t d[8];
-          tmem_ld8(dcol, d);
-          if (MODE == kW4A8) {
-            // add the int32 running sum of the earlier chunks of this unit:
-            // in tensor memory, or in this CTA's global scratch
-            const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
-            int32_t* gi = gi_base + coff;
-            uint32_t prev[8];
-            if (!first_chunk) {
-              if (p.gicopy) ld_cg_v8(gi, prev);
-              else tmem_ld8(icol, prev);
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(d[i])) +
-                                           (first_chunk ? 0 : static_cast<int32_t>(prev[i])));
-            if (!final_ev) {
-              if (p.gicopy) {
-                st_v8(gi, d);
-              } else {
-                tmem_st8(icol, d);
-                tmem_wait_st();
-              }
               continue;
             }
-          } else {
-            tmem_wait_ld();
-          }
-          // d: this unit's sums of the block (int32 or fp32 bits)
-          if (split && !reducer) {
-            st_v8(static_cast<uint32_t*>(args.partials) + my_slot + coff, d);
-            continue;
-          }
-          if (reducer) {
-            // add the contributors in K order, this unit's own sums at its place
-            uint32_t acc[8];
-            for (int sl = 0; sl < u.nslots; ++sl) {
-              uint32_t x[8];
-              if (sl == my_sl) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + r * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(wst + qq * 4096 + 2048 + r * 16);
+            const int grow = stage_in_group ? 0 : qq >> grow_shift;
+            uint32_t s2 = 0, nz2 = 0;
+            bool has_s = true;
+            if (MODE == kW4A8) {
+              has_s = args.scales != nullptr;
+              if (has_s) {
+                const float sg = static_cast<float>(
+                    reinterpret_cast<const int8_t*>(sst + grow * 128)[r]);
+                s2 = as_u32(__float2bfloat162_rn(sg));
+              }
+            } else {
+              const uint16_t sv = reinterpret_cast<const uint16_t*>(sst + grow * 256)[r];
+              s2 = static_cast<uint32_t>(sv) | (static_cast<uint32_t>(sv) << 16);
+              if (args.zeros) {
+                const uint16_t zv =
+                    reinterpret_cast<const uint16_t*>(zst + grow * 256)[r] ^ 0x8000u;
+                nz2 = static_cast<uint32_t>(zv) | (static_cast<uint32_t>(zv) << 16);
+              }
+            }
+            uint32_t v[32];
+            uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+            uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
+            convert_chunk<MODE>(w0, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v0);
+            convert_chunk<MODE>(w1, s2, nz2, args.zeros != nullptr, has_s, args.wbias, v1);
+            if (!row_ok) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = d[i];
-              } else {
+              for (int i = 0; i < 32; ++i) v[i] = 0;
+            }
+            tmem_st32(tcol + qq * 32, v);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // empty first: once the MMA thread sees tfull, this group's share
+          // of the stage's release has been counted
+          mbar_arrive(&sm.empty[s]);
+          if constexpr (PAIR) mbar_arrive_remote(tfull_c + ts * 8);
+          else mbar_arrive(&sm.tfull[ts]);
+        }
+        return true;
+      };
+      // drain the accumulator at the end of an exact chunk or of the unit
+      // (every converter warp); false when a wait gave up
+      auto drain = [&](bool final_ev) -> bool {
+          // ------------------------------------------------ drain an event
+          const bool split = final_ev && u.nslots > 1;
+          const size_t slot_elems = static_cast<size_t>(NT) * kTileN * BM;
+          const uint32_t* part = reinterpret_cast<const uint32_t*>(args.partials);
+          // Split tile: each warp takes its place in the arrival order of the
+          // tile's contributors for its sub-tile (low half of the counter).
+          // The last to arrive adds the others' partial sums to its own
+          // accumulator; the others write theirs and then count themselves as
+          // written (high half), which the last one waits for.
+          int* ctr = args.counters + (static_cast<size_t>(u.tile) * NCTA + rank) * kConvWarps + cw;
+          bool reducer = false;
+          if (split) {
+            int prev_count = 0;
+            if (lane == 0) prev_count = atomicAdd(ctr, 1);
+            prev_count = __shfl_sync(0xffffffffu, prev_count, 0);
+            reducer = (prev_count & 0xffff) == u.nslots - 1;
+          }
+          // position of this unit among the tile's contributors (K order), and
+          // the slot of contributor sl held by lane sl (<= 32 contributors)
+          // (a pair's two CTAs keep separate slots: pair slot * NCTA + rank)
+          const int my_sl = p.decomp == kSplitK ? u.split : static_cast<int>(wk.me) - u.cfirst;
+          const size_t lane_slot =
+              reducer && lane < u.nslots ? (slot_index(p, wk, u, lane) * NCTA + rank) * slot_elems : 0;
+          // Pull what this drain will read toward L2 while the last MMAs run:
+          // the other contributors' partial sums (reducer) and the int32
+          // running sum of the earlier chunks (W4A8 with the global copy).
+          int32_t* gi_base = args.icopy + static_cast<size_t>(blockIdx.x) * NT * BM * kTileN;
+          for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+            const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+            const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+            if (MODE == kW4A8 && p.gicopy && !first_chunk) prefetch_l2(gi_base + coff);
+            if (reducer) {
+              for (int sl = 0; sl < u.nslots; ++sl) {
+                if (sl == my_sl) continue;
                 const size_t sbase =
                     u.nslots <= 32
                         ? static_cast<size_t>(__shfl_sync(
                               0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
                         : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
-                ld_cg_v8(part + sbase + coff, x);
-              }
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (sl == 0) acc[i] = x[i];
-                else if (MODE == kW4A8)
-                  acc[i] = static_cast<uint32_t>(static_cast<int32_t>(acc[i]) +
-                                                 static_cast<int32_t>(x[i]));
-                else
-                  acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __uint_as_float(x[i]));
+                prefetch_l2(part + sbase + coff);
               }
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) d[i] = acc[i];
           }
-          // outputs
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int64_t m = m0 + cc + i;
-            if (nrow < N && m < M)
-              store_out<MODE>(args, m, nrow, __uint_as_float(d[i]), static_cast<int32_t>(d[i]));
+          if (!__all_sync(0xffffffffu, mbar_wait<true>(sm.dfull, ev & 1, abort, args.status))) {
+            return false;
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (PAIR) mbar_arrive_remote(dempty_c);
-          else mbar_arrive(sm.dempty);
-        }
-        first_chunk = false;
-        if (split && !reducer) {
-          // partial sums visible device-wide, then counted as written
-          __threadfence();
+          ++ev;
+          tc_fence_after();
+          if (reducer) {
+            // every other contributor has written its partial sums
+            bool done = true;
+            if (lane == 0) done = wait_count_hi(ctr, u.nslots - 1, abort, args.status);
+            if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, done, 0))) {
+              return false;
+            }
+            __threadfence();
+          }
+          const size_t my_slot =
+              split && !reducer ? (own_slot(p, wk, u) * NCTA + rank) * slot_elems : 0;
+          // Blocks of 8 accumulator columns over all weight tiles, round-robin
+          // over the converter groups.  Global layout of partial sums and of
+          // the int32 running sum: block (t, cc) is 128 rows x 8 columns, row r
+          // holding its 8 columns contiguously.
+          for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
+            const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+            const uint32_t dcol = tmem + lane_base + t * BM + cc;
+            const int64_t nrow = n0 + t * kTileN + r;  // output column
+            const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+            uint32_t d[8];
+            tmem_ld8(dcol, d);
+            if (MODE == kW4A8) {
+              // add the int32 running sum of the earlier chunks of this unit:
+              // in tensor memory, or in this CTA's global scratch
+              const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
+              int32_t* gi = gi_base + coff;
+              uint32_t prev[8];
+              if (!first_chunk) {
+                if (p.gicopy) ld_cg_v8(gi, prev);
+                else tmem_ld8(icol, prev);
+              }
+              tmem_wait_ld();
+  #pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(d[i])) +
+                                             (first_chunk ? 0 : static_cast<int32_t>(prev[i])));
+              if (!final_ev) {
+                if (p.gicopy) {
+                  st_v8(gi, d);
+                } else {
+                  tmem_st8(icol, d);
+                  tmem_wait_st();
+                }
+                continue;
+              }
+            } else {
+              tmem_wait_ld();
+            }
+            // d: this unit's sums of the block (int32 or fp32 bits)
+            if (split && !reducer) {
+              st_v8(static_cast<uint32_t*>(args.partials) + my_slot + coff, d);
+              continue;
+            }
+            if (reducer) {
+              // add the contributors in K order, this unit's own sums at its place
+              uint32_t acc[8];
+              for (int sl = 0; sl < u.nslots; ++sl) {
+                uint32_t x[8];
+                if (sl == my_sl) {
+  #pragma unroll
+                  for (int i = 0; i < 8; ++i) x[i] = d[i];
+                } else {
+                  const size_t sbase =
+                      u.nslots <= 32
+                          ? static_cast<size_t>(__shfl_sync(
+                                0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
+                          : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
+                  ld_cg_v8(part + sbase + coff, x);
+                }
+  #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  if (sl == 0) acc[i] = x[i];
+                  else if (MODE == kW4A8)
+                    acc[i] = static_cast<uint32_t>(static_cast<int32_t>(acc[i]) +
+                                                   static_cast<int32_t>(x[i]));
+                  else
+                    acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __uint_as_float(x[i]));
+                }
+              }
+  #pragma unroll
+              for (int i = 0; i < 8; ++i) d[i] = acc[i];
+            }
+            // outputs
+  #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int64_t m = m0 + cc + i;
+              if (nrow < N && m < M)
+                store_out<MODE>(args, m, nrow, __uint_as_float(d[i]), static_cast<int32_t>(d[i]));
+            }
+          }
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) atomicAdd(ctr, 0x10000);
-        } else if (reducer) {
-          if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
+          if (lane == 0) {
+            if constexpr (PAIR) mbar_arrive_remote(dempty_c);
+            else mbar_arrive(sm.dempty);
+          }
+          first_chunk = false;
+          if (split && !reducer) {
+            // partial sums visible device-wide, then counted as written
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicAdd(ctr, 0x10000);
+          } else if (reducer) {
+            if (lane == 0) *ctr = 0;  // leave the counter at zero for the next call
+          }
+        return true;
+      };
+      if constexpr (kOwnStages) {
+        // Exact chunks (W4A8) or the whole unit, each ended by a drain;
+        // within a chunk this group visits only its own stages (every
+        // kConvGroups-th one): stepping over the other groups' stages one by
+        // one cost about as much as converting its own.
+        for (int c0 = 0; ok && c0 < nkb; c0 += chunk_len) {
+          const int c1 = c0 + chunk_len < nkb ? c0 + chunk_len : nkb;
+          int j = c0 + static_cast<int>((static_cast<uint32_t>(grp) + kConvGroups -
+                                         (it_u + c0) % kConvGroups) % kConvGroups);
+          uint32_t it = it_u + j;
+          // ring positions of stage it (divisions once per chunk, then steps
+          // of kConvGroups <= S stages): shared-memory slot it % S and its
+          // phase, tensor-memory slot it % TS, and the slot and phase of
+          // stage it - TS
+          uint32_t cs = it % S, cph = (it / S) & 1u, cts = it % TS, ps = 0, pph = 0;
+          if (it >= static_cast<uint32_t>(TS)) {
+            ps = (it - TS) % S;
+            pph = ((it - TS) / S) & 1u;
+          }
+          for (; j < c1; j += kConvGroups, it += kConvGroups) {
+            if (!conv_stage(j, it, cs, cph, cts, ps, pph)) {
+              ok = false;
+              break;
+            }
+            // the next stage of this group, kConvGroups further on
+            cs += kConvGroups;
+            if (cs >= static_cast<uint32_t>(S)) {
+              cs -= S;
+              cph ^= 1u;
+            }
+            cts += kConvGroups;
+            while (cts >= static_cast<uint32_t>(TS)) cts -= TS;
+            const uint32_t itn = it + kConvGroups;
+            if (it >= static_cast<uint32_t>(TS)) {
+              ps += kConvGroups;
+              if (ps >= static_cast<uint32_t>(S)) {
+                ps -= S;
+                pph ^= 1u;
+              }
+            } else if (itn >= static_cast<uint32_t>(TS)) {
+              ps = (itn - TS) % S;
+              pph = ((itn - TS) / S) & 1u;
+            }
+          }
+          if (!ok) break;
+          if (!drain(c1 == nkb)) {
+            ok = false;
+            break;
+          }
+        }
+      } else {
+        // every stage in turn, converting this group's (the single-CTA W4A8
+        // kernels: the loop above needs more registers there and spills)
+        uint32_t it = it_u;
+        uint32_t cs = it % S, cph = (it / S) & 1u, cts = it % TS, ps = 0, pph = 0;
+        if (it >= static_cast<uint32_t>(TS)) {
+          ps = (it - TS) % S;
+          pph = ((it - TS) / S) & 1u;
+        }
+        int cleft = 0;  // stages left in the current exact chunk
+        for (int j = 0; j < nkb; ++j, ++it) {
+          if (cleft == 0) cleft = chunk_len < nkb - j ? chunk_len : nkb - j;
+          if (static_cast<int>(it % kConvGroups) == grp &&
+              !conv_stage(j, it, cs, cph, cts, ps, pph)) {
+            ok = false;
+            break;
+          }
+          if (++cs == static_cast<uint32_t>(S)) {
+            cs = 0;
+            cph ^= 1u;
+          }
+          if (++cts == static_cast<uint32_t>(TS)) cts = 0;
+          if (it + 1 > static_cast<uint32_t>(TS) && ++ps == static_cast<uint32_t>(S)) {
+            ps = 0;
+            pph ^= 1u;
+          }
+          if (--cleft != 0) continue;
+          if (!drain(j == nkb - 1)) {
+            ok = false;
+            break;
+          }
         }
       }
+      it_u += nkb;
     }
   }
 

@@ -52,10 +52,13 @@ def test_default_heuristic(lib):
     assert name(16, 4096, 4096, torch.bfloat16, 64) == "tc16_sk"   # group 64 splits a K block
     assert name(32, 8192, 21760, torch.int8, -1) == "ds32_sk"
     assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
-    # W4A8 at 256-row tiles on CTA pairs (stream-K: 256 tiles < 4 waves); W4A16 on single CTAs
+    # 256-row tiles on CTA pairs (stream-K: 256 tiles < 4 waves; data-parallel beyond)
     assert name(1024, 8192, 21760, torch.int8, -1) == "tc256p_sk"
-    assert name(1024, 8192, 21760, torch.bfloat16, 128) == "tc256_sk"
-    assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"
+    assert name(1024, 8192, 21760, torch.bfloat16, 128) == "tc256p_sk"
+    assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256p_dp"
+    # 128-row tiles: pairs for W4A8, single CTAs otherwise
+    assert name(128, 8192, 21760, torch.int8, -1) == "tc128p_sk"
+    assert name(128, 8192, 21760, torch.bfloat16, 128) == "tc128_sk"
     assert name(4, 13, 512, torch.float16, 128) == "dk8_sk"  # any N (streamed needs N % 8 == 0)
     assert name(20, 13, 512, torch.float16, 128) == "simt"  # N % 8 != 0 beyond 16 rows
     assert w4.default_schedule(0, 8, 64, torch.float16, -1) == -1
@@ -296,10 +299,12 @@ def test_override_table(lib):
     validated on the host."""
     import torch
     name = lambda M, N, K, dt, g: w4.schedule_names()[w4.default_schedule(M, N, K, dt, g)]
-    # built-in: Llama-3-70B prefill shapes prefer the stream-K 256-row tiles
-    assert name(4096, 8192, 28672, torch.bfloat16, 128) == "tc256_sk"
-    assert name(8192, 57344, 8192, torch.bfloat16, 128) == "tc256_sk"
-    assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256_dp"  # outside the range
+    # built-in: Llama-3-70B prefill shapes on data-parallel CTA-pair tiles (the
+    # heuristic's choice too); outside the entries' M range the heuristic decides
+    assert name(4096, 8192, 28672, torch.bfloat16, 128) == "tc256p_dp"
+    assert name(8192, 57344, 8192, torch.bfloat16, 128) == "tc256p_dp"
+    assert name(16384, 57344, 8192, torch.bfloat16, 128) == "tc256p_dp"
+    assert name(2048, 8192, 28672, torch.bfloat16, 128) == "tc256p_sk"  # 512 tiles < 4 waves
     # installed at run time
     assert name(64, 4096, 4096, torch.bfloat16, 128) == "tc64_sk"
     w4.override_schedule(torch.bfloat16, 33, 64, 4096, 4096, 128, "tc128_sk")
