@@ -96,6 +96,8 @@ struct TcPlan {
 // MMA groups issued by two alternating threads (else one): where a group's
 // MMAs are short (N <= 128 activation rows)
 inline bool tc_mma2(const TcPlan& p) { return p.bm <= 128 && !p.pair; }
+// W4A8 with group scales: exact chunks of 1024 K (16384 K per-channel)
+inline bool tc_grouped(const TcPlan& p) { return p.chunk_stages * kStageK * p.nsub < 16384; }
 
 struct TcArgs {
   const uint8_t* b_packed;

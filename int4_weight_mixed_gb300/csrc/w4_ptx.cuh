@@ -152,6 +152,18 @@ __device__ __forceinline__ void st_v8(void* p, const uint32_t* v) {
   q[0] = make_uint4(v[0], v[1], v[2], v[3]);
   q[1] = make_uint4(v[4], v[5], v[6], v[7]);
 }
+// 8 words as two 16-byte halves `half` words apart (a warp's lanes 16 bytes
+// apart: each load or store instruction covers 512 contiguous bytes).
+__device__ __forceinline__ void ld_cg_halves(const uint32_t* p, int half, uint32_t (&v)[8]) {
+  const uint4 a = __ldcg(reinterpret_cast<const uint4*>(p));
+  const uint4 b = __ldcg(reinterpret_cast<const uint4*>(p + half));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st_halves(uint32_t* p, int half, const uint32_t* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<uint4*>(p + half) = make_uint4(v[4], v[5], v[6], v[7]);
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }

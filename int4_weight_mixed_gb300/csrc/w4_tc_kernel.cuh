@@ -265,6 +265,17 @@ struct Smem {
 
 }  // namespace
 
+// d (fp32 sums of one W4A8 chunk, exact integers below 2^24) becomes its
+// int32 value plus the running sum prev (unless this is the first chunk).
+__device__ __forceinline__ void add_chunk_sums(uint32_t (&d)[8], const uint32_t (&prev)[8],
+                                               bool first) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t v = static_cast<uint32_t>(__float2int_rn(__uint_as_float(d[k])));
+    d[k] = first ? v : v + prev[k];
+  }
+}
+
 // MMA2: two alternating MMA-issuing threads; a separate instantiation.
 // PAIR: a cluster of two CTAs shares every MMA (cta_group::2, M = 256): CTA
 // rank r converts weight columns [n0 + 128r, n0 + 128r + 128) of the pair's
@@ -274,7 +285,15 @@ struct Smem {
 // weight columns against all BM rows.  Per SM the MMA work of a stage is
 // that of a single CTA, but the activation bytes per stage halve, so twice
 // as many stages fit in shared memory.
-template <int MODE, bool MMA2, bool PAIR = false>
+// LEAN (CTA pairs): the single 128-column weight tile of each CTA is a
+// compile-time constant, and the stream-K partial sums use the layout of the
+// running sums (each 16-byte access of a warp covering 512 contiguous
+// bytes).  Measured (chained launches, N=8192 K=21760): grouped W4A8 7-9%,
+// fp8 activations 5% and W4A16 prefill 3-6% faster with it, while the
+// per-channel W4A8 pair kernel, whose time is spent in a few long exact
+// chunks and the stream-K fix-up, was 3-14% slower in every variant of it
+// tried; that one is instantiated without it.
+template <int MODE, bool MMA2, bool PAIR = false, bool LEAN = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap amap,
                    const __grid_constant__ CUtensorMap smap,
@@ -301,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages, NT = p.nt;
+  const int S = p.stages, BM = p.bm, NS = p.nsub, TS = p.tstages, NT = LEAN ? 1 : p.nt;
   const int BMc = BM / NCTA;  // activation rows held by this CTA
   const uint32_t a_sub = static_cast<uint32_t>(BMc) * 128;  // bytes of one 64-K activation tile
   Smem sm;
@@ -955,11 +974,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // Pull what this drain will read toward L2 while the last MMAs run:
           // the other contributors' partial sums (reducer) and the int32
           // running sum of the earlier chunks (W4A8 with the global copy).
-          int32_t* gi_base = args.icopy + static_cast<size_t>(blockIdx.x) * NT * BM * kTileN;
+          uint32_t* gi_base = reinterpret_cast<uint32_t*>(args.icopy) +
+                              static_cast<size_t>(blockIdx.x) * NT * BM * kTileN;
           for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
-            const int t = bb / nblk, cc = (bb - t * nblk) * 8;
-            const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
-            if (MODE == kW4A8 && p.gicopy && !first_chunk) prefetch_l2(gi_base + coff);
+            const int t = LEAN ? 0 : bb / nblk, cc = (bb - t * nblk) * 8;
+            const size_t goff = static_cast<size_t>(bb) * 1024 + q * 256 + lane * 4;
+            const size_t coff = LEAN ? goff : static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+            if (MODE == kW4A8 && p.gicopy && !first_chunk) {
+              prefetch_l2(gi_base + goff);
+              prefetch_l2(gi_base + goff + 128);
+            }
             if (reducer) {
               for (int sl = 0; sl < u.nslots; ++sl) {
                 if (sl == my_sl) continue;
@@ -969,6 +993,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
                         : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
                 prefetch_l2(part + sbase + coff);
+                if (LEAN) prefetch_l2(part + sbase + coff + 128);
               }
             }
           }
@@ -989,34 +1014,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const size_t my_slot =
               split && !reducer ? (own_slot(p, wk, u) * NCTA + rank) * slot_elems : 0;
           // Blocks of 8 accumulator columns over all weight tiles, round-robin
-          // over the converter groups.  Global layout of partial sums and of
-          // the int32 running sum: block (t, cc) is 128 rows x 8 columns, row r
-          // holding its 8 columns contiguously.
+          // over the converter groups.  Global layout of the int32 running
+          // sum (and of the partial sums, LEAN): block bb = (t, cc) is 1024
+          // words, the 32 rows of lane quadrant q at q * 256, columns 0-3 of
+          // each row (16 bytes per lane) first and columns 4-7 128 words
+          // further on, so that each 16-byte access of a warp covers 512
+          // contiguous bytes; partial sums otherwise: row r of the block
+          // holds its 8 columns contiguously at r * 8.
           for (int bb = grp; bb < NT * nblk; bb += kConvGroups) {
-            const int t = bb / nblk, cc = (bb - t * nblk) * 8;
+            const int t = LEAN ? 0 : bb / nblk, cc = (bb - t * nblk) * 8;
             const uint32_t dcol = tmem + lane_base + t * BM + cc;
             const int64_t nrow = n0 + t * kTileN + r;  // output column
-            const size_t coff = static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
+            const size_t goff = static_cast<size_t>(bb) * 1024 + q * 256 + lane * 4;
+            const size_t coff = LEAN ? goff : static_cast<size_t>(t * BM + cc) * kTileN + r * 8;
             uint32_t d[8];
             tmem_ld8(dcol, d);
             if (MODE == kW4A8) {
               // add the int32 running sum of the earlier chunks of this unit:
               // in tensor memory, or in this CTA's global scratch
               const uint32_t icol = tmem + lane_base + p.icol + t * BM + cc;
-              int32_t* gi = gi_base + coff;
               uint32_t prev[8];
               if (!first_chunk) {
-                if (p.gicopy) ld_cg_v8(gi, prev);
+                if (p.gicopy) ld_cg_halves(gi_base + goff, 128, prev);
                 else tmem_ld8(icol, prev);
               }
               tmem_wait_ld();
-  #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                d[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(d[i])) +
-                                             (first_chunk ? 0 : static_cast<int32_t>(prev[i])));
+              add_chunk_sums(d, prev, first_chunk);
               if (!final_ev) {
                 if (p.gicopy) {
-                  st_v8(gi, d);
+                  st_halves(gi_base + goff, 128, d);
                 } else {
                   tmem_st8(icol, d);
                   tmem_wait_st();
@@ -1028,7 +1054,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // d: this unit's sums of the block (int32 or fp32 bits)
             if (split && !reducer) {
-              st_v8(static_cast<uint32_t*>(args.partials) + my_slot + coff, d);
+              if (LEAN) st_halves(static_cast<uint32_t*>(args.partials) + my_slot + coff, 128, d);
+              else st_v8(static_cast<uint32_t*>(args.partials) + my_slot + coff, d);
               continue;
             }
             if (reducer) {
@@ -1045,7 +1072,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           ? static_cast<size_t>(__shfl_sync(
                                 0xffffffffu, static_cast<unsigned long long>(lane_slot), sl))
                           : (slot_index(p, wk, u, sl) * NCTA + rank) * slot_elems;
-                  ld_cg_v8(part + sbase + coff, x);
+                  if (LEAN) ld_cg_halves(part + sbase + coff, 128, x);
+                  else ld_cg_v8(part + sbase + coff, x);
                 }
   #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -1186,10 +1214,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 
 namespace {
-template <int MODE, bool MMA2, bool PAIR>
+template <int MODE, bool MMA2, bool PAIR, bool LEAN = false>
 cudaError_t launch_tc_mode(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                            const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
-  auto* fn = &tc_gemm_kernel<MODE, MMA2, PAIR>;
+  auto* fn = &tc_gemm_kernel<MODE, MMA2, PAIR, LEAN>;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem_bytes));
@@ -1226,11 +1254,17 @@ cudaError_t launch_tc_mode(const TcPlan& plan, const CUtensorMap& amap, const CU
 template <bool MMA2, bool PAIR = false>
 cudaError_t launch_tc_t(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                         const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  // CTA pairs: LEAN except for per-channel W4A8 (see tc_gemm_kernel)
   switch (plan.mode) {
-    case kW4A16_F16: return launch_tc_mode<kW4A16_F16, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
-    case kW4A16_BF16: return launch_tc_mode<kW4A16_BF16, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
-    case kW4A8F8: return launch_tc_mode<kW4A8F8, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
-    default: return launch_tc_mode<kW4A8, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
+    case kW4A16_F16:
+      return launch_tc_mode<kW4A16_F16, MMA2, PAIR, PAIR>(plan, amap, smap, zmap, args, s);
+    case kW4A16_BF16:
+      return launch_tc_mode<kW4A16_BF16, MMA2, PAIR, PAIR>(plan, amap, smap, zmap, args, s);
+    case kW4A8F8: return launch_tc_mode<kW4A8F8, MMA2, PAIR, PAIR>(plan, amap, smap, zmap, args, s);
+    default:
+      if (PAIR && tc_grouped(plan))
+        return launch_tc_mode<kW4A8, MMA2, PAIR, PAIR>(plan, amap, smap, zmap, args, s);
+      return launch_tc_mode<kW4A8, MMA2, PAIR>(plan, amap, smap, zmap, args, s);
   }
 }
 
