@@ -329,6 +329,30 @@ def test_w4a8_extreme_magnitudes_exact(gpu_lib, gs):
         assert np.array_equal(acc.numpy().astype(np.int64), ref), name
 
 
+@pytest.mark.parametrize("name", ["tc256p_sk", "tc256p_dp", "tc128p_sk"])
+@pytest.mark.parametrize("gs", [-1, 128])
+def test_w4a8_extreme_magnitudes_pairs(gpu_lib, name, gs):
+    """The same largest partial sums on CTA pairs, over enough weight tiles
+    that a unit spans several exact chunks (the int32 running sum of the
+    256-row tiles in global scratch, of the 128-row tiles in tensor memory)
+    and stream-K tiles are shared by several pairs."""
+    w4 = gpu_lib
+    M, N, K = 5, 2048, 21760
+    q = np.full((K, N), 8, dtype=np.uint8)
+    q[:, 1::2] = 7
+    w = torch.from_numpy(oracle.pack(q, oracle.NK_EXLLAMA))
+    a = torch.full((M, K), -128, dtype=torch.int8)
+    a[1] = 127
+    a[2, ::2] = 127
+    a[3] = torch.randint(-128, 128, (K,), generator=torch.Generator().manual_seed(1)).to(torch.int8)
+    a[4, 1::2] = 127
+    sg = torch.full((K // 128, N), 16, dtype=torch.int8) if gs == 128 else None
+    e = dict(a=a, w=w, sg=sg, layout=oracle.NK_EXLLAMA, wtype=w4.INT4, K=K, N=N, group_size=gs)
+    acc = run_w4a8(w4, e, torch.int32, sched(w4, name))
+    ref = oracle.w4a8(a, w, oracle.NK_EXLLAMA, w4.INT4, sg, gs, K, N)
+    assert np.array_equal(acc.numpy().astype(np.int64), ref)
+
+
 @pytest.mark.parametrize("M", w4synth.QQQ_CH_M)
 def test_w4a8_qqq_per_channel(gpu_lib, M):
     w4 = gpu_lib
@@ -396,7 +420,7 @@ def test_deterministic_stream_k(gpu_lib):
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("name", ["tc16_sk", "tc32_sk"])
+@pytest.mark.parametrize("name", ["tc16_sk", "tc32_sk", "tc256p_sk", "tc128p_sk"])
 def test_stream_k_many_contributors(gpu_lib, name):
     """One weight tile over a long K: stream-K spreads its stages over more
     than 32 CTAs, so the tile's last arriving warp adds over 32 other partial
