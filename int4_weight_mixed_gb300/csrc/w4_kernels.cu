@@ -82,23 +82,52 @@ __global__ void unprepack_kernel(const uint32_t* __restrict__ packed, int wtype,
   }
 }
 
+// int8 -> the bf16 value, four codes of a word at a time without the
+// conversion unit: byte k of w ^ 0x80808080 is v + 128; placed in the low
+// mantissa byte of 2^23 (the bit pattern 0x4B0000uu) it reads 2^23 + v + 128,
+// so subtracting 2^23 + 128 leaves v exactly, and a pair of such floats
+// rounds to bf16 exactly (|v| <= 128).
+__device__ __forceinline__ void s8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  float f[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t bits;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(bits) : "r"(u), "r"(0x4B000000u), "r"(0x7540u | k));
+    f[k] = __fsub_rn(__uint_as_float(bits), 8388736.f);  // 2^23 + 128
+  }
+  __nv_bfloat162 p0 = __floats2bfloat162_rn(f[0], f[1]);
+  __nv_bfloat162 p1 = __floats2bfloat162_rn(f[2], f[3]);
+  lo = *reinterpret_cast<uint32_t*>(&p0);
+  hi = *reinterpret_cast<uint32_t*>(&p1);
+}
+
+// int8 activations -> the bf16 copy the tensor-core W4A8 schedule reads:
+// sixteen codes (one 16-byte load, two 16-byte stores) per thread and
+// step; an odd last group of eight goes by itself.
 __global__ void a8_to_bf16_kernel(const int8_t* __restrict__ a, int64_t count8,
                                   uint4* __restrict__ out) {
   // the W4A8 tensor-core GEMM that follows may launch now: it streams weights
   // until this grid is complete
   asm volatile("griddepcontrol.launch_dependents;");
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count8;
+  const int64_t count16 = count8 >> 1;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count16;
        i += (int64_t)gridDim.x * blockDim.x) {
-    uint2 v = reinterpret_cast<const uint2*>(a)[i];
-    const int8_t* b = reinterpret_cast<const int8_t*>(&v);
-    uint32_t r[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(b[2 * p]),
-                                               static_cast<float>(b[2 * p + 1]));
-      r[p] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    out[i] = make_uint4(r[0], r[1], r[2], r[3]);
+    const uint4 v = reinterpret_cast<const uint4*>(a)[i];
+    uint4 o0, o1;
+    s8x4_to_bf16x4(v.x, o0.x, o0.y);
+    s8x4_to_bf16x4(v.y, o0.z, o0.w);
+    s8x4_to_bf16x4(v.z, o1.x, o1.y);
+    s8x4_to_bf16x4(v.w, o1.z, o1.w);
+    out[2 * i] = o0;
+    out[2 * i + 1] = o1;
+  }
+  if ((count8 & 1) && blockIdx.x == 0 && threadIdx.x == 0) {
+    const uint2 v = reinterpret_cast<const uint2*>(a)[count8 - 1];
+    uint4 o;
+    s8x4_to_bf16x4(v.x, o.x, o.y);
+    s8x4_to_bf16x4(v.y, o.z, o.w);
+    out[count8 - 1] = o;
   }
 }
 
@@ -216,7 +245,7 @@ cudaError_t launch_unprepack(const uint8_t* packed, int wtype, int layout, int64
 
 cudaError_t launch_a8_to_bf16(const int8_t* a, int64_t count, void* out, cudaStream_t s) {
   int64_t c8 = count / 8;
-  a8_to_bf16_kernel<<<grid_for(c8, 256), 256, 0, s>>>(a, c8, static_cast<uint4*>(out));
+  a8_to_bf16_kernel<<<grid_for((c8 + 1) / 2, 256), 256, 0, s>>>(a, c8, static_cast<uint4*>(out));
   return cudaGetLastError();
 }
 
