@@ -625,7 +625,7 @@ def test_quantize_feeds_w4a8(gpu_lib, M):
 
 BIAS_SCHEDULES = ["simt", "tc16_sk", "tc64_sk", "tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp",
                   "dk8_sk", "dk16_sk", "ds8_sk", "ds16_sk", "ds32_sk", "gv8_cl", "gv16_cl",
-                  "gv32_cl", "tc256p_sk"]
+                  "gv32_cl", "tc256p_sk", "tc256p_dp", "tc128p_sk"]
 
 
 @pytest.mark.parametrize("name", BIAS_SCHEDULES)
@@ -647,20 +647,24 @@ def test_w4a16_bias_every_engine(gpu_lib, name, dt):
 
 
 @pytest.mark.parametrize("name", BIAS_SCHEDULES)
-def test_w4a8_bias_every_engine(gpu_lib, name):
+@pytest.mark.parametrize("gs", [128, -1])
+def test_w4a8_bias_every_engine(gpu_lib, name, gs):
+    """Bias on the W4A8 fp16 epilogue, with group scales and per-channel (on
+    CTA pairs these are different kernel instances)."""
     w4 = gpu_lib
     M = min(ROWS.get(name, 40), 40) - 2
     N, K = 384, 2048
-    e = w4synth.gen_w4a8(M, N, K, group_size=128, seed=M + 88)
+    e = w4synth.gen_w4a8(M, N, K, group_size=gs, seed=M + 88)
     b = w4.prepack_B(e["w"].to(DEV), e["wtype"], e["layout"], K, N)
     rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
     rows, cols = rows.reshape(-1), cols.reshape(-1)
-    acc = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], 128, K, N).reshape(-1)
+    acc = oracle.w4a8(e["a"], e["w"], e["layout"], e["wtype"], e["sg"], gs, K, N).reshape(-1)
     prod = oracle.w4a8_scale(acc, rows, cols, e["s_tok"], e["s_ch"])
     # a bias near minus the product in some columns (cancellation), random elsewhere
     bias = torch.from_numpy(-prod.reshape(M, N)[0]).to(torch.float16)
     bias[1::2] = (torch.randn(N // 2, generator=torch.Generator().manual_seed(6))).half()
-    got = w4.gemm(e["a"].to(DEV), b, e["wtype"], N, scales=e["sg"].to(DEV), group_size=128,
+    sg = e["sg"].to(DEV) if gs > 0 else None
+    got = w4.gemm(e["a"].to(DEV), b, e["wtype"], N, scales=sg, group_size=gs,
                   token_scales=e["s_tok"].to(DEV), channel_scales=e["s_ch"].to(DEV),
                   schedule=sched(w4, name), bias=bias.to(DEV))
     torch.cuda.synchronize()
@@ -746,6 +750,21 @@ def test_w4a8_fp8_every_schedule(gpu_lib, name):
     got = run_fp8(w4, e, sched(w4, name))
     ref, absref = fp8_ref(e)
     assert_within(got, ref, absref, "f16", f"fp8 {name}")
+
+
+@pytest.mark.parametrize("name", ["tc64_sk", "tc256_sk", "gv16_cl", "tc256p_sk", "tc256p_dp",
+                                  "tc128p_sk"])
+def test_w4a8_fp8_bias(gpu_lib, name):
+    """fp8 activations with a bias: added in fp32 to the scaled sum before the
+    one rounding to fp16 (the bias is exact in fp32, so the bound is the
+    product's plus the final rounding)."""
+    w4 = gpu_lib
+    M = min(ROWS.get(name, 40), 40) - 5
+    e = w4synth.gen_w4a8_fp8(M, 384, 2048, seed=M + 15)
+    bias = (torch.randn(384, generator=torch.Generator().manual_seed(16)) * 4).half()
+    got = run_fp8(w4, e, sched(w4, name), bias=bias.to(DEV))
+    ref, absref = fp8_ref(e)
+    assert_within(got, ref + bias.double().numpy()[None, :], absref, "f16", f"fp8 bias {name}")
 
 
 @pytest.mark.parametrize("M", [1, 8, 32, 128, 1024])
