@@ -11,6 +11,9 @@ namespace w4 {
 
 cudaError_t launch_tc_pair(const TcPlan& plan, const CUtensorMap& amap, const CUtensorMap& smap,
                            const CUtensorMap& zmap, const TcArgs& args, cudaStream_t s) {
+  // one 128-column weight tile per CTA of a pair (the kernel's tile geometry,
+  // a compile-time constant in its LEAN instances)
+  if (plan.nt != 1) return cudaErrorInvalidValue;
   if (W4_PAIR_MMA2) return launch_tc_t<true, true>(plan, amap, smap, zmap, args, s);
   return launch_tc_t<false, true>(plan, amap, smap, zmap, args, s);
 }
