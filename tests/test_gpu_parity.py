@@ -138,7 +138,7 @@ def test_w4a16_several_tiles(gpu_lib, name, zeros, dt):
 
 @pytest.mark.parametrize("M", [256, 1000])
 @pytest.mark.parametrize("name", ["tc128_sk", "tc256_sk", "tc256_dp", "tc128x2_kp", "tc256p_sk",
-                                  "tc256p_dp"])
+                                  "tc256p_dp", "tc128p_sk"])
 def test_w4a16_f16_zero_points_large_m(gpu_lib, name, M):
     """fp16 activations with uint4 + pre-scaled zero-points on the wide
     tensor-core tiles (the large-M path), ragged N, several K groups."""
