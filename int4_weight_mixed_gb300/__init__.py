@@ -277,9 +277,8 @@ def gemm(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
         out_dtype = torch.float16 if a.dtype in (torch.int8, torch.float8_e4m3fn) else a.dtype
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
-    nbytes = workspace_size(M, N, K, a.dtype, group_size)
-    if ws is None:
-        ws = workspace(a.device, nbytes)
+    if ws is None:  # (a given workspace is checked against the plan by the library)
+        ws = workspace(a.device, workspace_size(M, N, K, a.dtype, group_size))
     scale_code = _DTYPE_CODE[scales.dtype] if scales is not None else a_code
     if bias is None:
         st = lib.w4_gemm_ex(_ptr(a), a_code, M, K, _ptr(b_packed), wtype, N, _ptr(scales),
@@ -315,9 +314,8 @@ def gemm_dynamic(a: torch.Tensor, b_packed: torch.Tensor, wtype: int, N: int,
     act = _DTYPE_CODE[act_dtype]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=a.device)
-    nbytes = int(lib.w4_gemm_dynamic_workspace_size(M, N, K, act, group_size))
-    if ws is None:
-        ws = workspace(a.device, nbytes)
+    if ws is None:  # (a given workspace is checked against the plan by the library)
+        ws = workspace(a.device, int(lib.w4_gemm_dynamic_workspace_size(M, N, K, act, group_size)))
     scale_code = _DTYPE_CODE[scales.dtype] if scales is not None else S8
     _check(lib.w4_gemm_dynamic(_ptr(a), _DTYPE_CODE[a.dtype], M, K, _ptr(b_packed), wtype, N,
                                _ptr(scales), scale_code, group_size, _ptr(channel_scales), act,

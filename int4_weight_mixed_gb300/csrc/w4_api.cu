@@ -11,7 +11,9 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <string>
 
 #include "../../include/w4.h"
@@ -674,11 +676,29 @@ size_t w4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int a_type, int64
   pr.has_sg = pr.gs != pr.K;
   size_t need = kWsHeader;
   if (pr.M == 0 || pr.N == 0 || pr.K == 0 || pr.K % kStageK != 0) return need;
+  // Remembered per shape and device (planning every schedule costs tens of
+  // microseconds of host time, and callers ask once per call).
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  const auto key = std::make_tuple(pr.M, pr.N, pr.K, pr.gs, pr.mode, dev);
+  static std::mutex mu;
+  static std::map<decltype(key), size_t> cache;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
   for (int si = 0; si < kNumSchedules; ++si) {
     if (!schedule_fits(si, pr.mode, pr.M, pr.N, pr.K, pr.gs, pr.has_sg)) continue;
     size_t b = ws_needed(si, pr);
     if (b > need) need = b;
   }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 4096) cache.clear();
+  cache.emplace(key, need);
   return need;
 }
 
