@@ -111,7 +111,7 @@ bool schedule_fits(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs
 }
 
 // Build the launch plan of a tc schedule.
-TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) {
+TcPlan make_plan_uncached(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) {
   const Schedule& sc = kSchedules[si];
   TcPlan p{};
   p.mode = mode;
@@ -247,6 +247,30 @@ TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) 
   p.ws_icopy = align256(p.ws_act + act);
   const size_t icopy = p.gicopy ? static_cast<size_t>(p.grid) * dcols * kTileN * 4 : 0;
   p.ws_total = align256(p.ws_icopy + icopy);
+  return p;
+}
+
+// The plan of a tc schedule, remembered per shape and device: a call plans
+// its schedule several times (fit, workspace, launch), each a few
+// microseconds of host time.
+TcPlan make_plan(int si, int mode, int64_t M, int64_t N, int64_t K, int64_t gs) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  const auto key = std::make_tuple(si, mode, M, N, K, gs, dev);
+  static std::mutex mu;
+  static std::map<decltype(key), TcPlan> cache;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const TcPlan p = make_plan_uncached(si, mode, M, N, K, gs);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 4096) cache.clear();
+  cache.emplace(key, p);
   return p;
 }
 
