@@ -621,15 +621,17 @@ def run_gpu(args):
         x0.record(stream)
         h2d_stream.wait_stream(stream)
         d2h_stream.wait_stream(stream)
+        h0 = time.perf_counter()
         for _ in range(e2e_steps):
             e2e_step()
+        host_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps  # enqueueing, on the host
         stream.wait_stream(d2h_stream)  # the last results are back on the host
         x1.record(stream)
         barrier()
         e2e_ms = slowest_rank_ms(x0.elapsed_time(x1) / e2e_steps, world, dev)
         e2e = {"value": job_tflops(sum(flops(M) for M in M_SWEEP), world, e2e_ms),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms, "host_enqueue_ms_per_step": round(host_ms, 4)}
 
     if rank != 0:
         if world > 1:
